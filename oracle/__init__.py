@@ -1,0 +1,47 @@
+"""fp64 CPU oracle of the Krea 2 single-stream DiT block forward.
+
+TEST INFRASTRUCTURE ONLY: imported by ``tests/``, by ``__graft_entry__.smoke()``
+and by the benchmark's CPU-baseline leg, never by the library. It shares no code
+with the CUDA path. Parity pins: every function here is pinned by the CPU tests
+(textbook library routines, closed forms, invariants, brute force on tiny
+inputs); none is "parity unpinned".
+"""
+from __future__ import annotations
+
+from typing import Dict, Optional, Sequence
+
+import numpy as np
+
+from .block import (  # noqa: F401
+    apply_rope_2d,
+    block_forward,
+    gqa_attention,
+    modulation,
+    rms_norm,
+    rope_angles,
+    swiglu,
+    timestep_embedding,
+    timestep_mlp,
+    token_positions,
+    zero_centred_rms_norm,
+)
+
+
+def mod_shared_for(case) -> np.ndarray:
+    """Timestep -> sinusoid -> shared MLP -> mod_shared [B, 6, d] for a seeded case."""
+    e = timestep_embedding(case.t)
+    return timestep_mlp(e, case.temb["w1"], case.temb["b1"], case.temb["w2"], case.temb["b2"])
+
+
+def run_case(case, rows: Optional[Sequence[np.ndarray]] = None, *, rope_on: bool = True,
+             mod_shared: Optional[np.ndarray] = None) -> Dict[str, list]:
+    """Timestep embedding plus one block forward for a seeded case (duck-typed:
+    ``case.cfg`` shapes, ``case.t``, ``case.temb``, ``case.w``, ``case.x_txt``,
+    ``case.x_img``)."""
+    cfg = case.cfg
+    ms = mod_shared_for(case) if mod_shared is None else mod_shared
+    return block_forward(
+        case.x_txt, case.x_img, (cfg.img_h, cfg.img_w), ms, case.w,
+        n_q=cfg.n_q, n_kv=cfg.n_kv, hd=cfg.hd, eps=cfg.eps, rope_base=cfg.rope_base,
+        gate_on=cfg.gate_on, rope_on=rope_on, rows=rows,
+    )
