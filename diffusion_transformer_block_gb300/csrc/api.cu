@@ -1,0 +1,547 @@
+// C ABI of the DiT block library: argument validation, workspace, TMA tensor maps,
+// kernel sequencing, per-kernel timing and device-side failure reporting.
+// The operation and every argument are documented in include/krea_dit.h.
+#include <cudaTypedefs.h>
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include <mutex>
+#include <new>
+#include <vector>
+
+#include "internal.h"
+#include "krea_dit.h"
+
+using kd::Fwd;
+using kd::QkvgDst;
+using kd::RowSrc;
+
+namespace {
+
+// ---- kernel slots (one per logical kernel the library launches) --------------------
+enum Slot {
+  S_NORM1,
+  S_QKVG_TC,
+  S_ATTN,
+  S_OPROJ_TC,
+  S_NORM2,
+  S_UPGATE_TC,
+  S_DOWN_TC,
+  S_QKVG_F32,
+  S_QKVG_POST_F32,
+  S_OPROJ_F32,
+  S_RESID_ATTN_F32,
+  S_GATE_F32,
+  S_UP_F32,
+  S_SWIGLU_F32,
+  S_DOWN_F32,
+  S_RESID_MLP_F32,
+  S_TEMB_SIN,
+  S_TEMB_MLP1,
+  S_TEMB_MLP2,
+  S_COUNT
+};
+const char* const kSlotNames[S_COUNT] = {
+    "norm1_modulate",       "qkvg_gemm_qknorm_rope", "attention_gate",  "oproj_gemm_residual",
+    "norm2_modulate",       "upgate_gemm_swiglu",    "down_gemm_residual", "qkvg_gemm_f32",
+    "qkvg_qknorm_rope_f32", "oproj_gemm_f32",        "residual_attn_f32", "gate_gemm_f32",
+    "up_gemm_f32",          "swiglu_f32",            "down_gemm_f32",   "residual_mlp_f32",
+    "temb_sinusoid",        "temb_mlp1",             "temb_mlp2"};
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+bool get_encode() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  return g_encode != nullptr;
+}
+
+// 2D bf16 tensor map over a row-major [rows, cols] matrix with pitch `pitch_elems`,
+// box = box_cols x box_rows, 128-byte swizzle, zero fill outside the matrix.
+bool encode_2d(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint64_t pitch_elems,
+               uint32_t box_cols, uint32_t box_rows) {
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {pitch_elems * 2};
+  cuuint32_t box[2] = {box_cols, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 3D bf16 tensor map over [planes, rows, cols] (cols contiguous, pitch `pitch_elems`).
+bool encode_3d(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint64_t planes,
+               uint64_t pitch_elems, uint32_t box_cols, uint32_t box_rows) {
+  cuuint64_t dims[3] = {cols, rows, planes};
+  cuuint64_t strides[2] = {pitch_elems * 2, pitch_elems * 2 * rows};
+  cuuint32_t box[3] = {box_cols, box_rows, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+  if (!a || !b || !na || !nb) return false;
+  const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+  return a0 < b0 + nb && b0 < a0 + na;
+}
+
+struct TimedLaunch {
+  int slot;
+  cudaEvent_t begin, end;
+};
+
+}  // namespace
+
+struct krea_dit_block_s {
+  krea_dit_config cfg{};
+  int device = 0, num_sms = 0;
+  bool bf16 = true;
+  size_t esz = 2;
+  size_t max_T = 0;
+  int n_qkvg = 0;
+  int rope_rows = 0;
+  // one device allocation, carved into the buffers below
+  char* ws = nullptr;
+  size_t ws_bytes = 0;
+  void *xn = nullptr, *q = nullptr, *k = nullptr, *vt = nullptr, *g = nullptr, *og = nullptr, *h1 = nullptr,
+       *hn = nullptr, *hmid = nullptr;
+  size_t sz_xn = 0, sz_q = 0, sz_k = 0, sz_vt = 0, sz_g = 0, sz_og = 0, sz_h1 = 0, sz_hn = 0, sz_hmid = 0;
+  float *raw_qkvg = nullptr, *raw_o = nullptr, *raw_a = nullptr, *raw_u = nullptr, *raw_down = nullptr;
+  float *temb_e = nullptr, *temb_h = nullptr;
+  float2* rope = nullptr;
+  int* err = nullptr;
+  Fwd last{};
+  bool have_last = false;
+  // timing
+  bool timing = false;
+  std::vector<cudaEvent_t> free_events;
+  std::vector<TimedLaunch> pending;
+  double total_ms[S_COUNT] = {};
+  int launches[S_COUNT] = {};
+  int inject = 0;
+};
+
+namespace {
+
+int harvest(krea_dit_block_s* h) {
+  for (auto& t : h->pending) {
+    if (cudaEventSynchronize(t.end) != cudaSuccess) return KREA_DIT_ERR_CUDA;
+    float ms = 0.f;
+    if (cudaEventElapsedTime(&ms, t.begin, t.end) != cudaSuccess) return KREA_DIT_ERR_CUDA;
+    h->total_ms[t.slot] += ms;
+    h->launches[t.slot] += 1;
+    h->free_events.push_back(t.begin);
+    h->free_events.push_back(t.end);
+  }
+  h->pending.clear();
+  return KREA_DIT_OK;
+}
+
+cudaEvent_t take_event(krea_dit_block_s* h) {
+  if (h->free_events.empty()) {
+    if (h->pending.size() >= 4096) harvest(h);  // bound the number of live events
+  }
+  if (!h->free_events.empty()) {
+    cudaEvent_t e = h->free_events.back();
+    h->free_events.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+  return e;
+}
+
+// Runs one launch; when timing is on, brackets it with events on `st`.
+template <class F>
+cudaError_t timed(krea_dit_block_s* h, int slot, cudaStream_t st, F&& launch) {
+  if (!h->timing) return launch();
+  cudaEvent_t b = take_event(h), e = take_event(h);
+  if (!b || !e) return cudaErrorMemoryAllocation;
+  cudaEventRecord(b, st);
+  cudaError_t r = launch();
+  cudaEventRecord(e, st);
+  h->pending.push_back({slot, b, e});
+  return r;
+}
+
+bool sm103_current(int* dev, int* sms) {
+  if (cudaGetDevice(dev) != cudaSuccess) return false;
+  int major = 0, minor = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, *dev) != cudaSuccess) return false;
+  if (cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, *dev) != cudaSuccess) return false;
+  if (cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, *dev) != cudaSuccess) return false;
+  return major == 10 && minor == 3;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* krea_dit_status_string(int s) {
+  switch (s) {
+    case KREA_DIT_OK: return "ok";
+    case KREA_DIT_ERR_INVALID_ARG: return "invalid argument";
+    case KREA_DIT_ERR_UNSUPPORTED_SHAPE: return "unsupported shape";
+    case KREA_DIT_ERR_MISALIGNED: return "device pointer not 16-byte aligned";
+    case KREA_DIT_ERR_EXCEEDS_CREATE_LIMITS: return "call exceeds the limits the handle was created with";
+    case KREA_DIT_ERR_CUDA: return "CUDA runtime or driver error";
+    case KREA_DIT_ERR_NO_DEVICE: return "current device is not an sm_103 GPU";
+    case KREA_DIT_ERR_DEVICE_TIMEOUT: return "a bounded on-device wait expired";
+    case KREA_DIT_ERR_INJECTED: return "injected fault";
+    default: return "unknown status";
+  }
+}
+
+int krea_dit_kernel_names(const char** names, int cap) {
+  for (int i = 0; i < S_COUNT && i < cap; ++i)
+    if (names) names[i] = kSlotNames[i];
+  return S_COUNT;
+}
+
+int krea_dit_block_create(const krea_dit_config* c, krea_dit_block_t* out) {
+  if (!out) return KREA_DIT_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (!c) return KREA_DIT_ERR_INVALID_ARG;
+  if (c->mode != KREA_DIT_BF16 && c->mode != KREA_DIT_FP32) return KREA_DIT_ERR_INVALID_ARG;
+  if (c->max_batch < 1 || c->max_seq < 1 || c->img_h_max < 0 || c->img_w_max < 0) return KREA_DIT_ERR_INVALID_ARG;
+  if (!(c->eps > 0.f) || !(c->rope_base > 0.f) || (c->gate_on != 0 && c->gate_on != 1))
+    return KREA_DIT_ERR_INVALID_ARG;
+  if (c->d_model <= 0 || c->n_q <= 0 || c->n_kv <= 0 || c->ffn <= 0) return KREA_DIT_ERR_INVALID_ARG;
+  if (c->d_model % 64 || c->ffn % 64 || c->n_q % c->n_kv) return KREA_DIT_ERR_UNSUPPORTED_SHAPE;
+  if (c->head_dim != 64 && c->head_dim != 128) return KREA_DIT_ERR_UNSUPPORTED_SHAPE;
+  if (c->mode == KREA_DIT_BF16 && c->head_dim != 128) return KREA_DIT_ERR_UNSUPPORTED_SHAPE;
+  // 32-bit index arithmetic inside the kernels
+  const double big = static_cast<double>(c->max_batch) * c->max_seq *
+                     (c->ffn > (2 * c->n_q + 2 * c->n_kv) * c->head_dim ? c->ffn
+                                                                          : (2 * c->n_q + 2 * c->n_kv) * c->head_dim);
+  if (static_cast<double>(c->max_batch) * c->max_seq > 2147483647.0 || big > 9.0e15)
+    return KREA_DIT_ERR_UNSUPPORTED_SHAPE;
+
+  int dev = 0, sms = 0;
+  if (!sm103_current(&dev, &sms)) return KREA_DIT_ERR_NO_DEVICE;
+
+  krea_dit_block_s* h = new (std::nothrow) krea_dit_block_s();
+  if (!h) return KREA_DIT_ERR_CUDA;
+  h->cfg = *c;
+  h->device = dev;
+  h->num_sms = sms;
+  h->bf16 = c->mode == KREA_DIT_BF16;
+  h->esz = h->bf16 ? 2 : 4;
+  h->max_T = static_cast<size_t>(c->max_batch) * c->max_seq;
+  h->n_qkvg = ((c->gate_on ? 2 : 1) * c->n_q + 2 * c->n_kv) * c->head_dim;
+  h->rope_rows = c->img_h_max > c->img_w_max ? c->img_h_max : c->img_w_max;
+  if (h->rope_rows < 1) h->rope_rows = 1;
+
+  const size_t T = h->max_T, d = c->d_model, hd = c->head_dim, F = c->ffn, es = h->esz;
+  const size_t Lp = round_up(static_cast<size_t>(c->max_seq), 64);
+  struct Item {
+    void** p;
+    size_t bytes;
+    size_t* sz;
+  };
+  h->sz_xn = T * d * es;
+  h->sz_q = T * c->n_q * hd * es;
+  h->sz_k = T * c->n_kv * hd * es;
+  h->sz_vt = static_cast<size_t>(c->max_batch) * c->n_kv * hd * Lp * es;
+  h->sz_g = T * c->n_q * hd * es;
+  h->sz_og = T * c->n_q * hd * es;
+  h->sz_h1 = T * d * es;
+  h->sz_hn = T * d * es;
+  h->sz_hmid = T * F * es;
+  std::vector<Item> items = {
+      {&h->xn, h->sz_xn, nullptr},  {&h->q, h->sz_q, nullptr},   {&h->k, h->sz_k, nullptr},
+      {&h->vt, h->sz_vt, nullptr},  {&h->g, h->sz_g, nullptr},   {&h->og, h->sz_og, nullptr},
+      {&h->h1, h->sz_h1, nullptr},  {&h->hn, h->sz_hn, nullptr}, {&h->hmid, h->sz_hmid, nullptr},
+  };
+  if (!h->bf16) {
+    items.push_back({reinterpret_cast<void**>(&h->raw_qkvg), T * h->n_qkvg * 4, nullptr});
+    items.push_back({reinterpret_cast<void**>(&h->raw_o), T * d * 4, nullptr});
+    items.push_back({reinterpret_cast<void**>(&h->raw_a), T * F * 4, nullptr});
+    items.push_back({reinterpret_cast<void**>(&h->raw_u), T * F * 4, nullptr});
+    items.push_back({reinterpret_cast<void**>(&h->raw_down), T * d * 4, nullptr});
+  }
+  items.push_back({reinterpret_cast<void**>(&h->temb_e), static_cast<size_t>(c->max_batch) * 256 * 4, nullptr});
+  items.push_back({reinterpret_cast<void**>(&h->temb_h), static_cast<size_t>(c->max_batch) * d * 4, nullptr});
+  items.push_back({reinterpret_cast<void**>(&h->rope), static_cast<size_t>(h->rope_rows) * (hd / 4) * 8, nullptr});
+  items.push_back({reinterpret_cast<void**>(&h->err), 256, nullptr});
+  size_t total = 0;
+  for (auto& it : items) total += round_up(it.bytes, 256);
+  if (cudaMalloc(&h->ws, total) != cudaSuccess) {
+    delete h;
+    return KREA_DIT_ERR_CUDA;
+  }
+  h->ws_bytes = total;
+  size_t off = 0;
+  for (auto& it : items) {
+    *it.p = h->ws + off;
+    off += round_up(it.bytes, 256);
+  }
+  // zero the workspace once so padded V^T columns are finite from the first call
+  if (cudaMemset(h->ws, 0, total) != cudaSuccess) {
+    cudaFree(h->ws);
+    delete h;
+    return KREA_DIT_ERR_CUDA;
+  }
+  // RoPE table: (cos, sin) of pos * base^(-2j/D), D = hd/2, j < hd/4, computed in double.
+  {
+    const int Q = c->head_dim / 4;
+    const double D = c->head_dim / 2;
+    std::vector<float2> tab(static_cast<size_t>(h->rope_rows) * Q);
+    for (int p = 0; p < h->rope_rows; ++p)
+      for (int j = 0; j < Q; ++j) {
+        const double ang = p * pow(static_cast<double>(c->rope_base), -2.0 * j / D);
+        tab[static_cast<size_t>(p) * Q + j] = make_float2(static_cast<float>(cos(ang)), static_cast<float>(sin(ang)));
+      }
+    if (cudaMemcpy(h->rope, tab.data(), tab.size() * sizeof(float2), cudaMemcpyHostToDevice) != cudaSuccess) {
+      cudaFree(h->ws);
+      delete h;
+      return KREA_DIT_ERR_CUDA;
+    }
+  }
+  if (h->bf16) {
+    if (!get_encode() || kd::gemm_tc_init() != cudaSuccess) {
+      cudaFree(h->ws);
+      delete h;
+      return KREA_DIT_ERR_CUDA;
+    }
+  }
+  *out = h;
+  return KREA_DIT_OK;
+}
+
+int krea_dit_block_destroy(krea_dit_block_t h) {
+  if (!h) return KREA_DIT_OK;
+  cudaDeviceSynchronize();
+  harvest(h);
+  for (auto e : h->free_events) cudaEventDestroy(e);
+  cudaError_t r = cudaFree(h->ws);
+  delete h;
+  return r == cudaSuccess ? KREA_DIT_OK : KREA_DIT_ERR_CUDA;
+}
+
+int krea_dit_timestep_embed(krea_dit_block_t h, const float* t, int B, const krea_dit_temb_weights* w,
+                            float* mod_shared, krea_dit_stream_t stream) {
+  if (!h || !t || !w || !mod_shared || !w->w1 || !w->b1 || !w->w2 || !w->b2) return KREA_DIT_ERR_INVALID_ARG;
+  if (B < 0) return KREA_DIT_ERR_INVALID_ARG;
+  if (B > h->cfg.max_batch) return KREA_DIT_ERR_EXCEEDS_CREATE_LIMITS;
+  if (!aligned16(t) || !aligned16(mod_shared) || !aligned16(w->w1) || !aligned16(w->b1) || !aligned16(w->w2) ||
+      !aligned16(w->b2))
+    return KREA_DIT_ERR_MISALIGNED;
+  if (B == 0) return KREA_DIT_OK;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const int d = h->cfg.d_model;
+  cudaError_t e;
+  e = timed(h, S_TEMB_SIN, st, [&] { return kd::launch_temb_sinusoid(t, B, h->temb_e, st); });
+  if (e == cudaSuccess)
+    e = timed(h, S_TEMB_MLP1, st,
+              [&] { return kd::launch_gemm_simt_f32(h->temb_e, w->w1, h->temb_h, B, d, 256, w->b1, 1, st); });
+  if (e == cudaSuccess)
+    e = timed(h, S_TEMB_MLP2, st,
+              [&] { return kd::launch_gemm_simt_f32(h->temb_h, w->w2, mod_shared, B, 6 * d, d, w->b2, 0, st); });
+  return e == cudaSuccess ? KREA_DIT_OK : KREA_DIT_ERR_CUDA;
+}
+
+int krea_dit_block_forward(krea_dit_block_t h, const void* x_img, const void* x_txt, int B, int img_h, int img_w,
+                           int n_txt, const float* t_emb, const krea_dit_weights* w, void* out,
+                           krea_dit_stream_t stream) {
+  if (!h || !w || !t_emb || !out) return KREA_DIT_ERR_INVALID_ARG;
+  if (B < 0 || img_h < 0 || img_w < 0 || n_txt < 0) return KREA_DIT_ERR_INVALID_ARG;
+  if (!w->w_qkvg || !w->w_o || !w->w_gate || !w->w_up || !w->w_down || !w->norm1_w || !w->norm2_w ||
+      !w->q_norm_w || !w->k_norm_w || !w->mod_bias)
+    return KREA_DIT_ERR_INVALID_ARG;
+  const krea_dit_config& c = h->cfg;
+  const long long n_img_ll = static_cast<long long>(img_h) * img_w;
+  const long long L_ll = n_img_ll + n_txt;
+  if (B > c.max_batch || L_ll > c.max_seq || (n_img_ll > 0 && (img_h > c.img_h_max || img_w > c.img_w_max)))
+    return KREA_DIT_ERR_EXCEEDS_CREATE_LIMITS;
+  const int n_img = static_cast<int>(n_img_ll), L = static_cast<int>(L_ll);
+  if ((n_img > 0 && !x_img) || (n_txt > 0 && !x_txt)) return KREA_DIT_ERR_INVALID_ARG;
+  const void* ptrs[] = {w->w_qkvg, w->w_o,     w->w_gate,   w->w_up,     w->w_down, w->norm1_w, w->norm2_w,
+                        w->q_norm_w, w->k_norm_w, w->mod_bias, t_emb, out};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return KREA_DIT_ERR_MISALIGNED;
+  if ((x_img && !aligned16(x_img)) || (x_txt && !aligned16(x_txt))) return KREA_DIT_ERR_MISALIGNED;
+  const size_t es = h->esz, d = c.d_model;
+  const size_t out_bytes = static_cast<size_t>(B) * L * d * es;
+  if (overlaps(out, out_bytes, x_img, static_cast<size_t>(B) * n_img * d * es) ||
+      overlaps(out, out_bytes, x_txt, static_cast<size_t>(B) * n_txt * d * es) ||
+      overlaps(out, out_bytes, t_emb, static_cast<size_t>(B) * 6 * d * 4))
+    return KREA_DIT_ERR_INVALID_ARG;
+  if (B == 0 || L == 0) return KREA_DIT_OK;
+  if (h->inject > 0) {
+    --h->inject;
+    return KREA_DIT_ERR_INJECTED;
+  }
+
+  Fwd f{};
+  f.B = B;
+  f.L = L;
+  f.n_txt = n_txt;
+  f.n_img = n_img;
+  f.img_w = img_w > 0 ? img_w : 1;
+  f.T = B * L;
+  f.Lp = static_cast<int>(round_up(static_cast<size_t>(L), 64));
+  f.d = c.d_model;
+  f.n_q = c.n_q;
+  f.n_kv = c.n_kv;
+  f.hd = c.head_dim;
+  f.F = c.ffn;
+  f.gate_on = c.gate_on;
+  f.eps = c.eps;
+  h->last = f;
+  h->have_last = true;
+
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const RowSrc xsrc{x_txt, x_img, nullptr};
+  const RowSrc h1src{nullptr, nullptr, h->h1};
+  const QkvgDst dst{h->q, h->k, h->vt, h->g, w->q_norm_w, w->k_norm_w, h->rope};
+  const int nqhd = c.n_q * c.head_dim;
+  cudaError_t e = cudaSuccess;
+#define KD_RUN(slot, expr)                                 \
+  do {                                                     \
+    if (e == cudaSuccess) e = timed(h, slot, st, [&] { return (expr); }); \
+  } while (0)
+
+  if (h->bf16) {
+    CUtensorMap tm_xn, tm_wqkvg, tm_og, tm_wo, tm_hn, tm_wgate, tm_wup, tm_hmid, tm_wdown, tm_q, tm_k, tm_vt;
+    const uint64_t T = static_cast<uint64_t>(f.T);
+    bool ok = encode_2d(&tm_xn, h->xn, d, T, d, 64, 128) &&
+              encode_2d(&tm_wqkvg, w->w_qkvg, d, h->n_qkvg, d, 64, 256) &&
+              encode_2d(&tm_og, h->og, nqhd, T, nqhd, 64, 128) &&
+              encode_2d(&tm_wo, w->w_o, nqhd, d, nqhd, 64, 256) && encode_2d(&tm_hn, h->hn, d, T, d, 64, 128) &&
+              encode_2d(&tm_wgate, w->w_gate, d, c.ffn, d, 64, 128) &&
+              encode_2d(&tm_wup, w->w_up, d, c.ffn, d, 64, 128) &&
+              encode_2d(&tm_hmid, h->hmid, c.ffn, T, c.ffn, 64, 128) &&
+              encode_2d(&tm_wdown, w->w_down, c.ffn, d, c.ffn, 64, 256) &&
+              encode_3d(&tm_q, h->q, c.head_dim, L, static_cast<uint64_t>(B) * c.n_q, c.head_dim, 64, 128) &&
+              encode_3d(&tm_k, h->k, c.head_dim, L, static_cast<uint64_t>(B) * c.n_kv, c.head_dim, 64, 128) &&
+              encode_3d(&tm_vt, h->vt, L, c.head_dim, static_cast<uint64_t>(B) * c.n_kv, f.Lp, 64, 128);
+    if (!ok) return KREA_DIT_ERR_CUDA;
+    const int sms = h->num_sms;
+    KD_RUN(S_NORM1, kd::launch_norm_modulate(true, f, xsrc, w->norm1_w, t_emb, w->mod_bias, 0, 1, h->xn, st));
+    KD_RUN(S_QKVG_TC, kd::launch_gemm_qkvg(f, &tm_xn, &tm_wqkvg, h->n_qkvg, dst, sms, h->err, st));
+    KD_RUN(S_ATTN, kd::launch_attn_simt(true, f, h->q, h->k, h->vt, h->g, h->og, st));
+    (void)tm_q; (void)tm_k; (void)tm_vt;
+    KD_RUN(S_OPROJ_TC, kd::launch_gemm_resid(f, &tm_og, &tm_wo, nqhd, xsrc, t_emb, w->mod_bias, 2, h->h1, sms,
+                                             h->err, st));
+    KD_RUN(S_NORM2, kd::launch_norm_modulate(true, f, h1src, w->norm2_w, t_emb, w->mod_bias, 3, 4, h->hn, st));
+    KD_RUN(S_UPGATE_TC, kd::launch_gemm_swiglu(f, &tm_hn, &tm_wgate, &tm_wup, h->hmid, sms, h->err, st));
+    KD_RUN(S_DOWN_TC, kd::launch_gemm_resid(f, &tm_hmid, &tm_wdown, c.ffn, h1src, t_emb, w->mod_bias, 5, out, sms,
+                                            h->err, st));
+  } else {
+    const int T = f.T;
+    const float* wq = static_cast<const float*>(w->w_qkvg);
+    KD_RUN(S_NORM1, kd::launch_norm_modulate(false, f, xsrc, w->norm1_w, t_emb, w->mod_bias, 0, 1, h->xn, st));
+    KD_RUN(S_QKVG_F32, kd::launch_gemm_simt_f32(static_cast<const float*>(h->xn), wq, h->raw_qkvg, T, h->n_qkvg,
+                                                c.d_model, nullptr, 0, st));
+    KD_RUN(S_QKVG_POST_F32, kd::launch_qkvg_post_f32(f, h->raw_qkvg, dst, st));
+    KD_RUN(S_ATTN, kd::launch_attn_simt(false, f, h->q, h->k, h->vt, h->g, h->og, st));
+    KD_RUN(S_OPROJ_F32, kd::launch_gemm_simt_f32(static_cast<const float*>(h->og), static_cast<const float*>(w->w_o),
+                                                 h->raw_o, T, c.d_model, nqhd, nullptr, 0, st));
+    KD_RUN(S_RESID_ATTN_F32, kd::launch_residual_f32(f, xsrc, h->raw_o, t_emb, w->mod_bias, 2,
+                                                     static_cast<float*>(h->h1), st));
+    KD_RUN(S_NORM2, kd::launch_norm_modulate(false, f, h1src, w->norm2_w, t_emb, w->mod_bias, 3, 4, h->hn, st));
+    KD_RUN(S_GATE_F32, kd::launch_gemm_simt_f32(static_cast<const float*>(h->hn),
+                                                static_cast<const float*>(w->w_gate), h->raw_a, T, c.ffn, c.d_model,
+                                                nullptr, 0, st));
+    KD_RUN(S_UP_F32, kd::launch_gemm_simt_f32(static_cast<const float*>(h->hn), static_cast<const float*>(w->w_up),
+                                              h->raw_u, T, c.ffn, c.d_model, nullptr, 0, st));
+    KD_RUN(S_SWIGLU_F32, kd::launch_swiglu_f32(f, h->raw_a, h->raw_u, static_cast<float*>(h->hmid), st));
+    KD_RUN(S_DOWN_F32, kd::launch_gemm_simt_f32(static_cast<const float*>(h->hmid),
+                                                static_cast<const float*>(w->w_down), h->raw_down, T, c.d_model,
+                                                c.ffn, nullptr, 0, st));
+    KD_RUN(S_RESID_MLP_F32,
+           kd::launch_residual_f32(f, h1src, h->raw_down, t_emb, w->mod_bias, 5, static_cast<float*>(out), st));
+  }
+#undef KD_RUN
+  return e == cudaSuccess ? KREA_DIT_OK : KREA_DIT_ERR_CUDA;
+}
+
+int krea_dit_block_workspace(krea_dit_block_t h, int which, void** dev_ptr, size_t* bytes) {
+  if (!h || !dev_ptr || !bytes) return KREA_DIT_ERR_INVALID_ARG;
+  const Fwd& f = h->last;
+  const size_t es = h->esz;
+  const size_t T = h->have_last ? static_cast<size_t>(f.T) : 0;
+  const size_t hd = h->cfg.head_dim;
+  switch (which) {
+    case KREA_DIT_BUF_XN: *dev_ptr = h->xn; *bytes = T * h->cfg.d_model * es; break;
+    case KREA_DIT_BUF_Q: *dev_ptr = h->q; *bytes = T * h->cfg.n_q * hd * es; break;
+    case KREA_DIT_BUF_K: *dev_ptr = h->k; *bytes = T * h->cfg.n_kv * hd * es; break;
+    case KREA_DIT_BUF_VT:
+      *dev_ptr = h->vt;
+      *bytes = h->have_last ? static_cast<size_t>(f.B) * h->cfg.n_kv * hd * f.Lp * es : 0;
+      break;
+    case KREA_DIT_BUF_G: *dev_ptr = h->g; *bytes = T * h->cfg.n_q * hd * es; break;
+    case KREA_DIT_BUF_OG: *dev_ptr = h->og; *bytes = T * h->cfg.n_q * hd * es; break;
+    case KREA_DIT_BUF_H1: *dev_ptr = h->h1; *bytes = T * h->cfg.d_model * es; break;
+    case KREA_DIT_BUF_HN: *dev_ptr = h->hn; *bytes = T * h->cfg.d_model * es; break;
+    case KREA_DIT_BUF_HMID: *dev_ptr = h->hmid; *bytes = T * h->cfg.ffn * es; break;
+    default: return KREA_DIT_ERR_INVALID_ARG;
+  }
+  return KREA_DIT_OK;
+}
+
+int krea_dit_block_set_timing(krea_dit_block_t h, int enable) {
+  if (!h) return KREA_DIT_ERR_INVALID_ARG;
+  h->timing = enable != 0;
+  return KREA_DIT_OK;
+}
+
+int krea_dit_block_timing_reset(krea_dit_block_t h) {
+  if (!h) return KREA_DIT_ERR_INVALID_ARG;
+  int r = harvest(h);
+  for (int i = 0; i < S_COUNT; ++i) {
+    h->total_ms[i] = 0.0;
+    h->launches[i] = 0;
+  }
+  return r;
+}
+
+int krea_dit_block_kernel_times(krea_dit_block_t h, const char** names, double* total_ms, int* launches, int cap,
+                                int* n) {
+  if (!h || !n) return KREA_DIT_ERR_INVALID_ARG;
+  int r = harvest(h);
+  for (int i = 0; i < S_COUNT && i < cap; ++i) {
+    if (names) names[i] = kSlotNames[i];
+    if (total_ms) total_ms[i] = h->total_ms[i];
+    if (launches) launches[i] = h->launches[i];
+  }
+  *n = S_COUNT;
+  return r;
+}
+
+int krea_dit_block_device_status(krea_dit_block_t h, krea_dit_stream_t stream, int* site) {
+  if (!h || !site) return KREA_DIT_ERR_INVALID_ARG;
+  *site = 0;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(st) != cudaSuccess) return KREA_DIT_ERR_CUDA;
+  int word = 0;
+  if (cudaMemcpy(&word, h->err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return KREA_DIT_ERR_CUDA;
+  if (word) {
+    *site = word;
+    if (cudaMemset(h->err, 0, sizeof(int)) != cudaSuccess) return KREA_DIT_ERR_CUDA;
+    return KREA_DIT_ERR_DEVICE_TIMEOUT;
+  }
+  return KREA_DIT_OK;
+}
+
+int krea_dit_block_inject_fault(krea_dit_block_t h, int count) {
+  if (!h || count < 0) return KREA_DIT_ERR_INVALID_ARG;
+  h->inject = count;
+  return KREA_DIT_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,433 @@
+// Tensor-core GEMMs of the DiT block (bf16 in, fp32 accumulate), tcgen05 + TMA, sm_103a.
+//
+// One persistent, warp-specialised kernel template with three fused epilogues:
+//   * QKVG  : xn W_qkvg^T -> per-head QK-RMSNorm, 2D axial RoPE, scatter to Q, K, V^T, G
+//             (Krea 2 Technical Report, "Transformer block", "Positional encoding",
+//             "Normalisation")
+//   * RESID : out = res + gate * (A W^T)   -- attention output projection and the MLP
+//             down projection, each with its gated residual ("Residual design",
+//             "Timestep conditioning")
+//   * SWIGLU: silu(hn W_gate^T) * (hn W_up^T), both products in one 128x256 accumulator
+//             ("Transformer block": SwiGLU MLP)
+//
+// Tile 128 x 256 x 64: A tile 16 KB + B tile 32 KB per stage, 4 stages in shared memory,
+// written by TMA with the 128-byte swizzle. The accumulator is double-buffered in TMEM
+// (2 x 256 columns), so the epilogue of one tile overlaps the main loop of the next.
+// Warp roles: warp 0 = TMA producer (one thread), warp 1 = TMEM allocator + MMA issuer
+// (one thread), warps 2..9 = epilogue (two warpgroups, one per 128-column half).
+#include "common.cuh"
+#include "internal.h"
+
+namespace kd {
+namespace {
+
+constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;
+constexpr int B_BYTES = BN * BK * 2;
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int TMEM_COLS = 2 * BN;
+constexpr int NUM_EPI_WARPS = 8;
+constexpr int NUM_THREADS = 64 + NUM_EPI_WARPS * 32;
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*alignment slack*/ + 256 /*barriers*/;
+constexpr int GROUP_M = 16;  // tile raster: GROUP_M m-blocks share each n-block in turn
+
+__device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int& mb, int& nb) {
+  const int per_group = GROUP_M * num_n;
+  const int group = tile / per_group;
+  const int first_m = group * GROUP_M;
+  const int gsize = min(num_m - first_m, GROUP_M);
+  const int r = tile - group * per_group;
+  mb = first_m + r % gsize;
+  nb = r / gsize;
+}
+
+// Wait used while tearing down: ignores the abort flag, still bounded.
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, int* err, int site) {
+  const unsigned long long t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      atomicOr(err, site);
+      return;
+    }
+  }
+}
+
+__device__ __forceinline__ float u2f(uint32_t u) { return __uint_as_float(u); }
+
+// ------------------------------------------------------------------ epilogues
+// apply(): called by one epilogue warp for its 32 rows (one per lane) and one 128-column
+// half of the 256-column accumulator. `taddr` = TMEM address of the lane's row at
+// accumulator column 0. TMEM loads are warp-collective; stores are masked by row < M.
+
+struct EpiQKVG {
+  Fwd f;
+  QkvgDst dst;
+  int N;  // rows of W_qkvg
+  __device__ __forceinline__ void apply(int row, int nb, int half, uint32_t taddr, int M) const {
+    constexpr int HD = 128;
+    const int n0 = nb * BN + half * HD;
+    if (n0 >= N) return;
+    const bool ok = row < M;
+    const int seg = n0 / HD;
+    int kind, head;
+    if (seg < f.n_q) { kind = 0; head = seg; }
+    else if (seg < f.n_q + f.n_kv) { kind = 1; head = seg - f.n_q; }
+    else if (seg < f.n_q + 2 * f.n_kv) { kind = 2; head = seg - f.n_q - f.n_kv; }
+    else { kind = 3; head = seg - f.n_q - 2 * f.n_kv; }
+    const int b = ok ? row / f.L : 0;
+    const int l = ok ? row - b * f.L : 0;
+    const uint32_t t0 = taddr + half * HD;
+    uint32_t r[32];
+
+    if (kind <= 1) {
+      float ss = 0.f;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        tmem_ld32(t0 + c * 32, r);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) ss = fmaf(u2f(r[i]), u2f(r[i]), ss);
+      }
+      const float rstd = 1.0f / sqrtf(ss * (1.0f / HD) + f.eps);
+      const float* w = kind == 0 ? dst.q_norm_w : dst.k_norm_w;
+      const bool img = ok && l >= f.n_txt;
+      int pr = 0, pc = 0;
+      if (img) {
+        const int n = l - f.n_txt;
+        pr = n / f.img_w;
+        pc = n - pr * f.img_w;
+      }
+      const int nh = kind == 0 ? f.n_q : f.n_kv;
+      bf16* out = reinterpret_cast<bf16*>(kind == 0 ? dst.q : dst.k) +
+                  ((static_cast<size_t>(b) * nh + head) * f.L + l) * HD;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        tmem_ld32(t0 + c * 32, r);
+        float v[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = u2f(r[i]) * rstd * (1.0f + __ldg(w + c * 32 + i));
+        if (img) {
+          // chunk c holds pairs 16c .. 16c+15; pairs 0..31 turn with the row, 32..63 with the column
+          const float2* tab = dst.rope + (c < 2 ? pr : pc) * (HD / 4) + (c & 1) * 16;
+#pragma unroll
+          for (int p = 0; p < 16; ++p) {
+            const float2 cs = __ldg(tab + p);
+            const float a = v[2 * p], bb = v[2 * p + 1];
+            v[2 * p] = a * cs.x - bb * cs.y;
+            v[2 * p + 1] = a * cs.y + bb * cs.x;
+          }
+        }
+        if (ok) {
+          uint4* o4 = reinterpret_cast<uint4*>(out + c * 32);
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4)
+            o4[q4] = make_uint4(pack_bf16x2(v[8 * q4 + 0], v[8 * q4 + 1]), pack_bf16x2(v[8 * q4 + 2], v[8 * q4 + 3]),
+                                pack_bf16x2(v[8 * q4 + 4], v[8 * q4 + 5]), pack_bf16x2(v[8 * q4 + 6], v[8 * q4 + 7]));
+        }
+      }
+    } else if (kind == 2) {
+      // V^T [B, n_kv, hd, Lp]: lanes hold consecutive tokens, so each channel's 32 values
+      // from a warp land in one contiguous 64-byte run.
+      bf16* vt = reinterpret_cast<bf16*>(dst.vt) + (static_cast<size_t>(b) * f.n_kv + head) * HD * f.Lp + l;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        tmem_ld32(t0 + c * 32, r);
+        if (ok) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) vt[static_cast<size_t>(c * 32 + i) * f.Lp] = __float2bfloat16_rn(u2f(r[i]));
+        }
+      }
+    } else {
+      bf16* g = reinterpret_cast<bf16*>(dst.g) + static_cast<size_t>(row) * (f.n_q * HD) + head * HD;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        tmem_ld32(t0 + c * 32, r);
+        if (ok) {
+          uint4* o4 = reinterpret_cast<uint4*>(g + c * 32);
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4)
+            o4[q4] = make_uint4(pack_bf16x2(u2f(r[8 * q4 + 0]), u2f(r[8 * q4 + 1])),
+                                pack_bf16x2(u2f(r[8 * q4 + 2]), u2f(r[8 * q4 + 3])),
+                                pack_bf16x2(u2f(r[8 * q4 + 4]), u2f(r[8 * q4 + 5])),
+                                pack_bf16x2(u2f(r[8 * q4 + 6]), u2f(r[8 * q4 + 7])));
+        }
+      }
+    }
+  }
+};
+
+struct EpiResid {
+  Fwd f;
+  RowSrc res;
+  const float* mod_shared;
+  const float* mod_bias;
+  int chunk;  // modulation chunk of the gate (2 = gate_a, 5 = gate_m)
+  bf16* out;  // [T, d]
+  __device__ __forceinline__ void apply(int row, int nb, int half, uint32_t taddr, int M) const {
+    const int N = f.d;
+    const int n0 = nb * BN + half * 128;
+    if (n0 >= N) return;
+    const bool ok = row < M;
+    const int b = ok ? row / f.L : 0;
+    const bf16* x = ok ? row_src_ptr<bf16>(res, row, f.L, f.n_txt, f.n_img, f.d) : nullptr;
+    const float* gs = mod_shared + (static_cast<size_t>(b) * 6 + chunk) * N;
+    const float* gb = mod_bias + static_cast<size_t>(chunk) * N;
+    uint32_t r[32];
+#pragma unroll 1
+    for (int c = 0; c < 4; ++c) {
+      const int col = n0 + c * 32;
+      if (col >= N) break;
+      tmem_ld32(taddr + half * 128 + c * 32, r);
+      if (ok) {
+        const uint4* x4 = reinterpret_cast<const uint4*>(x + col);
+        const float4* gs4 = reinterpret_cast<const float4*>(gs + col);
+        const float4* gb4 = reinterpret_cast<const float4*>(gb + col);
+        uint4* o4 = reinterpret_cast<uint4*>(out + static_cast<size_t>(row) * N + col);
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          const uint4 xv = x4[q4];
+          const float4 s0 = __ldg(gs4 + 2 * q4), s1 = __ldg(gs4 + 2 * q4 + 1);
+          const float4 b0 = __ldg(gb4 + 2 * q4), b1 = __ldg(gb4 + 2 * q4 + 1);
+          const float gt[8] = {s0.x + b0.x, s0.y + b0.y, s0.z + b0.z, s0.w + b0.w,
+                               s1.x + b1.x, s1.y + b1.y, s1.z + b1.z, s1.w + b1.w};
+          const float2 x0 = unpack_bf16x2(xv.x), x1 = unpack_bf16x2(xv.y), x2 = unpack_bf16x2(xv.z),
+                       x3 = unpack_bf16x2(xv.w);
+          const int o = 8 * q4;
+          o4[q4] = make_uint4(pack_bf16x2(fmaf(gt[0], u2f(r[o + 0]), x0.x), fmaf(gt[1], u2f(r[o + 1]), x0.y)),
+                              pack_bf16x2(fmaf(gt[2], u2f(r[o + 2]), x1.x), fmaf(gt[3], u2f(r[o + 3]), x1.y)),
+                              pack_bf16x2(fmaf(gt[4], u2f(r[o + 4]), x2.x), fmaf(gt[5], u2f(r[o + 5]), x2.y)),
+                              pack_bf16x2(fmaf(gt[6], u2f(r[o + 6]), x3.x), fmaf(gt[7], u2f(r[o + 7]), x3.y)));
+        }
+      }
+    }
+  }
+};
+
+struct EpiSwiGLU {
+  int F;
+  bf16* hmid;  // [T, F]
+  // accumulator columns [0,128) = hn W_gate^T, [128,256) = hn W_up^T for F-columns nb*128 ..
+  __device__ __forceinline__ void apply(int row, int nb, int half, uint32_t taddr, int M) const {
+    const int f0 = nb * 128 + half * 64;
+    if (f0 >= F) return;
+    const bool ok = row < M;
+    uint32_t rg[32], ru[32];
+#pragma unroll 1
+    for (int c = 0; c < 2; ++c) {
+      tmem_ld32x2(taddr + half * 64 + c * 32, taddr + 128 + half * 64 + c * 32, rg, ru);
+      if (ok) {
+        uint4* o4 = reinterpret_cast<uint4*>(hmid + static_cast<size_t>(row) * F + f0 + c * 32);
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          float h[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) h[i] = siluf_(u2f(rg[8 * q4 + i])) * u2f(ru[8 * q4 + i]);
+          o4[q4] = make_uint4(pack_bf16x2(h[0], h[1]), pack_bf16x2(h[2], h[3]), pack_bf16x2(h[4], h[5]),
+                              pack_bf16x2(h[6], h[7]));
+        }
+      }
+    }
+  }
+};
+
+// ------------------------------------------------------------------ the kernel
+template <class Epi, bool DUAL>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
+                   const __grid_constant__ CUtensorMap tm_b2, int M, int num_n, int K, Epi epi, int* err) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  uint64_t* empty = full + STAGES;
+  uint64_t* tfull = empty + STAGES;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* done = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int num_m = (M + BM - 1) / BM;
+  const int num_tiles = num_m * num_n;
+  const int num_kb = (K + BK - 1) / BK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], NUM_EPI_WARPS);
+    }
+    mbar_init(done, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const WaitCtx wc{abort_flag, err};
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer
+      tma_prefetch_desc(&tm_a);
+      tma_prefetch_desc(&tm_b);
+      if (DUAL) tma_prefetch_desc(&tm_b2);
+      int stage = 0;
+      uint32_t phase = 0;
+      long long issued = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+        int mb, nb;
+        tile_coords(tile, num_m, num_n, mb, nb);
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1, wc, SITE_GEMM_PRODUCER)) {
+            ok = false;
+            break;
+          }
+          uint8_t* sa = smem + stage * STAGE_BYTES;
+          uint8_t* sb = sa + A_BYTES;
+          mbar_arrive_expect_tx(&full[stage], STAGE_BYTES);
+          tma_load_2d(sa, &tm_a, &full[stage], kb * BK, mb * BM);
+          if (DUAL) {
+            tma_load_2d(sb, &tm_b, &full[stage], kb * BK, nb * (BN / 2));
+            tma_load_2d(sb + B_BYTES / 2, &tm_b2, &full[stage], kb * BK, nb * (BN / 2));
+          } else {
+            tma_load_2d(sb, &tm_b, &full[stage], kb * BK, nb * BN);
+          }
+          ++issued;
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+      // every copy this thread started has landed before the CTA exits
+      for (long long i = (issued > STAGES ? issued - STAGES : 0); i < issued; ++i)
+        drain_wait(&full[i % STAGES], static_cast<uint32_t>((i / STAGES) & 1), err, SITE_GEMM_TEARDOWN);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------- MMA issuer
+      constexpr uint32_t idesc = idesc_bf16_f32(BM, BN);
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+        if (!mbar_wait(&tempty[acc], acc_phase ^ 1, wc, SITE_GEMM_MMA)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait(&full[stage], phase, wc, SITE_GEMM_MMA)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(smem + stage * STAGE_BYTES);
+          const uint32_t sb = sa + A_BYTES;
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k)
+            mma_bf16_ss(d_tmem, sdesc_kmajor_sw128(sa + k * 32), sdesc_kmajor_sw128(sb + k * 32), idesc,
+                        (kb | k) != 0 ? 1u : 0u);
+          mma_commit(&empty[stage]);  // frees the stage once these MMAs have read it
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (!ok) break;
+        mma_commit(&tfull[acc]);  // accumulator ready for the epilogue
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1;
+        }
+      }
+      mma_commit(done);  // completes when every MMA issued above has finished
+      drain_wait(done, 0, err, SITE_GEMM_TEARDOWN);
+    }
+  } else {
+    // ---------------- epilogue warps
+    const int quad = warp & 3;                 // TMEM lanes this warp may access: 32*quad ..
+    const int half = (warp - 2) / 4;           // 128-column half of the accumulator
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+      int mb, nb;
+      tile_coords(tile, num_m, num_n, mb, nb);
+      const bool got = mbar_wait(&tfull[acc], acc_phase, wc, SITE_GEMM_EPILOGUE);
+      if (!__all_sync(0xffffffffu, got)) break;
+      tc_fence_after();
+      const int row = mb * BM + quad * 32 + lane;
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(acc * BN);
+      epi.apply(row, nb, half, taddr, M);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[acc]);
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1;
+      }
+    }
+  }
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+template <class Epi, bool DUAL>
+cudaError_t set_smem_attr() {
+  return cudaFuncSetAttribute(gemm_tc_kernel<Epi, DUAL>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+}
+
+template <class Epi, bool DUAL>
+cudaError_t launch(const CUtensorMap* a, const CUtensorMap* b, const CUtensorMap* b2, int M, int num_n, int K,
+                   const Epi& epi, int num_sms, int* err, cudaStream_t st) {
+  const int tiles = ((M + BM - 1) / BM) * num_n;
+  if (tiles == 0) return cudaSuccess;
+  const int grid = tiles < num_sms ? tiles : num_sms;
+  gemm_tc_kernel<Epi, DUAL><<<grid, NUM_THREADS, SMEM_BYTES, st>>>(*a, *b, *b2, M, num_n, K, epi, err);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+int gemm_tc_smem_bytes() { return SMEM_BYTES; }
+
+cudaError_t gemm_tc_init() {
+  cudaError_t e;
+  if ((e = set_smem_attr<EpiQKVG, false>()) != cudaSuccess) return e;
+  if ((e = set_smem_attr<EpiResid, false>()) != cudaSuccess) return e;
+  if ((e = set_smem_attr<EpiSwiGLU, true>()) != cudaSuccess) return e;
+  return cudaSuccess;
+}
+
+cudaError_t launch_gemm_qkvg(const Fwd& f, const CUtensorMap* tm_a, const CUtensorMap* tm_b, int N,
+                             const QkvgDst& dst, int num_sms, int* err, cudaStream_t st) {
+  EpiQKVG epi{f, dst, N};
+  return launch<EpiQKVG, false>(tm_a, tm_b, tm_b, f.T, (N + BN - 1) / BN, f.d, epi, num_sms, err, st);
+}
+
+cudaError_t launch_gemm_resid(const Fwd& f, const CUtensorMap* tm_a, const CUtensorMap* tm_b, int K, RowSrc res,
+                              const float* mod_shared, const float* mod_bias, int chunk_gate, void* out, int num_sms,
+                              int* err, cudaStream_t st) {
+  EpiResid epi{f, res, mod_shared, mod_bias, chunk_gate, reinterpret_cast<bf16*>(out)};
+  return launch<EpiResid, false>(tm_a, tm_b, tm_b, f.T, (f.d + BN - 1) / BN, K, epi, num_sms, err, st);
+}
+
+cudaError_t launch_gemm_swiglu(const Fwd& f, const CUtensorMap* tm_a, const CUtensorMap* tm_gate,
+                               const CUtensorMap* tm_up, void* hmid, int num_sms, int* err, cudaStream_t st) {
+  EpiSwiGLU epi{f.F, reinterpret_cast<bf16*>(hmid)};
+  return launch<EpiSwiGLU, true>(tm_a, tm_gate, tm_up, f.T, (f.F + 127) / 128, f.d, epi, num_sms, err, st);
+}
+
+}  // namespace kd

@@ -1,0 +1,85 @@
+// Internal launcher interface between the C ABI (api.cu) and the kernel files.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace kd {
+
+// Shape of one forward call plus the block hyper-parameters.
+struct Fwd {
+  int B, L, n_txt, n_img, img_w, T, Lp;  // T = B*L joint rows, Lp = L rounded up to 64
+  int d, n_q, n_kv, hd, F, gate_on;
+  float eps;
+};
+
+// Where row m (joint order, m = b*L + l) of a block input lives: the split caller
+// buffers (text rows l < n_txt, image rows after) or one joint [T, d] buffer.
+struct RowSrc {
+  const void* x_txt;  // [B, n_txt, d]
+  const void* x_img;  // [B, n_img, d]
+  const void* joint;  // [T, d]; used when non-null
+};
+
+// Destination buffers of the fused QKV+gate projection.
+struct QkvgDst {
+  void* q;   // [B, n_q, L, hd]
+  void* k;   // [B, n_kv, L, hd]
+  void* vt;  // [B, n_kv, hd, Lp]
+  void* g;   // [T, n_q*hd]
+  const float* q_norm_w;
+  const float* k_norm_w;
+  const float2* rope;  // [pos][hd/4] (cos, sin)
+};
+
+#ifdef __CUDACC__
+// Pointer to row m of a block input (see RowSrc).
+template <class T>
+__device__ __forceinline__ const T* row_src_ptr(const RowSrc& s, int m, int L, int n_txt, int n_img, int d) {
+  if (s.joint) return reinterpret_cast<const T*>(s.joint) + static_cast<size_t>(m) * d;
+  const int b = m / L, l = m - b * L;
+  if (l < n_txt) return reinterpret_cast<const T*>(s.x_txt) + (static_cast<size_t>(b) * n_txt + l) * d;
+  return reinterpret_cast<const T*>(s.x_img) + (static_cast<size_t>(b) * n_img + (l - n_txt)) * d;
+}
+#endif
+
+// ---- kernels_simt.cu (both modes: norm; fp32 mode: everything else) ----
+cudaError_t launch_norm_modulate(bool bf16, const Fwd& f, RowSrc src, const float* gain_w, const float* mod_shared,
+                                 const float* mod_bias, int chunk_shift, int chunk_scale, void* out,
+                                 cudaStream_t st);
+cudaError_t launch_temb_sinusoid(const float* t, int B, float* e, cudaStream_t st);
+// C[M,N] = act(A[M,K] * W[N,K]^T + bias), fp32, act = 1 -> silu
+cudaError_t launch_gemm_simt_f32(const float* A, const float* W, float* C, int M, int N, int K, const float* bias,
+                                 int act, cudaStream_t st);
+// fp32 mode: raw [T, Nqkvg] -> QK-norm + RoPE + scatter
+cudaError_t launch_qkvg_post_f32(const Fwd& f, const float* raw, QkvgDst dst, cudaStream_t st);
+// attention with gate epilogue, SIMT, both dtypes (bf16: stand-in until the tensor-core kernel)
+cudaError_t launch_attn_simt(bool bf16, const Fwd& f, const void* q, const void* k, const void* vt, const void* g,
+                             void* og, cudaStream_t st);
+// fp32 mode: out = res + gate_chunk * acc
+cudaError_t launch_residual_f32(const Fwd& f, RowSrc res, const float* acc, const float* mod_shared,
+                                const float* mod_bias, int chunk_gate, float* out, cudaStream_t st);
+// fp32 mode: hmid = silu(a) * u
+cudaError_t launch_swiglu_f32(const Fwd& f, const float* a, const float* u, float* hmid, cudaStream_t st);
+
+// ---- gemm_tc.cu (bf16 mode, tcgen05 + TMA) ----
+int gemm_tc_smem_bytes();
+cudaError_t gemm_tc_init();  // sets the kernels' dynamic shared-memory limit (once per process)
+// xn[T,d] x W_qkvg^T -> QK-norm, RoPE, scatter to Q / K / V^T / G
+cudaError_t launch_gemm_qkvg(const Fwd& f, const CUtensorMap* tm_a, const CUtensorMap* tm_b, int N,
+                             const QkvgDst& dst, int num_sms, int* err, cudaStream_t st);
+// out[T,d] = res + gate_chunk * (A W^T)
+cudaError_t launch_gemm_resid(const Fwd& f, const CUtensorMap* tm_a, const CUtensorMap* tm_b, int K, RowSrc res,
+                              const float* mod_shared, const float* mod_bias, int chunk_gate, void* out, int num_sms,
+                              int* err, cudaStream_t st);
+// hmid[T,F] = silu(hn W_gate^T) * (hn W_up^T)
+cudaError_t launch_gemm_swiglu(const Fwd& f, const CUtensorMap* tm_a, const CUtensorMap* tm_gate,
+                               const CUtensorMap* tm_up, void* hmid, int num_sms, int* err, cudaStream_t st);
+
+// ---- attn_tc.cu (bf16 mode, tcgen05 + TMA) ----
+cudaError_t attn_tc_init();
+cudaError_t launch_attn_tc(const Fwd& f, const CUtensorMap* tm_q, const CUtensorMap* tm_k, const CUtensorMap* tm_vt,
+                           const void* g, void* og, int num_sms, int* err, cudaStream_t st);
+
+}  // namespace kd

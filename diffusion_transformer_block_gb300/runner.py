@@ -1,0 +1,101 @@
+"""Convenience owner of one library handle plus the caller-side device tensors.
+
+Marshalling only: torch allocates device memory and supplies streams; every step of
+the block runs in libkrea_dit.so. Used by the tests, the benchmark and the smoke check.
+"""
+from __future__ import annotations
+
+from typing import Dict, Optional, Sequence
+
+import torch
+
+from . import (KREA_DIT_BF16, KREA_DIT_FP32, krea_dit_block_create, krea_dit_block_destroy,
+               krea_dit_block_forward, krea_dit_block_workspace, krea_dit_timestep_embed, make_config,
+               make_temb_weights, make_weights)
+
+WEIGHT_KEYS = ("w_qkvg", "w_o", "w_gate", "w_up", "w_down", "norm1_w", "norm2_w", "q_norm_w", "k_norm_w",
+               "mod_bias")
+TEMB_KEYS = ("w1", "b1", "w2", "b2")
+
+
+class _DevView:
+    """Exposes a raw device range through __cuda_array_interface__ for torch.as_tensor."""
+
+    def __init__(self, ptr: int, shape: Sequence[int], typestr: str):
+        self.__cuda_array_interface__ = {"shape": tuple(shape), "typestr": typestr, "data": (ptr, True),
+                                         "version": 3, "strides": None}
+
+
+class DitBlock:
+    """One block handle. ``mode`` is "bf16" or "fp32" (the storage / arithmetic mode)."""
+
+    def __init__(self, *, max_batch: int, max_seq: int, d: int, n_q: int, n_kv: int, hd: int, F: int,
+                 img_h_max: int, img_w_max: int, gate_on: bool = True, mode: str = "bf16", eps: float = 1e-6,
+                 rope_base: float = 10000.0, device: str = "cuda:0"):
+        self.device = torch.device(device)
+        self.mode = mode
+        self.dtype = torch.bfloat16 if mode == "bf16" else torch.float32
+        self.dims = dict(d=d, n_q=n_q, n_kv=n_kv, hd=hd, F=F, gate_on=gate_on)
+        cfg = make_config(max_batch=max_batch, max_seq=max_seq, d_model=d, n_q=n_q, n_kv=n_kv, head_dim=hd, ffn=F,
+                          img_h_max=img_h_max, img_w_max=img_w_max, eps=eps, rope_base=rope_base, gate_on=gate_on,
+                          mode=KREA_DIT_BF16 if mode == "bf16" else KREA_DIT_FP32)
+        with torch.cuda.device(self.device):
+            self.handle = krea_dit_block_create(cfg)
+        self.w: Dict[str, torch.Tensor] = {}
+        self.tw: Dict[str, torch.Tensor] = {}
+        self._wstruct = None
+        self._twstruct = None
+
+    def set_weights(self, w: Dict[str, torch.Tensor]) -> None:
+        self.w = {k: w[k].to(self.device).contiguous() for k in WEIGHT_KEYS}
+        self._wstruct = make_weights(self.w)
+
+    def set_temb_weights(self, tw: Dict[str, torch.Tensor]) -> None:
+        self.tw = {k: tw[k].to(self.device, torch.float32).contiguous() for k in TEMB_KEYS}
+        self._twstruct = make_temb_weights(self.tw)
+
+    def timestep_embed(self, t: torch.Tensor, out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+        B = t.shape[0]
+        if out is None:
+            out = torch.empty(B, 6, self.dims["d"], device=self.device, dtype=torch.float32)
+        krea_dit_timestep_embed(self.handle, t, B, self._twstruct, out, stream or torch.cuda.current_stream(self.device))
+        return out
+
+    def forward(self, x_img: Optional[torch.Tensor], x_txt: Optional[torch.Tensor], B: int, img_h: int, img_w: int,
+                n_txt: int, t_emb: torch.Tensor, out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+        L = n_txt + img_h * img_w
+        if out is None:
+            out = torch.empty(B, L, self.dims["d"], device=self.device, dtype=self.dtype)
+        xi = x_img if (x_img is not None and img_h * img_w > 0) else None
+        xt = x_txt if (x_txt is not None and n_txt > 0) else None
+        krea_dit_block_forward(self.handle, xi, xt, B, img_h, img_w, n_txt, t_emb, self._wstruct, out,
+                               stream or torch.cuda.current_stream(self.device))
+        return out
+
+    def workspace(self, name: str, shape: Sequence[int]) -> torch.Tensor:
+        """Copy of a workspace buffer of the last forward, viewed with ``shape``."""
+        ptr, nbytes = krea_dit_block_workspace(self.handle, name)
+        esz = 2 if self.mode == "bf16" else 4
+        n = 1
+        for s in shape:
+            n *= s
+        if n * esz > nbytes:
+            raise ValueError(f"{name}: {n * esz} bytes requested, {nbytes} available")
+        if n == 0:
+            return torch.empty(tuple(shape), device=self.device, dtype=self.dtype)
+        view = torch.as_tensor(_DevView(ptr, (n,), "<i2" if esz == 2 else "<f4"), device=self.device)
+        t = view.clone()
+        if esz == 2:
+            t = t.view(torch.bfloat16)
+        return t.view(tuple(shape))
+
+    def close(self) -> None:
+        if getattr(self, "handle", None):
+            krea_dit_block_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):  # pragma: no cover - best effort
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -1,0 +1,202 @@
+/*
+ * krea_dit.h -- C ABI of the GB300 (sm_103a) Krea 2 single-stream DiT block forward.
+ *
+ * The operation (Krea 2 Technical Report, section "Architecture": "Transformer block",
+ * "Modality streams", "Timestep conditioning", "Positional encoding", "Normalisation"):
+ * one transformer block over the joint [text; image] token sequence, with weights shared
+ * by both modalities.
+ *
+ *   mod    = mod_shared[b] + mod_bias              (shift_a, scale_a, gate_a, shift_m, scale_m, gate_m)
+ *   X      = [x_txt[b]; x_img[b]]                  (text rows first, image rows row-major over (r, c))
+ *   xn     = rms(X) * (1 + norm1_w) * (1 + scale_a) + shift_a
+ *   q,k,v,g= xn W_q^T, xn W_k^T, xn W_v^T, xn W_g^T
+ *   q,k    = rms_hd(.) * (1 + q_norm_w / k_norm_w), then 2D axial RoPE on image rows
+ *   o_h    = softmax(q_h k_{h/G}^T / sqrt(hd)) v_{h/G}            (GQA, no mask)
+ *   o_g    = o * sigmoid(g)                        (omitted when gate_on = 0)
+ *   h1     = X + gate_a * (o_g W_o^T)
+ *   hn     = rms(h1) * (1 + norm2_w) * (1 + scale_m) + shift_m
+ *   out    = h1 + gate_m * ((silu(hn W_gate^T) * (hn W_up^T)) W_down^T)
+ *
+ * rms(v) = v / sqrt(mean(v^2) + eps). RoPE: head_dim is split in halves, [0, hd/2) turns
+ * with the row r and [hd/2, hd) with the column c; pair (2j, 2j+1) of a half of size
+ * D = hd/2 turns by pos * rope_base^(-2j/D). Text tokens sit at position 0 (identity).
+ *
+ * Conventions shared by every call:
+ *  - Pointers marked "device" are CUDA device (or managed) memory owned by the caller;
+ *    the library never frees them. Pointers marked "host" are host memory.
+ *  - Matrices are row-major; weights are nn.Linear-style [out_features, in_features].
+ *  - Storage dtype: KREA_DIT_BF16 mode stores weights, token activations and outputs as
+ *    bf16 (fp32 accumulation); KREA_DIT_FP32 mode stores them as fp32 (a check mode with
+ *    fp32 arithmetic and no tensor cores). Gains, modulation and timestep weights are fp32
+ *    in both modes.
+ *  - Every device pointer must be 16-byte aligned (tensor-memory-accelerator rule).
+ *  - Return value: KREA_DIT_OK (0) or a negative KREA_DIT_ERR_* code. All argument checks
+ *    happen on the host before anything is enqueued; a failed check enqueues nothing.
+ *  - Calls that take a stream only enqueue work on it: they do not allocate device
+ *    memory and do not synchronise. A handle's workspace is shared by its calls, so one
+ *    handle must not run on two streams at once.
+ */
+#ifndef KREA_DIT_H
+#define KREA_DIT_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ------------------------------------------------------------------ */
+#define KREA_DIT_OK 0
+#define KREA_DIT_ERR_INVALID_ARG (-1)          /* null pointer, negative size, bad enum */
+#define KREA_DIT_ERR_UNSUPPORTED_SHAPE (-2)    /* shape outside what the kernels implement */
+#define KREA_DIT_ERR_MISALIGNED (-3)           /* a device pointer is not 16-byte aligned */
+#define KREA_DIT_ERR_EXCEEDS_CREATE_LIMITS (-4) /* call larger than the handle was created for */
+#define KREA_DIT_ERR_CUDA (-5)                 /* a CUDA runtime/driver call failed */
+#define KREA_DIT_ERR_NO_DEVICE (-6)            /* current device is not an sm_103 GPU */
+#define KREA_DIT_ERR_DEVICE_TIMEOUT (-7)       /* a bounded on-device wait expired (see krea_dit_block_device_status) */
+#define KREA_DIT_ERR_INJECTED (-8)             /* host-side fault injection fired (testing aid) */
+
+/* ---- modes -------------------------------------------------------------------------- */
+#define KREA_DIT_BF16 0
+#define KREA_DIT_FP32 1
+
+typedef struct krea_dit_block_s* krea_dit_block_t;
+/* Same object as cudaStream_t / CUstream. NULL means the legacy default stream. */
+typedef struct CUstream_st* krea_dit_stream_t;
+
+/* Block hyper-parameters and the largest call a handle must serve.
+ *  max_batch, max_seq  : largest B and L = n_txt + img_h*img_w a forward may use
+ *  d_model             : width d (multiple of 64)
+ *  n_q, n_kv, head_dim : query heads, key/value heads (n_q % n_kv == 0), hd (64 or 128;
+ *                        BF16 mode needs 128)
+ *  ffn                 : SwiGLU hidden size F (multiple of 64)
+ *  img_h_max, img_w_max: largest image grid (sizes the RoPE table)
+ *  eps                 : RMSNorm epsilon (the block uses 1e-6)
+ *  rope_base           : RoPE base (10000)
+ *  gate_on             : 1 = sigmoid output gate on attention, 0 = off (then w_qkvg has no g rows)
+ *  mode                : KREA_DIT_BF16 or KREA_DIT_FP32 */
+typedef struct {
+  int max_batch, max_seq;
+  int d_model, n_q, n_kv, head_dim, ffn;
+  int img_h_max, img_w_max;
+  float eps, rope_base;
+  int gate_on;
+  int mode;
+} krea_dit_config;
+
+/* Block weights, all device memory, caller-owned. "dtype" = the mode's storage dtype.
+ *  w_qkvg  [(2 n_q + 2 n_kv) hd, d] dtype, rows ordered q | k | v | g (heads contiguous
+ *          inside each part); [(n_q + 2 n_kv) hd, d] when gate_on = 0
+ *  w_o     [d, n_q hd] dtype
+ *  w_gate  [F, d] dtype ; w_up [F, d] dtype ; w_down [d, F] dtype
+ *  norm1_w, norm2_w [d] fp32 : zero-centred gain offsets (gain = 1 + w)
+ *  q_norm_w, k_norm_w [hd] fp32 : QK-RMSNorm gain offsets (gain = 1 + w)
+ *  mod_bias [6, d] fp32 : this block's modulation bias, chunk order
+ *          shift_a, scale_a, gate_a, shift_m, scale_m, gate_m */
+typedef struct {
+  const void* w_qkvg;
+  const void* w_o;
+  const void* w_gate;
+  const void* w_up;
+  const void* w_down;
+  const float* norm1_w;
+  const float* norm2_w;
+  const float* q_norm_w;
+  const float* k_norm_w;
+  const float* mod_bias;
+} krea_dit_weights;
+
+/* Shared timestep-MLP weights, fp32 device memory: w1 [d, 256], b1 [d], w2 [6d, d], b2 [6d]. */
+typedef struct {
+  const float* w1;
+  const float* b1;
+  const float* w2;
+  const float* b2;
+} krea_dit_temb_weights;
+
+/* Create a handle on the current CUDA device. Validates the config, checks the device is
+ * sm_103, allocates the workspace for max_batch x max_seq tokens (the only allocation
+ * the library makes) and uploads the RoPE table. Synchronous. On error *out is NULL. */
+int krea_dit_block_create(const krea_dit_config* cfg, krea_dit_block_t* out);
+
+/* Free the handle and its workspace. Synchronises the device first. NULL is a no-op. */
+int krea_dit_block_destroy(krea_dit_block_t h);
+
+/* Shared timestep embedding (Krea 2 Technical Report, "Timestep conditioning"):
+ * e = [cos(1000 t w_i) | sin(1000 t w_i)], w_i = 10000^(-i/128), i < 128;
+ * mod_shared = W2 silu(W1 e + b1) + b2, written as [B, 6, d].
+ *  t          device fp32 [B], t in [0, 1]
+ *  B          1 .. max_batch
+ *  mod_shared device fp32 [B, 6, d], written. */
+int krea_dit_timestep_embed(krea_dit_block_t h, const float* t, int B, const krea_dit_temb_weights* w,
+                            float* mod_shared, krea_dit_stream_t stream);
+
+/* One block forward (operation at the top of this file).
+ *  x_img      device dtype [B, img_h*img_w, d] (may be NULL when img_h*img_w == 0)
+ *  x_txt      device dtype [B, n_txt, d]       (may be NULL when n_txt == 0)
+ *  B, img_h, img_w, n_txt : B <= max_batch, img_h <= img_h_max, img_w <= img_w_max,
+ *               L = n_txt + img_h*img_w <= max_seq; B == 0 or L == 0 enqueues nothing
+ *  t_emb      device fp32 [B, 6, d]: mod_shared from krea_dit_timestep_embed
+ *  out        device dtype [B, L, d], text rows first; must not alias any input. */
+int krea_dit_block_forward(krea_dit_block_t h, const void* x_img, const void* x_txt, int B, int img_h,
+                           int img_w, int n_txt, const float* t_emb, const krea_dit_weights* w, void* out,
+                           krea_dit_stream_t stream);
+
+/* Static text for a status code. Never NULL. */
+const char* krea_dit_status_string(int status);
+
+/* ---- inspection, timing and failure reporting ------------------------------------- */
+
+/* Workspace buffers written by the most recent forward (read-only views, owned by the
+ * handle, valid until the next forward or destroy). T = B L rows in joint order.
+ *  XN   [T, d] dtype       normed+modulated input of the attention branch
+ *  Q    [B, n_q, L, hd]    dtype, after QK-norm and RoPE
+ *  K    [B, n_kv, L, hd]   dtype, after QK-norm and RoPE
+ *  VT   [B, n_kv, hd, Lp]  dtype, values transposed, Lp = L rounded up to 64
+ *  G    [T, n_q hd]        dtype, gate pre-activation (unused when gate_on = 0)
+ *  OG   [T, n_q hd]        dtype, o * sigmoid(g)
+ *  H1   [T, d]             dtype, block state after the attention residual
+ *  HN   [T, d]             dtype, normed+modulated input of the MLP
+ *  HMID [T, F]             dtype, silu(hn W_gate^T) * (hn W_up^T) */
+#define KREA_DIT_BUF_XN 0
+#define KREA_DIT_BUF_Q 1
+#define KREA_DIT_BUF_K 2
+#define KREA_DIT_BUF_VT 3
+#define KREA_DIT_BUF_G 4
+#define KREA_DIT_BUF_OG 5
+#define KREA_DIT_BUF_H1 6
+#define KREA_DIT_BUF_HN 7
+#define KREA_DIT_BUF_HMID 8
+int krea_dit_block_workspace(krea_dit_block_t h, int which, void** dev_ptr, size_t* bytes);
+
+/* Per-kernel timing. When enabled, each forward records a CUDA event before and after
+ * every kernel it launches, on the forward's stream. krea_dit_block_kernel_times waits
+ * for those events and returns, per kernel slot, the summed milliseconds and the number
+ * of launches since the last reset (names: host strings owned by the library).
+ * cap = capacity of the arrays; *n = number of slots. Timing adds one event record per
+ * kernel and nothing else. */
+int krea_dit_block_set_timing(krea_dit_block_t h, int enable);
+int krea_dit_block_kernel_times(krea_dit_block_t h, const char** names, double* total_ms, int* launches,
+                                int cap, int* n);
+int krea_dit_block_timing_reset(krea_dit_block_t h);
+
+/* Every wait inside the tensor-core kernels (on a TMA arrival or an MMA commit) gives up
+ * after about one second, records which wait it was in a device-side error word, and the
+ * kernel returns. This call synchronises `stream`, reads the word, clears it, and returns
+ * KREA_DIT_OK or KREA_DIT_ERR_DEVICE_TIMEOUT (*site = the first wait that gave up, a
+ * bit mask of sites otherwise 0). */
+int krea_dit_block_device_status(krea_dit_block_t h, krea_dit_stream_t stream, int* site);
+
+/* Testing aid: make the next `count` calls of krea_dit_block_forward fail with
+ * KREA_DIT_ERR_INJECTED after validation and before any launch. */
+int krea_dit_block_inject_fault(krea_dit_block_t h, int count);
+
+/* Kernel names this library launches (for launch accounting): returns the number of
+ * names, fills up to cap of them. */
+int krea_dit_kernel_names(const char** names, int cap);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* KREA_DIT_H */
