@@ -221,6 +221,7 @@ int krea_dit_block_create(const krea_dit_config* c, krea_dit_block_t* out) {
     return KREA_DIT_ERR_INVALID_ARG;
   if (c->d_model <= 0 || c->n_q <= 0 || c->n_kv <= 0 || c->ffn <= 0) return KREA_DIT_ERR_INVALID_ARG;
   if (c->d_model % 64 || c->ffn % 64 || c->n_q % c->n_kv) return KREA_DIT_ERR_UNSUPPORTED_SHAPE;
+  if (c->d_model > 8192) return KREA_DIT_ERR_UNSUPPORTED_SHAPE;  // norm kernel: one thread per 8 columns
   if (c->head_dim != 64 && c->head_dim != 128) return KREA_DIT_ERR_UNSUPPORTED_SHAPE;
   if (c->mode == KREA_DIT_BF16 && c->head_dim != 128) return KREA_DIT_ERR_UNSUPPORTED_SHAPE;
   // 32-bit index arithmetic inside the kernels
@@ -258,7 +259,7 @@ int krea_dit_block_create(const krea_dit_config* c, krea_dit_block_t* out) {
   h->sz_vt = static_cast<size_t>(c->max_batch) * c->n_kv * hd * Lp * es;
   h->sz_g = T * c->n_q * hd * es;
   h->sz_og = T * c->n_q * hd * es;
-  h->sz_h1 = T * d * es;
+  h->sz_h1 = T * d * 4;  // the residual stream between the two residual adds is fp32 in both modes
   h->sz_hn = T * d * es;
   h->sz_hmid = T * F * es;
   std::vector<Item> items = {
@@ -312,7 +313,7 @@ int krea_dit_block_create(const krea_dit_config* c, krea_dit_block_t* out) {
     }
   }
   if (h->bf16) {
-    if (!get_encode() || kd::gemm_tc_init() != cudaSuccess) {
+    if (!get_encode() || kd::gemm_tc_init() != cudaSuccess || kd::attn_tc_init() != cudaSuccess) {
       cudaFree(h->ws);
       delete h;
       return KREA_DIT_ERR_CUDA;
@@ -431,20 +432,22 @@ int krea_dit_block_forward(krea_dit_block_t h, const void* x_img, const void* x_
               encode_3d(&tm_vt, h->vt, L, c.head_dim, static_cast<uint64_t>(B) * c.n_kv, f.Lp, 64, 128);
     if (!ok) return KREA_DIT_ERR_CUDA;
     const int sms = h->num_sms;
-    KD_RUN(S_NORM1, kd::launch_norm_modulate(true, f, xsrc, w->norm1_w, t_emb, w->mod_bias, 0, 1, h->xn, st));
+    KD_RUN(S_NORM1, kd::launch_norm_modulate(kd::NormIO::BF16_BF16, f, xsrc, w->norm1_w, t_emb, w->mod_bias, 0, 1,
+                                             h->xn, sms, st));
     KD_RUN(S_QKVG_TC, kd::launch_gemm_qkvg(f, &tm_xn, &tm_wqkvg, h->n_qkvg, dst, sms, h->err, st));
-    KD_RUN(S_ATTN, kd::launch_attn_simt(true, f, h->q, h->k, h->vt, h->g, h->og, st));
-    (void)tm_q; (void)tm_k; (void)tm_vt;
-    KD_RUN(S_OPROJ_TC, kd::launch_gemm_resid(f, &tm_og, &tm_wo, nqhd, xsrc, t_emb, w->mod_bias, 2, h->h1, sms,
-                                             h->err, st));
-    KD_RUN(S_NORM2, kd::launch_norm_modulate(true, f, h1src, w->norm2_w, t_emb, w->mod_bias, 3, 4, h->hn, st));
+    KD_RUN(S_ATTN, kd::launch_attn_tc(f, &tm_q, &tm_k, &tm_vt, h->g, h->og, sms, h->err, st));
+    KD_RUN(S_OPROJ_TC, kd::launch_gemm_resid_attn(f, &tm_og, &tm_wo, nqhd, xsrc, t_emb, w->mod_bias,
+                                                  static_cast<float*>(h->h1), sms, h->err, st));
+    KD_RUN(S_NORM2, kd::launch_norm_modulate(kd::NormIO::F32_BF16, f, h1src, w->norm2_w, t_emb, w->mod_bias, 3, 4,
+                                             h->hn, sms, st));
     KD_RUN(S_UPGATE_TC, kd::launch_gemm_swiglu(f, &tm_hn, &tm_wgate, &tm_wup, h->hmid, sms, h->err, st));
-    KD_RUN(S_DOWN_TC, kd::launch_gemm_resid(f, &tm_hmid, &tm_wdown, c.ffn, h1src, t_emb, w->mod_bias, 5, out, sms,
-                                            h->err, st));
+    KD_RUN(S_DOWN_TC, kd::launch_gemm_resid_mlp(f, &tm_hmid, &tm_wdown, c.ffn, static_cast<const float*>(h->h1),
+                                                t_emb, w->mod_bias, out, sms, h->err, st));
   } else {
     const int T = f.T;
     const float* wq = static_cast<const float*>(w->w_qkvg);
-    KD_RUN(S_NORM1, kd::launch_norm_modulate(false, f, xsrc, w->norm1_w, t_emb, w->mod_bias, 0, 1, h->xn, st));
+    KD_RUN(S_NORM1, kd::launch_norm_modulate(kd::NormIO::F32_F32, f, xsrc, w->norm1_w, t_emb, w->mod_bias, 0, 1,
+                                             h->xn, h->num_sms, st));
     KD_RUN(S_QKVG_F32, kd::launch_gemm_simt_f32(static_cast<const float*>(h->xn), wq, h->raw_qkvg, T, h->n_qkvg,
                                                 c.d_model, nullptr, 0, st));
     KD_RUN(S_QKVG_POST_F32, kd::launch_qkvg_post_f32(f, h->raw_qkvg, dst, st));
@@ -453,7 +456,8 @@ int krea_dit_block_forward(krea_dit_block_t h, const void* x_img, const void* x_
                                                  h->raw_o, T, c.d_model, nqhd, nullptr, 0, st));
     KD_RUN(S_RESID_ATTN_F32, kd::launch_residual_f32(f, xsrc, h->raw_o, t_emb, w->mod_bias, 2,
                                                      static_cast<float*>(h->h1), st));
-    KD_RUN(S_NORM2, kd::launch_norm_modulate(false, f, h1src, w->norm2_w, t_emb, w->mod_bias, 3, 4, h->hn, st));
+    KD_RUN(S_NORM2, kd::launch_norm_modulate(kd::NormIO::F32_F32, f, h1src, w->norm2_w, t_emb, w->mod_bias, 3, 4,
+                                             h->hn, h->num_sms, st));
     KD_RUN(S_GATE_F32, kd::launch_gemm_simt_f32(static_cast<const float*>(h->hn),
                                                 static_cast<const float*>(w->w_gate), h->raw_a, T, c.ffn, c.d_model,
                                                 nullptr, 0, st));
@@ -486,7 +490,7 @@ int krea_dit_block_workspace(krea_dit_block_t h, int which, void** dev_ptr, size
       break;
     case KREA_DIT_BUF_G: *dev_ptr = h->g; *bytes = T * h->cfg.n_q * hd * es; break;
     case KREA_DIT_BUF_OG: *dev_ptr = h->og; *bytes = T * h->cfg.n_q * hd * es; break;
-    case KREA_DIT_BUF_H1: *dev_ptr = h->h1; *bytes = T * h->cfg.d_model * es; break;
+    case KREA_DIT_BUF_H1: *dev_ptr = h->h1; *bytes = T * h->cfg.d_model * 4; break;
     case KREA_DIT_BUF_HN: *dev_ptr = h->hn; *bytes = T * h->cfg.d_model * es; break;
     case KREA_DIT_BUF_HMID: *dev_ptr = h->hmid; *bytes = T * h->cfg.ffn * es; break;
     default: return KREA_DIT_ERR_INVALID_ARG;

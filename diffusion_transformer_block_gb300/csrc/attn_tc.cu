@@ -1,0 +1,402 @@
+// Flash-style GQA attention with the sigmoid output gate, tcgen05 + TMA, sm_103a
+// (Krea 2 Technical Report, "Transformer block": GQA with gated attention output; the
+// pass is pure prefill, so there is no mask and no KV cache).
+//
+// Work unit = two 128-row query tiles of the same (batch, KV group): both tiles read the
+// same K/V tiles from shared memory, so every K/V tile loaded is used by two query
+// tiles; the other query tiles of the group re-read the group's K/V from L2.
+//
+// Per unit, for each 128-key K/V tile j:
+//   S_t   = Q_t K_j^T            (tensor core, fp32 in TMEM, t = 0, 1)
+//   P_t   = exp2(S_t * log2(e)/sqrt(hd) - m_t)   (softmax warpgroup t, one thread per row,
+//                                   bf16 into 128B-swizzled shared memory)
+//   O_t  += P_t V_j               (tensor core, fp32 in TMEM)
+// The running max m_t is raised only when the tile max exceeds it by more than 2^8 (then
+// O_t is rescaled in TMEM), so most tiles skip the rescale. The two tiles ping-pong:
+// while warpgroup 0 turns S_0 into P_0 the tensor core runs tile 1's products.
+// Epilogue: O_t / l_t * sigmoid(g) -> bf16 [T, n_q*hd].
+//
+// Warps 0-3: softmax/epilogue for tile 0, warps 4-7: tile 1, warp 8: TMA loads,
+// warp 9: TMEM allocation + MMA issue. TMEM: S_0, S_1, O_0, O_1 (4 x 128 columns).
+// Shared memory: Q_0, Q_1 (32 KB each), a 3-slot ring of 32 KB K or V^T tiles, P_0, P_1.
+#include "common.cuh"
+#include "internal.h"
+
+namespace kd {
+namespace {
+
+constexpr int HD = 128;            // head dim
+constexpr int BQ = 128;            // query rows per tile
+constexpr int BKV = 128;           // keys per K/V tile
+constexpr int TILE_BYTES = 128 * 128 * 2;  // one 128 x 128 bf16 operand (two 64-col swizzled halves)
+constexpr int HALF_BYTES = TILE_BYTES / 2;
+constexpr int NSLOT = 3;
+constexpr int NUM_THREADS = 320;
+constexpr int SMEM_Q = 0;
+constexpr int SMEM_KV = SMEM_Q + 2 * TILE_BYTES;
+constexpr int SMEM_P = SMEM_KV + NSLOT * TILE_BYTES;
+constexpr int SMEM_BAR = SMEM_P + 2 * TILE_BYTES;
+constexpr int SMEM_BYTES = SMEM_BAR + 256 + 1024;
+constexpr float RESCALE_THRESHOLD = 8.0f;  // log2 units: rescale O only if the max grows by > 2^8
+
+struct AttnArgs {
+  int B, L, n_q, n_kv, G, nqt, nkt, npairs, gate_on;
+  float scale_log2;  // log2(e) / sqrt(hd)
+  const bf16* g;     // [T, n_q*hd] gate pre-activation
+  bf16* og;          // [T, n_q*hd]
+  int* err;
+};
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, int* err, int site) {
+  const unsigned long long t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      atomicOr(err, site);
+      return;
+    }
+  }
+}
+
+// Byte offset of the 16-byte chunk `c16` (8 bf16 of K) of row `r` inside a 128-row x
+// 64-column K-major tile with the 128-byte swizzle (the layout TMA writes).
+__device__ __forceinline__ uint32_t sw128_off(int r, int c16) {
+  return static_cast<uint32_t>(r * 128 + ((c16 ^ (r & 7)) << 4));
+}
+
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                   const __grid_constant__ CUtensorMap tm_vt, AttnArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + SMEM_BAR);
+  uint64_t* bar_q = bar + 0;
+  uint64_t* kv_full = bar + 1;          // [NSLOT]
+  uint64_t* kv_empty = bar + 1 + NSLOT; // [NSLOT]
+  uint64_t* s_full = bar + 1 + 2 * NSLOT;   // [2]
+  uint64_t* p_full = s_full + 2;            // [2]
+  uint64_t* o_done = p_full + 2;            // [2]
+  uint64_t* done = o_done + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // ---- work unit: (b, kv group, pair of query tiles)
+  const int unit = blockIdx.x;
+  const int p = unit % a.npairs;
+  const int bk = unit / a.npairs;  // b * n_kv + kv
+  const int b = bk / a.n_kv, kvh = bk - b * a.n_kv;
+  const int ntiles = a.G * a.nqt;
+  const int tile_i[2] = {2 * p, 2 * p + 1};
+  const bool has1 = tile_i[1] < ntiles;
+  int head[2], qt[2];
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+    const int i = tile_i[t] < ntiles ? tile_i[t] : tile_i[0];
+    head[t] = kvh * a.G + i / a.nqt;
+    qt[t] = i % a.nqt;
+  }
+  const int nkt = a.nkt;
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar_q, 1);
+    for (int s = 0; s < NSLOT; ++s) {
+      mbar_init(&kv_full[s], 1);
+      mbar_init(&kv_empty[s], 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&s_full[t], 1);
+      mbar_init(&p_full[t], 128);
+      mbar_init(&o_done[t], 1);
+    }
+    mbar_init(done, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 9) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const WaitCtx wc{abort_flag, a.err};
+
+  if (warp == 8) {
+    // ------------------------------------------------------------ TMA loads
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_vt);
+      mbar_arrive_expect_tx(bar_q, (has1 ? 2 : 1) * TILE_BYTES);
+      for (int t = 0; t < (has1 ? 2 : 1); ++t)
+        for (int kh = 0; kh < 2; ++kh)
+          tma_load_3d(smem + SMEM_Q + t * TILE_BYTES + kh * HALF_BYTES, &tm_q, bar_q, kh * 64, qt[t] * BQ,
+                      b * a.n_q + head[t]);
+      int n = 0;
+      bool ok = true;
+      for (int j = 0; ok && j < nkt; ++j) {
+        for (int which = 0; which < 2; ++which, ++n) {  // 0: K_j, 1: V_j^T
+          const int slot = n % NSLOT;
+          const uint32_t ph = static_cast<uint32_t>((n / NSLOT) & 1);
+          if (!mbar_wait(&kv_empty[slot], ph ^ 1, wc, SITE_ATTN_LOAD)) {
+            ok = false;
+            break;
+          }
+          uint8_t* dst = smem + SMEM_KV + slot * TILE_BYTES;
+          mbar_arrive_expect_tx(&kv_full[slot], TILE_BYTES);
+          for (int h2 = 0; h2 < 2; ++h2) {
+            if (which == 0)
+              tma_load_3d(dst + h2 * HALF_BYTES, &tm_k, &kv_full[slot], h2 * 64, j * BKV, bk);
+            else
+              tma_load_3d(dst + h2 * HALF_BYTES, &tm_vt, &kv_full[slot], j * BKV + h2 * 64, 0, bk);
+          }
+        }
+      }
+      // every copy started here has landed before the CTA exits
+      drain_wait(bar_q, 0, a.err, SITE_ATTN_TEARDOWN);
+      for (int i = (n > NSLOT ? n - NSLOT : 0); i < n; ++i)
+        drain_wait(&kv_full[i % NSLOT], static_cast<uint32_t>((i / NSLOT) & 1), a.err, SITE_ATTN_TEARDOWN);
+    }
+  } else if (warp == 9) {
+    // ------------------------------------------------------------ MMA issue
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(128, 128);
+      const int nt = has1 ? 2 : 1;
+      const uint32_t sQ = smem_u32(smem + SMEM_Q), sKV = smem_u32(smem + SMEM_KV), sP = smem_u32(smem + SMEM_P);
+      auto issue_s = [&](int t, int slot) {  // S_t = Q_t K^T
+        const uint32_t d = tmem + t * 128;
+#pragma unroll
+        for (int kh = 0; kh < 2; ++kh)
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks)
+            mma_bf16_ss(d, sdesc_kmajor_sw128(sQ + t * TILE_BYTES + kh * HALF_BYTES + ks * 32),
+                        sdesc_kmajor_sw128(sKV + slot * TILE_BYTES + kh * HALF_BYTES + ks * 32), idesc,
+                        (kh | ks) != 0 ? 1u : 0u);
+      };
+      auto issue_pv = [&](int t, int slot, bool acc) {  // O_t += P_t V
+        const uint32_t d = tmem + 256 + t * 128;
+#pragma unroll
+        for (int kh = 0; kh < 2; ++kh)
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks)
+            mma_bf16_ss(d, sdesc_kmajor_sw128(sP + t * TILE_BYTES + kh * HALF_BYTES + ks * 32),
+                        sdesc_kmajor_sw128(sKV + slot * TILE_BYTES + kh * HALF_BYTES + ks * 32), idesc,
+                        (acc || (kh | ks) != 0) ? 1u : 0u);
+      };
+      bool ok = mbar_wait(bar_q, 0, wc, SITE_ATTN_MMA);
+      // K_0 is load 0
+      if (ok) ok = mbar_wait(&kv_full[0], 0, wc, SITE_ATTN_MMA);
+      if (ok) {
+        tc_fence_after();
+        for (int t = 0; t < nt; ++t) {
+          issue_s(t, 0);
+          mma_commit(&s_full[t]);
+        }
+        mma_commit(&kv_empty[0]);
+      }
+      for (int j = 0; ok && j < nkt; ++j) {
+        const int nv = 2 * j + 1, nk = 2 * j + 2;  // load indices of V_j and K_{j+1}
+        const int sv = nv % NSLOT, sk = nk % NSLOT;
+        const uint32_t pj = static_cast<uint32_t>(j & 1);
+        for (int t = 0; ok && t < nt; ++t) {
+          if (!mbar_wait(&p_full[t], pj, wc, SITE_ATTN_MMA)) { ok = false; break; }
+          if (t == 0 && !mbar_wait(&kv_full[sv], static_cast<uint32_t>((nv / NSLOT) & 1), wc, SITE_ATTN_MMA)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          issue_pv(t, sv, j > 0);
+          mma_commit(&o_done[t]);
+          if (j + 1 < nkt) {
+            if (t == 0 &&
+                !mbar_wait(&kv_full[sk], static_cast<uint32_t>((nk / NSLOT) & 1), wc, SITE_ATTN_MMA)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            issue_s(t, sk);
+            mma_commit(&s_full[t]);
+          }
+        }
+        if (!ok) break;
+        mma_commit(&kv_empty[sv]);
+        if (j + 1 < nkt) mma_commit(&kv_empty[sk]);
+      }
+      mma_commit(done);
+      drain_wait(done, 0, a.err, SITE_ATTN_TEARDOWN);
+    }
+  } else {
+    // ------------------------------------------------------------ softmax + epilogue
+    const int t = warp >> 2;         // query tile of this warpgroup
+    const int quad = warp & 3;       // TMEM lane quadrant
+    const int row = quad * 32 + lane;  // row inside the query tile
+    if (t == 0 || has1) {
+      const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+      const uint32_t tS = tmem + lane_off + t * 128;
+      const uint32_t tO = tmem + lane_off + 256 + t * 128;
+      uint8_t* pbuf = smem + SMEM_P + t * TILE_BYTES;
+      float m_run = -INFINITY, l_run = 0.f;
+      bool ok = true;
+      for (int j = 0; j < nkt; ++j) {
+        const bool got = mbar_wait(&s_full[t], static_cast<uint32_t>(j & 1), wc, SITE_ATTN_SOFTMAX);
+        if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
+        tc_fence_after();
+        const int kvalid = a.L - j * BKV;  // keys of this tile inside the sequence (>= 1)
+        // pass 1: row max of the tile
+        float mx = -INFINITY;
+        uint32_t r[32];
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          tmem_ld32(tS + c * 32, r);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const float s = (c * 32 + i < kvalid) ? __uint_as_float(r[i]) : -INFINITY;
+            mx = fmaxf(mx, s);
+          }
+        }
+        mx *= a.scale_log2;
+        bool waited = false;
+        if (j == 0) {
+          m_run = mx;
+        } else if (__any_sync(0xffffffffu, mx > m_run + RESCALE_THRESHOLD)) {
+          // Some row's max grew by more than 2^8: the whole warp rescales (the TMEM
+          // accesses are warp-collective), each row to its own new max (alpha = 1 for a
+          // row whose max did not grow), after the previous P V has landed.
+          const bool w2 = mbar_wait(&o_done[t], static_cast<uint32_t>((j - 1) & 1), wc, SITE_ATTN_SOFTMAX);
+          if (!__all_sync(0xffffffffu, w2)) { ok = false; break; }
+          waited = true;
+          tc_fence_after();
+          const float m_new = fmaxf(m_run, mx);
+          const float alpha = ex2(m_run - m_new);
+          l_run *= alpha;
+#pragma unroll 1
+          for (int c = 0; c < 4; ++c) {
+            tmem_ld32(tO + c * 32, r);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+            tmem_st32(tO + c * 32, r);
+          }
+          tmem_st_wait();
+          m_run = m_new;
+        }
+        // the previous P V must have read the P buffer before it is overwritten
+        if (j > 0 && !waited) {
+          const bool w3 = mbar_wait(&o_done[t], static_cast<uint32_t>((j - 1) & 1), wc, SITE_ATTN_SOFTMAX);
+          if (!__all_sync(0xffffffffu, w3)) { ok = false; break; }
+          tc_fence_after();
+        }
+        // pass 2: P = exp2(s * scale - m), bf16 into the swizzled P tile; row sum in fp32
+        float sum = 0.f;
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          tmem_ld32(tS + c * 32, r);
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 32; i += 2) {
+            const int col = c * 32 + i;
+            const float p0 = (col < kvalid) ? ex2(fmaf(__uint_as_float(r[i]), a.scale_log2, -m_run)) : 0.f;
+            const float p1 = (col + 1 < kvalid) ? ex2(fmaf(__uint_as_float(r[i + 1]), a.scale_log2, -m_run)) : 0.f;
+            sum += p0 + p1;
+            pk[i / 2] = pack_bf16x2(p0, p1);
+          }
+          // columns c*32 .. c*32+31 = half (c >> 1), 16-byte chunks (c & 1) * 4 .. + 3
+          uint8_t* hb = pbuf + (c >> 1) * HALF_BYTES;
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4)
+            *reinterpret_cast<uint4*>(hb + sw128_off(row, (c & 1) * 4 + q4)) =
+                make_uint4(pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2], pk[4 * q4 + 3]);
+        }
+        l_run += sum;
+        fence_proxy_async_smem();  // P visible to the tensor core
+        tc_fence_before();         // S reads (and any O rescale) ordered before the MMA
+        mbar_arrive(&p_full[t]);
+      }
+      // ---- epilogue: wait for the last P V, O / l * sigmoid(g) -> og
+      if (ok) {
+        const bool w4 = mbar_wait(&o_done[t], static_cast<uint32_t>((nkt - 1) & 1), wc, SITE_ATTN_SOFTMAX);
+        ok = __all_sync(0xffffffffu, w4);
+      }
+      if (ok) {
+        tc_fence_after();
+        const int ql = qt[t] * BQ + row;  // query position in the sequence
+        const bool valid = ql < a.L;
+        const float inv_l = 1.0f / l_run;
+        const size_t off = (static_cast<size_t>(b) * a.L + (valid ? ql : 0)) * (a.n_q * HD) + head[t] * HD;
+        uint32_t r[32];
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          tmem_ld32(tO + c * 32, r);
+          if (valid) {
+            float o[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = __uint_as_float(r[i]) * inv_l;
+            if (a.gate_on) {
+              const uint4* g4 = reinterpret_cast<const uint4*>(a.g + off + c * 32);
+#pragma unroll
+              for (int q4 = 0; q4 < 4; ++q4) {
+                const uint4 u = __ldg(g4 + q4);
+                const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  const float2 gg = unpack_bf16x2(w4[e]);
+                  o[8 * q4 + 2 * e] *= sigmoidf_(gg.x);
+                  o[8 * q4 + 2 * e + 1] *= sigmoidf_(gg.y);
+                }
+              }
+            }
+            uint4* o4 = reinterpret_cast<uint4*>(a.og + off + c * 32);
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4)
+              o4[q4] = make_uint4(pack_bf16x2(o[8 * q4 + 0], o[8 * q4 + 1]), pack_bf16x2(o[8 * q4 + 2], o[8 * q4 + 3]),
+                                  pack_bf16x2(o[8 * q4 + 4], o[8 * q4 + 5]), pack_bf16x2(o[8 * q4 + 6], o[8 * q4 + 7]));
+          }
+        }
+      }
+      tc_fence_before();
+    }
+  }
+  __syncthreads();
+  if (warp == 9) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+}  // namespace
+
+cudaError_t attn_tc_init() {
+  return cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+}
+
+cudaError_t launch_attn_tc(const Fwd& f, const CUtensorMap* tm_q, const CUtensorMap* tm_k, const CUtensorMap* tm_vt,
+                           const void* g, void* og, int num_sms, int* err, cudaStream_t st) {
+  (void)num_sms;
+  AttnArgs a;
+  a.B = f.B;
+  a.L = f.L;
+  a.n_q = f.n_q;
+  a.n_kv = f.n_kv;
+  a.G = f.n_q / f.n_kv;
+  a.nqt = (f.L + BQ - 1) / BQ;
+  a.nkt = (f.L + BKV - 1) / BKV;
+  a.npairs = (a.G * a.nqt + 1) / 2;
+  a.gate_on = f.gate_on;
+  a.scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(HD));
+  a.g = reinterpret_cast<const bf16*>(g);
+  a.og = reinterpret_cast<bf16*>(og);
+  a.err = err;
+  const long long units = static_cast<long long>(f.B) * f.n_kv * a.npairs;
+  if (units == 0) return cudaSuccess;
+  attn_tc_kernel<<<static_cast<unsigned>(units), NUM_THREADS, SMEM_BYTES, st>>>(*tm_q, *tm_k, *tm_vt, a);
+  return cudaGetLastError();
+}
+
+}  // namespace kd

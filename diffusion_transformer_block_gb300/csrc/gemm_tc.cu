@@ -6,7 +6,7 @@
 //             "Normalisation")
 //   * RESID : out = res + gate * (A W^T)   -- attention output projection and the MLP
 //             down projection, each with its gated residual ("Residual design",
-//             "Timestep conditioning")
+//             "Timestep conditioning"); the residual stream between them is fp32
 //   * SWIGLU: silu(hn W_gate^T) * (hn W_up^T), both products in one 128x256 accumulator
 //             ("Transformer block": SwiGLU MLP)
 //
@@ -155,20 +155,43 @@ struct EpiQKVG {
   }
 };
 
+// 8 consecutive residual values as fp32 (bf16 or fp32 storage)
+__device__ __forceinline__ void load_res8(const bf16* p, float (&v)[8]) {
+  const uint4 u = *reinterpret_cast<const uint4*>(p);
+  const float2 a = unpack_bf16x2(u.x), b = unpack_bf16x2(u.y), c = unpack_bf16x2(u.z), e = unpack_bf16x2(u.w);
+  v[0] = a.x; v[1] = a.y; v[2] = b.x; v[3] = b.y; v[4] = c.x; v[5] = c.y; v[6] = e.x; v[7] = e.y;
+}
+__device__ __forceinline__ void load_res8(const float* p, float (&v)[8]) {
+  const float4 a = reinterpret_cast<const float4*>(p)[0], b = reinterpret_cast<const float4*>(p)[1];
+  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+__device__ __forceinline__ void store_out8(bf16* p, const float (&v)[8]) {
+  *reinterpret_cast<uint4*>(p) = make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]),
+                                            pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7]));
+}
+__device__ __forceinline__ void store_out8(float* p, const float (&v)[8]) {
+  reinterpret_cast<float4*>(p)[0] = make_float4(v[0], v[1], v[2], v[3]);
+  reinterpret_cast<float4*>(p)[1] = make_float4(v[4], v[5], v[6], v[7]);
+}
+
+// out = res + gate * acc. The attention residual reads the bf16 block input from the
+// caller's split text/image buffers and writes the fp32 residual stream h1; the MLP
+// residual reads h1 and writes the bf16 block output.
+template <class TRes, class TOut>
 struct EpiResid {
   Fwd f;
   RowSrc res;
   const float* mod_shared;
   const float* mod_bias;
-  int chunk;  // modulation chunk of the gate (2 = gate_a, 5 = gate_m)
-  bf16* out;  // [T, d]
+  int chunk;   // modulation chunk of the gate (2 = gate_a, 5 = gate_m)
+  TOut* out;   // [T, d]
   __device__ __forceinline__ void apply(int row, int nb, int half, uint32_t taddr, int M) const {
     const int N = f.d;
     const int n0 = nb * BN + half * 128;
     if (n0 >= N) return;
     const bool ok = row < M;
     const int b = ok ? row / f.L : 0;
-    const bf16* x = ok ? row_src_ptr<bf16>(res, row, f.L, f.n_txt, f.n_img, f.d) : nullptr;
+    const TRes* x = ok ? row_src_ptr<TRes>(res, row, f.L, f.n_txt, f.n_img, f.d) : nullptr;
     const float* gs = mod_shared + (static_cast<size_t>(b) * 6 + chunk) * N;
     const float* gb = mod_bias + static_cast<size_t>(chunk) * N;
     uint32_t r[32];
@@ -178,29 +201,28 @@ struct EpiResid {
       if (col >= N) break;
       tmem_ld32(taddr + half * 128 + c * 32, r);
       if (ok) {
-        const uint4* x4 = reinterpret_cast<const uint4*>(x + col);
         const float4* gs4 = reinterpret_cast<const float4*>(gs + col);
         const float4* gb4 = reinterpret_cast<const float4*>(gb + col);
-        uint4* o4 = reinterpret_cast<uint4*>(out + static_cast<size_t>(row) * N + col);
+        TOut* o = out + static_cast<size_t>(row) * N + col;
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4) {
-          const uint4 xv = x4[q4];
+          float xv[8];
+          load_res8(x + col + 8 * q4, xv);
           const float4 s0 = __ldg(gs4 + 2 * q4), s1 = __ldg(gs4 + 2 * q4 + 1);
           const float4 b0 = __ldg(gb4 + 2 * q4), b1 = __ldg(gb4 + 2 * q4 + 1);
           const float gt[8] = {s0.x + b0.x, s0.y + b0.y, s0.z + b0.z, s0.w + b0.w,
                                s1.x + b1.x, s1.y + b1.y, s1.z + b1.z, s1.w + b1.w};
-          const float2 x0 = unpack_bf16x2(xv.x), x1 = unpack_bf16x2(xv.y), x2 = unpack_bf16x2(xv.z),
-                       x3 = unpack_bf16x2(xv.w);
-          const int o = 8 * q4;
-          o4[q4] = make_uint4(pack_bf16x2(fmaf(gt[0], u2f(r[o + 0]), x0.x), fmaf(gt[1], u2f(r[o + 1]), x0.y)),
-                              pack_bf16x2(fmaf(gt[2], u2f(r[o + 2]), x1.x), fmaf(gt[3], u2f(r[o + 3]), x1.y)),
-                              pack_bf16x2(fmaf(gt[4], u2f(r[o + 4]), x2.x), fmaf(gt[5], u2f(r[o + 5]), x2.y)),
-                              pack_bf16x2(fmaf(gt[6], u2f(r[o + 6]), x3.x), fmaf(gt[7], u2f(r[o + 7]), x3.y)));
+          float y[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) y[i] = fmaf(gt[i], u2f(r[8 * q4 + i]), xv[i]);
+          store_out8(o + 8 * q4, y);
         }
       }
     }
   }
 };
+using EpiResidAttn = EpiResid<bf16, float>;
+using EpiResidMlp = EpiResid<float, bf16>;
 
 struct EpiSwiGLU {
   int F;
@@ -406,7 +428,8 @@ int gemm_tc_smem_bytes() { return SMEM_BYTES; }
 cudaError_t gemm_tc_init() {
   cudaError_t e;
   if ((e = set_smem_attr<EpiQKVG, false>()) != cudaSuccess) return e;
-  if ((e = set_smem_attr<EpiResid, false>()) != cudaSuccess) return e;
+  if ((e = set_smem_attr<EpiResidAttn, false>()) != cudaSuccess) return e;
+  if ((e = set_smem_attr<EpiResidMlp, false>()) != cudaSuccess) return e;
   if ((e = set_smem_attr<EpiSwiGLU, true>()) != cudaSuccess) return e;
   return cudaSuccess;
 }
@@ -417,11 +440,18 @@ cudaError_t launch_gemm_qkvg(const Fwd& f, const CUtensorMap* tm_a, const CUtens
   return launch<EpiQKVG, false>(tm_a, tm_b, tm_b, f.T, (N + BN - 1) / BN, f.d, epi, num_sms, err, st);
 }
 
-cudaError_t launch_gemm_resid(const Fwd& f, const CUtensorMap* tm_a, const CUtensorMap* tm_b, int K, RowSrc res,
-                              const float* mod_shared, const float* mod_bias, int chunk_gate, void* out, int num_sms,
-                              int* err, cudaStream_t st) {
-  EpiResid epi{f, res, mod_shared, mod_bias, chunk_gate, reinterpret_cast<bf16*>(out)};
-  return launch<EpiResid, false>(tm_a, tm_b, tm_b, f.T, (f.d + BN - 1) / BN, K, epi, num_sms, err, st);
+cudaError_t launch_gemm_resid_attn(const Fwd& f, const CUtensorMap* tm_a, const CUtensorMap* tm_b, int K, RowSrc x,
+                                   const float* mod_shared, const float* mod_bias, float* h1, int num_sms, int* err,
+                                   cudaStream_t st) {
+  EpiResidAttn epi{f, x, mod_shared, mod_bias, 2, h1};
+  return launch<EpiResidAttn, false>(tm_a, tm_b, tm_b, f.T, (f.d + BN - 1) / BN, K, epi, num_sms, err, st);
+}
+
+cudaError_t launch_gemm_resid_mlp(const Fwd& f, const CUtensorMap* tm_a, const CUtensorMap* tm_b, int K,
+                                  const float* h1, const float* mod_shared, const float* mod_bias, void* out,
+                                  int num_sms, int* err, cudaStream_t st) {
+  EpiResidMlp epi{f, RowSrc{nullptr, nullptr, h1}, mod_shared, mod_bias, 5, reinterpret_cast<bf16*>(out)};
+  return launch<EpiResidMlp, false>(tm_a, tm_b, tm_b, f.T, (f.d + BN - 1) / BN, K, epi, num_sms, err, st);
 }
 
 cudaError_t launch_gemm_swiglu(const Fwd& f, const CUtensorMap* tm_a, const CUtensorMap* tm_gate,

@@ -45,8 +45,11 @@ __device__ __forceinline__ const T* row_src_ptr(const RowSrc& s, int m, int L, i
 #endif
 
 // ---- kernels_simt.cu (both modes: norm; fp32 mode: everything else) ----
-cudaError_t launch_norm_modulate(bool bf16, const Fwd& f, RowSrc src, const float* gain_w, const float* mod_shared,
-                                 const float* mod_bias, int chunk_shift, int chunk_scale, void* out,
+// input -> output storage types of a norm+modulate launch
+enum class NormIO { BF16_BF16, F32_BF16, F32_F32 };
+// requires d % 8 == 0 and d / 8 <= 1024 (one thread per 8 columns)
+cudaError_t launch_norm_modulate(NormIO io, const Fwd& f, RowSrc src, const float* gain_w, const float* mod_shared,
+                                 const float* mod_bias, int chunk_shift, int chunk_scale, void* out, int num_sms,
                                  cudaStream_t st);
 cudaError_t launch_temb_sinusoid(const float* t, int B, float* e, cudaStream_t st);
 // C[M,N] = act(A[M,K] * W[N,K]^T + bias), fp32, act = 1 -> silu
@@ -69,10 +72,14 @@ cudaError_t gemm_tc_init();  // sets the kernels' dynamic shared-memory limit (o
 // xn[T,d] x W_qkvg^T -> QK-norm, RoPE, scatter to Q / K / V^T / G
 cudaError_t launch_gemm_qkvg(const Fwd& f, const CUtensorMap* tm_a, const CUtensorMap* tm_b, int N,
                              const QkvgDst& dst, int num_sms, int* err, cudaStream_t st);
-// out[T,d] = res + gate_chunk * (A W^T)
-cudaError_t launch_gemm_resid(const Fwd& f, const CUtensorMap* tm_a, const CUtensorMap* tm_b, int K, RowSrc res,
-                              const float* mod_shared, const float* mod_bias, int chunk_gate, void* out, int num_sms,
-                              int* err, cudaStream_t st);
+// h1[T,d] (fp32) = x (bf16, split buffers) + gate_a * (A W^T)
+cudaError_t launch_gemm_resid_attn(const Fwd& f, const CUtensorMap* tm_a, const CUtensorMap* tm_b, int K, RowSrc x,
+                                   const float* mod_shared, const float* mod_bias, float* h1, int num_sms, int* err,
+                                   cudaStream_t st);
+// out[T,d] (bf16) = h1 (fp32) + gate_m * (A W^T)
+cudaError_t launch_gemm_resid_mlp(const Fwd& f, const CUtensorMap* tm_a, const CUtensorMap* tm_b, int K,
+                                  const float* h1, const float* mod_shared, const float* mod_bias, void* out,
+                                  int num_sms, int* err, cudaStream_t st);
 // hmid[T,F] = silu(hn W_gate^T) * (hn W_up^T)
 cudaError_t launch_gemm_swiglu(const Fwd& f, const CUtensorMap* tm_a, const CUtensorMap* tm_gate,
                                const CUtensorMap* tm_up, void* hmid, int num_sms, int* err, cudaStream_t st);

@@ -2,7 +2,7 @@
 //
 //  * norm_modulate  (both modes): zero-centred RMSNorm + shift/scale modulation with the
 //    per-block bias (Krea 2 Technical Report, "Normalisation" and "Timestep
-//    conditioning"). HBM-bound: one warp per row, 16-byte vector loads/stores, fp32 math.
+//    conditioning"). HBM-bound: 16-byte vector loads/stores, fp32 math.
 //  * temb_sinusoid  (both modes): the sinusoidal timestep embedding ("Timestep
 //    conditioning"), argument and sin/cos in fp64 then rounded to fp32.
 //  * fp32 check mode: a plain tiled fp32 GEMM, the QK-norm + RoPE scatter, the GQA
@@ -16,92 +16,131 @@
 namespace kd {
 
 // ============================================================== norm + modulate
-// 16-byte vector of the storage type: 8 bf16 or 4 fp32.
-template <class T>
-struct Vec;
-template <>
-struct Vec<bf16> {
-  static constexpr int N = 8;
-  static __device__ __forceinline__ void load(const bf16* p, float (&v)[8]) {
-    uint4 u = *reinterpret_cast<const uint4*>(p);
-    float2 a = unpack_bf16x2(u.x), b = unpack_bf16x2(u.y), c = unpack_bf16x2(u.z), e = unpack_bf16x2(u.w);
-    v[0] = a.x; v[1] = a.y; v[2] = b.x; v[3] = b.y; v[4] = c.x; v[5] = c.y; v[6] = e.x; v[7] = e.y;
-  }
-  static __device__ __forceinline__ void store(bf16* p, const float (&v)[8]) {
-    uint4 u;
-    u.x = pack_bf16x2(v[0], v[1]); u.y = pack_bf16x2(v[2], v[3]);
-    u.z = pack_bf16x2(v[4], v[5]); u.w = pack_bf16x2(v[6], v[7]);
-    *reinterpret_cast<uint4*>(p) = u;
-  }
-};
-template <>
-struct Vec<float> {
-  static constexpr int N = 4;
-  static __device__ __forceinline__ void load(const float* p, float (&v)[4]) {
-    float4 u = *reinterpret_cast<const float4*>(p);
-    v[0] = u.x; v[1] = u.y; v[2] = u.z; v[3] = u.w;
-  }
-  static __device__ __forceinline__ void store(float* p, const float (&v)[4]) {
-    *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
-  }
-};
-
+// Each thread owns 8 consecutive columns for the whole kernel, so the per-column
+// parameters (1 + w)(1 + scale) and shift are loaded once per (thread, batch element)
+// instead of once per element. A CTA handles groups of RG rows: 16-byte loads of the
+// RG row chunks, per-row sum of squares reduced over the CTA, then the modulated rows.
 // y = x / sqrt(mean(x^2) + eps) * (1 + w) * (1 + scale) + shift,
-// scale/shift = mod_shared[b, chunk] + mod_bias[chunk]. One warp per row.
+// scale/shift = mod_shared[b, chunk] + mod_bias[chunk].
+constexpr int NM_RG = 4;
+
 template <class T>
-__global__ void __launch_bounds__(256) norm_modulate_kernel(Fwd f, RowSrc src, const float* __restrict__ gain_w,
-                                                            const float* __restrict__ mod_shared,
-                                                            const float* __restrict__ mod_bias, int chunk_shift,
-                                                            int chunk_scale, T* __restrict__ out) {
-  constexpr int VN = Vec<T>::N;
-  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  if (warp >= f.T) return;
-  const int m = warp, d = f.d;
-  const int b = m / f.L;
-  const T* x = row_src_ptr<T>(src, m, f.L, f.n_txt, f.n_img, d);
-  const int nvec = d / VN;
+__device__ __forceinline__ void load8(const T* p, float (&v)[8]);
+template <>
+__device__ __forceinline__ void load8<bf16>(const bf16* p, float (&v)[8]) {
+  const uint4 u = *reinterpret_cast<const uint4*>(p);
+  const float2 a = unpack_bf16x2(u.x), b = unpack_bf16x2(u.y), c = unpack_bf16x2(u.z), e = unpack_bf16x2(u.w);
+  v[0] = a.x; v[1] = a.y; v[2] = b.x; v[3] = b.y; v[4] = c.x; v[5] = c.y; v[6] = e.x; v[7] = e.y;
+}
+template <>
+__device__ __forceinline__ void load8<float>(const float* p, float (&v)[8]) {
+  const float4 a = reinterpret_cast<const float4*>(p)[0], b = reinterpret_cast<const float4*>(p)[1];
+  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+template <class T>
+__device__ __forceinline__ void store8(T* p, const float (&v)[8]);
+template <>
+__device__ __forceinline__ void store8<bf16>(bf16* p, const float (&v)[8]) {
+  *reinterpret_cast<uint4*>(p) = make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]),
+                                            pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7]));
+}
+template <>
+__device__ __forceinline__ void store8<float>(float* p, const float (&v)[8]) {
+  reinterpret_cast<float4*>(p)[0] = make_float4(v[0], v[1], v[2], v[3]);
+  reinterpret_cast<float4*>(p)[1] = make_float4(v[4], v[5], v[6], v[7]);
+}
 
-  float ss = 0.f;
-  for (int v = lane; v < nvec; v += 32) {
-    float e[VN];
-    Vec<T>::load(x + v * VN, e);
+template <class Tin, class Tout>
+__global__ void __launch_bounds__(1024) norm_modulate_kernel(Fwd f, RowSrc src, const float* __restrict__ gain_w,
+                                                             const float* __restrict__ mod_shared,
+                                                             const float* __restrict__ mod_bias, int chunk_shift,
+                                                             int chunk_scale, Tout* __restrict__ out) {
+  __shared__ float red[2][32][NM_RG];
+  const int d = f.d;
+  const int c0 = threadIdx.x * 8;  // blockDim.x = d / 8 rounded up to whole warps
+  const bool active = c0 < d;      // threads past the row end only join the reductions
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
+  float gain[8], A[8], S[8];
 #pragma unroll
-    for (int i = 0; i < VN; ++i) ss = fmaf(e[i], e[i], ss);
+  for (int i = 0; i < 8; ++i) {
+    gain[i] = active ? 1.0f + gain_w[c0 + i] : 0.f;
+    A[i] = 0.f;
+    S[i] = 0.f;
   }
-  ss = warp_sum(ss);
-  const float rstd = 1.0f / sqrtf(ss / static_cast<float>(d) + f.eps);
-
-  const float* sh_s = mod_shared + (static_cast<size_t>(b) * 6 + chunk_shift) * d;
-  const float* sc_s = mod_shared + (static_cast<size_t>(b) * 6 + chunk_scale) * d;
-  const float* sh_b = mod_bias + static_cast<size_t>(chunk_shift) * d;
-  const float* sc_b = mod_bias + static_cast<size_t>(chunk_scale) * d;
-  T* y = out + static_cast<size_t>(m) * d;
-  for (int v = lane; v < nvec; v += 32) {
-    float e[VN];
-    Vec<T>::load(x + v * VN, e);
+  int cur_b = -1;
+  const int ngroups = (f.T + NM_RG - 1) / NM_RG;
+  int buf = 0;
+  for (int grp = blockIdx.x; grp < ngroups; grp += gridDim.x, buf ^= 1) {
+    float x[NM_RG][8], ss[NM_RG];
 #pragma unroll
-    for (int i = 0; i < VN; ++i) {
-      const int c = v * VN + i;
-      const float scale = sc_s[c] + sc_b[c];
-      const float shift = sh_s[c] + sh_b[c];
-      e[i] = fmaf(e[i] * rstd * (1.0f + gain_w[c]), 1.0f + scale, shift);
+    for (int r = 0; r < NM_RG; ++r) {
+      const int m = grp * NM_RG + r;
+      ss[r] = 0.f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) x[r][i] = 0.f;
+      if (active && m < f.T) {
+        load8<Tin>(row_src_ptr<Tin>(src, m, f.L, f.n_txt, f.n_img, d) + c0, x[r]);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) ss[r] = fmaf(x[r][i], x[r][i], ss[r]);
+      }
     }
-    Vec<T>::store(y + v * VN, e);
+#pragma unroll
+    for (int r = 0; r < NM_RG; ++r) {
+      ss[r] = warp_sum(ss[r]);
+      if (lane == 0) red[buf][warp][r] = ss[r];
+    }
+    __syncthreads();
+#pragma unroll
+    for (int r = 0; r < NM_RG; ++r) {
+      const int m = grp * NM_RG + r;
+      if (m >= f.T) break;
+      float tot = 0.f;
+      for (int w = 0; w < nwarps; ++w) tot += red[buf][w][r];
+      const float rstd = 1.0f / sqrtf(tot / static_cast<float>(d) + f.eps);
+      const int b = m / f.L;
+      if (!active) continue;
+      if (b != cur_b) {
+        cur_b = b;
+        const float* sc_s = mod_shared + (static_cast<size_t>(b) * 6 + chunk_scale) * d + c0;
+        const float* sh_s = mod_shared + (static_cast<size_t>(b) * 6 + chunk_shift) * d + c0;
+        const float* sc_b = mod_bias + static_cast<size_t>(chunk_scale) * d + c0;
+        const float* sh_b = mod_bias + static_cast<size_t>(chunk_shift) * d + c0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          A[i] = gain[i] * (1.0f + (sc_s[i] + sc_b[i]));
+          S[i] = sh_s[i] + sh_b[i];
+        }
+      }
+      float y[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) y[i] = fmaf(x[r][i] * rstd, A[i], S[i]);
+      store8<Tout>(out + static_cast<size_t>(m) * d + c0, y);
+    }
   }
 }
 
-cudaError_t launch_norm_modulate(bool bf16_mode, const Fwd& f, RowSrc src, const float* gain_w,
-                                 const float* mod_shared, const float* mod_bias, int chunk_shift, int chunk_scale,
-                                 void* out, cudaStream_t st) {
-  const int threads = 256, rows_per_cta = threads / 32;
-  const int grid = (f.T + rows_per_cta - 1) / rows_per_cta;
-  if (bf16_mode)
-    norm_modulate_kernel<bf16><<<grid, threads, 0, st>>>(f, src, gain_w, mod_shared, mod_bias, chunk_shift,
-                                                         chunk_scale, reinterpret_cast<bf16*>(out));
-  else
-    norm_modulate_kernel<float><<<grid, threads, 0, st>>>(f, src, gain_w, mod_shared, mod_bias, chunk_shift,
-                                                          chunk_scale, reinterpret_cast<float*>(out));
+cudaError_t launch_norm_modulate(NormIO io, const Fwd& f, RowSrc src, const float* gain_w, const float* mod_shared,
+                                 const float* mod_bias, int chunk_shift, int chunk_scale, void* out, int num_sms,
+                                 cudaStream_t st) {
+  const int threads = (f.d / 8 + 31) / 32 * 32;
+  const int ngroups = (f.T + NM_RG - 1) / NM_RG;
+  const int per_sm = threads <= 256 ? 8 : (threads <= 512 ? 4 : 2);
+  const int grid = ngroups < num_sms * per_sm ? ngroups : num_sms * per_sm;
+  switch (io) {
+    case NormIO::BF16_BF16:
+      norm_modulate_kernel<bf16, bf16><<<grid, threads, 0, st>>>(f, src, gain_w, mod_shared, mod_bias, chunk_shift,
+                                                                 chunk_scale, reinterpret_cast<bf16*>(out));
+      break;
+    case NormIO::F32_BF16:
+      norm_modulate_kernel<float, bf16><<<grid, threads, 0, st>>>(f, src, gain_w, mod_shared, mod_bias, chunk_shift,
+                                                                  chunk_scale, reinterpret_cast<bf16*>(out));
+      break;
+    case NormIO::F32_F32:
+      norm_modulate_kernel<float, float><<<grid, threads, 0, st>>>(f, src, gain_w, mod_shared, mod_bias,
+                                                                   chunk_shift, chunk_scale,
+                                                                   reinterpret_cast<float*>(out));
+      break;
+  }
   return cudaGetLastError();
 }
 

@@ -22,7 +22,7 @@ class _DevView:
     """Exposes a raw device range through __cuda_array_interface__ for torch.as_tensor."""
 
     def __init__(self, ptr: int, shape: Sequence[int], typestr: str):
-        self.__cuda_array_interface__ = {"shape": tuple(shape), "typestr": typestr, "data": (ptr, True),
+        self.__cuda_array_interface__ = {"shape": tuple(shape), "typestr": typestr, "data": (ptr, False),
                                          "version": 3, "strides": None}
 
 
@@ -73,9 +73,10 @@ class DitBlock:
         return out
 
     def workspace(self, name: str, shape: Sequence[int]) -> torch.Tensor:
-        """Copy of a workspace buffer of the last forward, viewed with ``shape``."""
+        """Copy of a workspace buffer of the last forward, viewed with ``shape``
+        (H1 is fp32 in both modes, every other buffer is in the storage dtype)."""
         ptr, nbytes = krea_dit_block_workspace(self.handle, name)
-        esz = 2 if self.mode == "bf16" else 4
+        esz = 2 if (self.mode == "bf16" and name != "H1") else 4
         n = 1
         for s in shape:
             n *= s

@@ -156,7 +156,8 @@ const char* krea_dit_status_string(int status);
  *  VT   [B, n_kv, hd, Lp]  dtype, values transposed, Lp = L rounded up to 64
  *  G    [T, n_q hd]        dtype, gate pre-activation (unused when gate_on = 0)
  *  OG   [T, n_q hd]        dtype, o * sigmoid(g)
- *  H1   [T, d]             dtype, block state after the attention residual
+ *  H1   [T, d]             fp32 in both modes, block state after the attention residual
+ *                          (the residual stream between the two residual adds)
  *  HN   [T, d]             dtype, normed+modulated input of the MLP
  *  HMID [T, F]             dtype, silu(hn W_gate^T) * (hn W_up^T) */
 #define KREA_DIT_BUF_XN 0

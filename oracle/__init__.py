@@ -17,6 +17,7 @@ from .block import (  # noqa: F401
     block_forward,
     gqa_attention,
     modulation,
+    round_to_bf16,
     rms_norm,
     rope_angles,
     swiglu,
@@ -34,7 +35,7 @@ def mod_shared_for(case) -> np.ndarray:
 
 
 def run_case(case, rows: Optional[Sequence[np.ndarray]] = None, *, rope_on: bool = True,
-             mod_shared: Optional[np.ndarray] = None) -> Dict[str, list]:
+             mod_shared: Optional[np.ndarray] = None, store=None) -> Dict[str, list]:
     """Timestep embedding plus one block forward for a seeded case (duck-typed:
     ``case.cfg`` shapes, ``case.t``, ``case.temb``, ``case.w``, ``case.x_txt``,
     ``case.x_img``)."""
@@ -43,5 +44,5 @@ def run_case(case, rows: Optional[Sequence[np.ndarray]] = None, *, rope_on: bool
     return block_forward(
         case.x_txt, case.x_img, (cfg.img_h, cfg.img_w), ms, case.w,
         n_q=cfg.n_q, n_kv=cfg.n_kv, hd=cfg.hd, eps=cfg.eps, rope_base=cfg.rope_base,
-        gate_on=cfg.gate_on, rope_on=rope_on, rows=rows,
+        gate_on=cfg.gate_on, rope_on=rope_on, rows=rows, store=store,
     )

@@ -42,12 +42,33 @@ __all__ = [
     "gqa_attention",
     "swiglu",
     "block_forward",
+    "round_to_bf16",
 ]
 
 F64 = np.float64
 TEMB_DIM = 256  # sinusoid width (DiT / FLUX convention; the report says only "sinusoidal")
 TEMB_T_SCALE = 1000.0  # t in [0,1] is scaled to [0,1000] before the sinusoid
 TEMB_MAX_PERIOD = 10000.0
+
+
+def round_to_bf16(x: np.ndarray) -> np.ndarray:
+    """Round float64 values to the nearest bf16 value (8 significant bits), ties to
+    even, directly from float64 (no intermediate float32 rounding)."""
+    x = np.asarray(x, F64)
+    m, e = np.frexp(x)  # x = m * 2^e, 0.5 <= |m| < 1
+    return np.ldexp(np.rint(m * 256.0), e - 8)
+
+
+def storage_rounding(store: Optional[str]):
+    """Identity (exact oracle) or the rounding applied where the CUDA path stores an
+    intermediate in its storage dtype ("bf16" or "fp32")."""
+    if store is None:
+        return lambda a: a
+    if store == "bf16":
+        return round_to_bf16
+    if store == "fp32":
+        return lambda a: np.asarray(a, F64).astype(np.float32).astype(F64)
+    raise ValueError(store)
 
 
 def sigmoid(x: np.ndarray) -> np.ndarray:
@@ -205,6 +226,7 @@ def block_forward(
     gate_on: bool = True,
     rope_on: bool = True,
     rows: Optional[Sequence[np.ndarray]] = None,
+    store=None,
 ) -> Dict[str, list]:
     """One single-stream block forward over the joint [text; image] sequence.
 
@@ -215,6 +237,12 @@ def block_forward(
     ``rows`` (optional, one index array per batch element) restricts the output
     to those joint-sequence rows. Every step except the keys/values is row-local,
     so K and V are still formed for all L rows and the sampled rows are exact.
+
+    ``store``: None is the exact definition. A dtype name ("bf16" or "fp32"), or a dict
+    from intermediate name (xn, q, k, v, g, o_g, h1, hn, hmid, out) to dtype name, rounds
+    those intermediates round-to-nearest-even at the point where an implementation
+    stores them (names missing from the dict stay exact); the arithmetic between
+    stores stays float64.
 
     Returns a dict of per-batch lists: ``rows`` and, for those rows, q and k
     (after QK-norm and RoPE, [n_q|n_kv, R, hd]), v, g, o_g ([R, n_q*hd], the
@@ -235,6 +263,9 @@ def block_forward(
     Wg = w_qkvg[wq_rows + 2 * wk_rows: 2 * wq_rows + 2 * wk_rows] if gate_on else None
     W_o = np.asarray(w["w_o"], F64)
 
+    names = ("xn", "q", "k", "v", "g", "o_g", "h1", "hn", "hmid", "out")
+    smap = store if isinstance(store, dict) else {n: store for n in names}
+    rnd = {n: storage_rounding(smap.get(n)) for n in names}
     pos = token_positions(Nt, H, W)
     ang = rope_angles(pos, hd, rope_base)
 
@@ -245,14 +276,14 @@ def block_forward(
         R = np.arange(L) if rows is None else np.asarray(rows[b], dtype=np.int64)
 
         # pre-norm + modulation: x_norm * (1 + scale) + shift
-        xn = zero_centred_rms_norm(X, w["norm1_w"], eps) * (1.0 + mod["scale_a"][b]) + mod["shift_a"][b]
+        xn = rnd["xn"](zero_centred_rms_norm(X, w["norm1_w"], eps) * (1.0 + mod["scale_a"][b]) + mod["shift_a"][b])
 
         def heads(m, n):  # [L', n*hd] -> [n, L', hd]
             return m.reshape(m.shape[0], n, hd).transpose(1, 0, 2)
 
         # K and V for every row; Q and G for the sampled rows only
         k = heads(xn @ Wk.T, n_kv)
-        v = heads(xn @ Wv.T, n_kv)
+        v = rnd["v"](heads(xn @ Wv.T, n_kv))
         q = heads(xn[R] @ Wq.T, n_q)
         # per-head QK-RMSNorm over head_dim, zero-centred gain
         q = zero_centred_rms_norm(q, w["q_norm_w"], eps)
@@ -260,21 +291,23 @@ def block_forward(
         if rope_on:
             q = apply_rope_2d(q, ang[R])
             k = apply_rope_2d(k, ang)
+        q, k = rnd["q"](q), rnd["k"](k)
 
         o = gqa_attention(q, k, v)  # [n_q, R, hd]
         o = o.transpose(1, 0, 2).reshape(len(R), n_q * hd)
         if gate_on:
-            g = xn[R] @ Wg.T
+            g = rnd["g"](xn[R] @ Wg.T)
             o_g = o * sigmoid(g)  # head-specific elementwise sigmoid gate on the SDPA output
         else:
             g = np.zeros_like(o)
             o_g = o
+        o_g = rnd["o_g"](o_g)
 
         # gated residual ("架构 › 残差设计": standard residual)
-        h1 = X[R] + mod["gate_a"][b] * (o_g @ W_o.T)
-        hn = zero_centred_rms_norm(h1, w["norm2_w"], eps) * (1.0 + mod["scale_m"][b]) + mod["shift_m"][b]
-        hmid = swiglu(hn, w["w_gate"], w["w_up"])
-        out = h1 + mod["gate_m"][b] * (hmid @ np.asarray(w["w_down"], F64).T)
+        h1 = rnd["h1"](X[R] + mod["gate_a"][b] * (o_g @ W_o.T))
+        hn = rnd["hn"](zero_centred_rms_norm(h1, w["norm2_w"], eps) * (1.0 + mod["scale_m"][b]) + mod["shift_m"][b])
+        hmid = rnd["hmid"](swiglu(hn, w["w_gate"], w["w_up"]))
+        out = rnd["out"](h1 + mod["gate_m"][b] * (hmid @ np.asarray(w["w_down"], F64).T))
 
         res["rows"].append(R)
         res["q"].append(q)

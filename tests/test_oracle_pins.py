@@ -411,3 +411,30 @@ def test_planted_timestep_layout_is_caught():
     assert e[0, 0] == 1.0 and e[0, 128] == 0.0
     swapped = np.concatenate([e[:, 128:], e[:, :128]], axis=1)
     assert swapped[0, 0] != 1.0
+
+
+# ------------------------------------------------------------- storage rounding
+def test_round_to_bf16_matches_torch_on_float32_values():
+    rng = np.random.default_rng(9)
+    x = (rng.standard_normal(100000) * np.exp(rng.uniform(-20, 20, 100000))).astype(np.float32).astype(np.float64)
+    ref = torch.from_numpy(x.astype(np.float32)).to(torch.bfloat16).to(torch.float64).numpy()
+    np.testing.assert_array_equal(oracle.round_to_bf16(x), ref)
+
+
+def test_round_to_bf16_ties_to_even():
+    e = 2.0 ** -8
+    cases = {1.0 + e: 1.0, 1.0 + 3 * e: 1.0 + 4 * e, -(1.0 + e): -1.0, 0.0: 0.0, 1.0 + 1.5 * e: 1.0 + 2 * e,
+             3.0: 3.0, 1.0 - e / 2: 1.0, 1.0 - e: 1.0 - e}
+    for x, want in cases.items():
+        assert oracle.round_to_bf16(np.array([x]))[0] == want, x
+
+
+def test_storage_rounded_oracle_stores_representable_values():
+    case = di.make_case(_small_cfg(dtype="bf16"))
+    r = oracle.run_case(case, store="bf16")
+    for key in ("q", "k", "v", "g", "o_g", "h1", "hn", "hmid", "out"):
+        a = np.concatenate([x.reshape(-1) for x in r[key]])
+        np.testing.assert_array_equal(oracle.round_to_bf16(a), a)
+    exact = oracle.run_case(case)
+    err = np.abs(np.stack(r["out"]) - np.stack(exact["out"])).max()
+    assert 0 < err < 0.05
