@@ -24,6 +24,8 @@ KREA_DIT_ERR_CUDA = -5
 KREA_DIT_ERR_NO_DEVICE = -6
 KREA_DIT_ERR_DEVICE_TIMEOUT = -7
 KREA_DIT_ERR_INJECTED = -8
+KREA_DIT_ERR_SCRATCH_TOO_SMALL = -9
+KREA_DIT_NOALLOC_SCRATCH_FLOATS = 262144
 KREA_DIT_BF16 = 0
 KREA_DIT_FP32 = 1
 BUFFERS = {"XN": 0, "Q": 1, "K": 2, "VT": 3, "G": 4, "OG": 5, "H1": 6, "HN": 7, "HMID": 8}
@@ -33,7 +35,7 @@ EXPORTS = [
     "krea_dit_block_create", "krea_dit_block_destroy", "krea_dit_timestep_embed", "krea_dit_block_forward",
     "krea_dit_status_string", "krea_dit_block_workspace", "krea_dit_block_set_timing",
     "krea_dit_block_kernel_times", "krea_dit_block_timing_reset", "krea_dit_block_device_status",
-    "krea_dit_block_inject_fault", "krea_dit_kernel_names",
+    "krea_dit_block_inject_fault", "krea_dit_kernel_names", "krea_dit_timestep_embed_noalloc",
 ]
 
 
@@ -84,6 +86,7 @@ def lib() -> ctypes.CDLL:
         L.krea_dit_block_device_status.argtypes = [vp, vp, ctypes.POINTER(ci)]
         L.krea_dit_block_inject_fault.argtypes = [vp, ci]
         L.krea_dit_kernel_names.argtypes = [ctypes.POINTER(ctypes.c_char_p), ci]
+        L.krea_dit_timestep_embed_noalloc.argtypes = [vp, ci, ci, ctypes.POINTER(krea_dit_temb_weights), vp, vp]
         for name in EXPORTS:
             getattr(L, name)  # every declared symbol must resolve
             if name != "krea_dit_status_string":
@@ -130,6 +133,13 @@ def krea_dit_block_destroy(handle: int) -> None:
 def krea_dit_timestep_embed(handle: int, t, B: int, w: krea_dit_temb_weights, mod_shared, stream=None) -> None:
     _check(lib().krea_dit_timestep_embed(handle, _ptr(t), B, ctypes.byref(w), _ptr(mod_shared), _stream(stream)),
            "krea_dit_timestep_embed")
+
+
+def krea_dit_timestep_embed_noalloc(t, B: int, d_model: int, w: krea_dit_temb_weights, mod_shared,
+                                    stream=None) -> None:
+    """Handle-free timestep embedding with fixed library-owned scratch (see the header)."""
+    _check(lib().krea_dit_timestep_embed_noalloc(_ptr(t), B, d_model, ctypes.byref(w), _ptr(mod_shared),
+                                                 _stream(stream)), "krea_dit_timestep_embed_noalloc")
 
 
 def krea_dit_block_forward(handle: int, x_img, x_txt, B: int, img_h: int, img_w: int, n_txt: int, t_emb,

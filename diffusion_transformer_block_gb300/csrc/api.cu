@@ -201,6 +201,7 @@ const char* krea_dit_status_string(int s) {
     case KREA_DIT_ERR_NO_DEVICE: return "current device is not an sm_103 GPU";
     case KREA_DIT_ERR_DEVICE_TIMEOUT: return "a bounded on-device wait expired";
     case KREA_DIT_ERR_INJECTED: return "injected fault";
+    case KREA_DIT_ERR_SCRATCH_TOO_SMALL: return "call needs more than the no-alloc entry point's fixed scratch";
     default: return "unknown status";
   }
 }

@@ -56,6 +56,7 @@ extern "C" {
 #define KREA_DIT_ERR_NO_DEVICE (-6)            /* current device is not an sm_103 GPU */
 #define KREA_DIT_ERR_DEVICE_TIMEOUT (-7)       /* a bounded on-device wait expired (see krea_dit_block_device_status) */
 #define KREA_DIT_ERR_INJECTED (-8)             /* host-side fault injection fired (testing aid) */
+#define KREA_DIT_ERR_SCRATCH_TOO_SMALL (-9)    /* call needs more than the no-alloc entry point's fixed scratch */
 
 /* ---- modes -------------------------------------------------------------------------- */
 #define KREA_DIT_BF16 0
@@ -142,6 +143,28 @@ int krea_dit_timestep_embed(krea_dit_block_t h, const float* t, int B, const kre
 int krea_dit_block_forward(krea_dit_block_t h, const void* x_img, const void* x_txt, int B, int img_h,
                            int img_w, int n_txt, const float* t_emb, const krea_dit_weights* w, void* out,
                            krea_dit_stream_t stream);
+
+/* Timestep embedding that allocates nothing (no counterpart in the Krea 2 report: it
+ * exists for callers, not for the method). For callers that cannot call cudaMalloc, e.g.
+ * a serving runtime that reserves all device memory for its own pool and forbids
+ * allocations after start-up, or a latency-critical loop where an allocation could
+ * block behind other streams. It needs no handle and computes the same mod_shared as
+ * krea_dit_timestep_embed.
+ *  t          device fp32 [B]
+ *  B, d_model B >= 0, d_model > 0, and B * (256 + d_model) <= KREA_DIT_NOALLOC_SCRATCH_FLOATS,
+ *             else KREA_DIT_ERR_SCRATCH_TOO_SMALL (e.g. d = 3072 allows B <= 78)
+ *  w          timestep-MLP weights as for krea_dit_timestep_embed
+ *  mod_shared device fp32 [B, 6, d_model], written
+ * Scratch lives in one fixed file-scope device array of KREA_DIT_NOALLOC_SCRATCH_FLOATS
+ * floats (1 MiB) that every GPU loading the library holds until the process exits. The
+ * first call on a device looks up the array's device address (with that device
+ * current) and caches it; make that first call before any stream capture. Every call
+ * shares the array and writes all scratch it reads, so nothing carries over between
+ * calls, but calls that overlap on the GPU (two streams, two threads) race. It calls
+ * no cudaMalloc, cudaFree or allocating library routine. */
+#define KREA_DIT_NOALLOC_SCRATCH_FLOATS 262144
+int krea_dit_timestep_embed_noalloc(const float* t, int B, int d_model, const krea_dit_temb_weights* w,
+                                    float* mod_shared, krea_dit_stream_t stream);
 
 /* Static text for a status code. Never NULL. */
 const char* krea_dit_status_string(int status);

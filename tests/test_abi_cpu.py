@@ -40,7 +40,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 def test_status_strings(lib):
     assert lib.krea_dit_status_string(0) == "ok"
-    for code in range(-8, 0):
+    for code in range(-9, 0):
         assert lib.krea_dit_status_string(code) != "unknown status"
     assert lib.krea_dit_status_string(-99) == "unknown status"
 
