@@ -83,13 +83,13 @@ def kernel_work(cfg):
     T, d, hd, F = cfg.T, cfg.d, cfg.hd, cfg.F
     nq, nkv = cfg.n_q, cfg.n_kv
     n_qkvg = ((2 if cfg.gate_on else 1) * nq + 2 * nkv) * hd
-    act = 2  # bf16 bytes
+    act = 2  # bf16 bytes; the residual stream h1 is fp32
     return {
         "norm1_modulate": ("hbm", 2.0 * T * d * act, "bytes"),
         "qkvg_gemm_qknorm_rope": ("tensor", 2.0 * T * d * n_qkvg, "flops"),
         "attention_gate": ("tensor", 4.0 * cfg.B * cfg.L * cfg.L * nq * hd, "flops"),
         "oproj_gemm_residual": ("tensor", 2.0 * T * nq * hd * d, "flops"),
-        "norm2_modulate": ("hbm", 2.0 * T * d * act, "bytes"),
+        "norm2_modulate": ("hbm", T * d * (4.0 + act), "bytes"),
         "upgate_gemm_swiglu": ("tensor", 2.0 * T * d * 2 * F, "flops"),
         "down_gemm_residual": ("tensor", 2.0 * T * F * d, "flops"),
     }
@@ -101,6 +101,7 @@ class ClockSampler:
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    PERIOD_MS = 20
 
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
@@ -111,7 +112,7 @@ class ClockSampler:
     def start(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                          "--format=csv,noheader,nounits", "-lms", str(self.PERIOD_MS)],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except (OSError, FileNotFoundError):
             self.proc = None
@@ -121,7 +122,10 @@ class ClockSampler:
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.perf_counter(), line.strip()))
+
+    def mark(self, which: str):
+        setattr(self, which, time.perf_counter())
 
     def stop(self):
         if self.proc is None:
@@ -135,7 +139,11 @@ class ClockSampler:
             self.thread.join(timeout=5)
         sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        t0 = getattr(self, "t_begin", None)
+        t1 = getattr(self, "t_end", None)
+        for ts, ln in self.lines:
+            if t0 is not None and t1 is not None and not (t0 <= ts <= t1 + self.PERIOD_MS / 1000.0):
+                continue  # keep samples taken during the timed region only
             p = [x.strip() for x in ln.split(",")]
             if len(p) < 9:
                 continue
@@ -263,15 +271,18 @@ def run_ours(args, cfg):
     clocks = ClockSampler(local)
     clocks.start()
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    time.sleep(0.3)  # let the sampler start
     barrier(world)
     torch.cuda.synchronize()
     wall0 = time.perf_counter()
+    clocks.mark("t_begin")
     for i in range(args.steps):
         flush.zero_()
         evs[i][0].record(stream)
         step()
         evs[i][1].record(stream)
     torch.cuda.synchronize()
+    clocks.mark("t_end")
     barrier(world)
     wall = time.perf_counter() - wall0
     clk = clocks.stop()
@@ -382,12 +393,12 @@ def run_ours(args, cfg):
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="1024px")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--cpu-rows", type=int, default=1024, help="query rows of the CPU-baseline oracle sample")
-    ap.add_argument("--ref-rows", type=int, default=256, help="query rows per reference-arm step")
+    ap.add_argument("--cpu-rows", type=int, default=4608, help="query rows of the CPU-baseline oracle sample")
+    ap.add_argument("--ref-rows", type=int, default=1024, help="query rows per reference-arm step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
     if args.warmup < 3:
