@@ -53,6 +53,12 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+__device__ __forceinline__ float max3f(float x, float y, float z) {
+  float m;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(m) : "f"(x), "f"(y), "f"(z));
+  return m;
+}
+
 __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, int* err, int site) {
   const unsigned long long t0 = globaltimer_ns();
   while (!mbar_try_wait(bar, parity)) {
@@ -92,15 +98,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const int bk = unit / a.npairs;  // b * n_kv + kv
   const int b = bk / a.n_kv, kvh = bk - b * a.n_kv;
   const int ntiles = a.G * a.nqt;
-  const int tile_i[2] = {2 * p, 2 * p + 1};
-  const bool has1 = tile_i[1] < ntiles;
-  int head[2], qt[2];
-#pragma unroll
-  for (int t = 0; t < 2; ++t) {
-    const int i = tile_i[t] < ntiles ? tile_i[t] : tile_i[0];
-    head[t] = kvh * a.G + i / a.nqt;
-    qt[t] = i % a.nqt;
-  }
+  const bool has1 = 2 * p + 1 < ntiles;
+  // query tile t of the unit = (head, query-tile index) of group tile 2p + t
+  auto tile_head = [&](int t) { return kvh * a.G + (2 * p + t) / a.nqt; };
+  auto tile_qt = [&](int t) { return (2 * p + t) % a.nqt; };
   const int nkt = a.nkt;
 
   if (threadIdx.x == 0) {
@@ -137,8 +138,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       mbar_arrive_expect_tx(bar_q, (has1 ? 2 : 1) * TILE_BYTES);
       for (int t = 0; t < (has1 ? 2 : 1); ++t)
         for (int kh = 0; kh < 2; ++kh)
-          tma_load_3d(smem + SMEM_Q + t * TILE_BYTES + kh * HALF_BYTES, &tm_q, bar_q, kh * 64, qt[t] * BQ,
-                      b * a.n_q + head[t]);
+          tma_load_3d(smem + SMEM_Q + t * TILE_BYTES + kh * HALF_BYTES, &tm_q, bar_q, kh * 64, tile_qt(t) * BQ,
+                      b * a.n_q + tile_head(t));
       int n = 0;
       bool ok = true;
       for (int j = 0; ok && j < nkt; ++j) {
@@ -249,26 +250,32 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
         tc_fence_after();
         const int kvalid = a.L - j * BKV;  // keys of this tile inside the sequence (>= 1)
-        // pass 1: row max of the tile
-        float mx = -INFINITY;
-        uint32_t r[32];
-#pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-          tmem_ld32(tS + c * 32, r);
+        uint32_t sv[128];
+        // S row of this thread; keys past L (ragged last tile, same for the whole warp) -> -inf
+        auto load_s = [&]() {
+          tmem_ld128(tS, sv);
+          if (kvalid < BKV) {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const float s = (c * 32 + i < kvalid) ? __uint_as_float(r[i]) : -INFINITY;
-            mx = fmaxf(mx, s);
+            for (int i = 0; i < 128; ++i)
+              if (i >= kvalid) sv[i] = __float_as_uint(-INFINITY);
           }
-        }
-        mx *= a.scale_log2;
+        };
+        load_s();
+        float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};  // 4 independent chains
+#pragma unroll
+        for (int i = 0; i < 128; i += 8)
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            mq[q] = max3f(mq[q], __uint_as_float(sv[i + 2 * q]), __uint_as_float(sv[i + 2 * q + 1]));
+        const float mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3])) * a.scale_log2;
         bool waited = false;
         if (j == 0) {
           m_run = mx;
         } else if (__any_sync(0xffffffffu, mx > m_run + RESCALE_THRESHOLD)) {
           // Some row's max grew by more than 2^8: the whole warp rescales (the TMEM
           // accesses are warp-collective), each row to its own new max (alpha = 1 for a
-          // row whose max did not grow), after the previous P V has landed.
+          // row whose max did not grow), after the previous P V has landed. S is read
+          // again afterwards so the S row and the O chunk are never live together.
           const bool w2 = mbar_wait(&o_done[t], static_cast<uint32_t>((j - 1) & 1), wc, SITE_ATTN_SOFTMAX);
           if (!__all_sync(0xffffffffu, w2)) { ok = false; break; }
           waited = true;
@@ -276,6 +283,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const float m_new = fmaxf(m_run, mx);
           const float alpha = ex2(m_run - m_new);
           l_run *= alpha;
+          uint32_t r[32];
 #pragma unroll 1
           for (int c = 0; c < 4; ++c) {
             tmem_ld32(tO + c * 32, r);
@@ -285,6 +293,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
           tmem_st_wait();
           m_run = m_new;
+          load_s();
         }
         // the previous P V must have read the P buffer before it is overwritten
         if (j > 0 && !waited) {
@@ -292,27 +301,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           if (!__all_sync(0xffffffffu, w3)) { ok = false; break; }
           tc_fence_after();
         }
-        // pass 2: P = exp2(s * scale - m), bf16 into the swizzled P tile; row sum in fp32
-        float sum = 0.f;
-#pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-          tmem_ld32(tS + c * 32, r);
-          uint32_t pk[16];
+        // P = exp2(s * scale - m) in bf16 into the swizzled P tile; row sum in fp32
+        const float2 sc2 = make_float2(a.scale_log2, a.scale_log2);
+        const float2 nm2 = make_float2(-m_run, -m_run);
+        float2 sum2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                          make_float2(0.f, 0.f)};  // 4 independent chains
 #pragma unroll
-          for (int i = 0; i < 32; i += 2) {
-            const int col = c * 32 + i;
-            const float p0 = (col < kvalid) ? ex2(fmaf(__uint_as_float(r[i]), a.scale_log2, -m_run)) : 0.f;
-            const float p1 = (col + 1 < kvalid) ? ex2(fmaf(__uint_as_float(r[i + 1]), a.scale_log2, -m_run)) : 0.f;
-            sum += p0 + p1;
-            pk[i / 2] = pack_bf16x2(p0, p1);
+        for (int c16 = 0; c16 < 16; ++c16) {  // 16-byte chunks of 8 keys
+          uint32_t pk[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int i = c16 * 8 + 2 * q;
+            const float2 x = __ffma2_rn(make_float2(__uint_as_float(sv[i]), __uint_as_float(sv[i + 1])), sc2, nm2);
+            const float2 pr = make_float2(ex2(x.x), ex2(x.y));
+            sum2[q] = __fadd2_rn(sum2[q], pr);
+            pk[q] = pack_bf16x2(pr.x, pr.y);
           }
-          // columns c*32 .. c*32+31 = half (c >> 1), 16-byte chunks (c & 1) * 4 .. + 3
-          uint8_t* hb = pbuf + (c >> 1) * HALF_BYTES;
-#pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4)
-            *reinterpret_cast<uint4*>(hb + sw128_off(row, (c & 1) * 4 + q4)) =
-                make_uint4(pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2], pk[4 * q4 + 3]);
+          *reinterpret_cast<uint4*>(pbuf + (c16 >> 3) * HALF_BYTES + sw128_off(row, c16 & 7)) =
+              make_uint4(pk[0], pk[1], pk[2], pk[3]);
         }
+        const float2 s01 = __fadd2_rn(sum2[0], sum2[1]), s23 = __fadd2_rn(sum2[2], sum2[3]);
+        const float sum = (s01.x + s01.y) + (s23.x + s23.y);
         l_run += sum;
         fence_proxy_async_smem();  // P visible to the tensor core
         tc_fence_before();         // S reads (and any O rescale) ordered before the MMA
@@ -325,10 +334,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
       if (ok) {
         tc_fence_after();
-        const int ql = qt[t] * BQ + row;  // query position in the sequence
+        const int ql = tile_qt(t) * BQ + row;  // query position in the sequence
         const bool valid = ql < a.L;
         const float inv_l = 1.0f / l_run;
-        const size_t off = (static_cast<size_t>(b) * a.L + (valid ? ql : 0)) * (a.n_q * HD) + head[t] * HD;
+        const size_t off = (static_cast<size_t>(b) * a.L + (valid ? ql : 0)) * (a.n_q * HD) + tile_head(t) * HD;
         uint32_t r[32];
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {
