@@ -6,19 +6,24 @@
 // same K/V tiles from shared memory, so every K/V tile loaded is used by two query
 // tiles; the other query tiles of the group re-read the group's K/V from L2.
 //
-// Per unit, for each 128-key K/V tile j:
-//   S_t   = Q_t K_j^T            (tensor core, fp32 in TMEM, t = 0, 1)
-//   P_t   = exp2(S_t * log2(e)/sqrt(hd) - m_t)   (softmax warpgroup t, one thread per row,
-//                                   bf16 into 128B-swizzled shared memory)
-//   O_t  += P_t V_j               (tensor core, fp32 in TMEM)
-// The running max m_t is raised only when the tile max exceeds it by more than 2^8 (then
-// O_t is rescaled in TMEM), so most tiles skip the rescale. The two tiles ping-pong:
-// while warpgroup 0 turns S_0 into P_0 the tensor core runs tile 1's products.
+// Per unit, for each 128-key K/V tile j and query tile t = 0, 1:
+//   S_t  = Q_t K_j^T        tensor core, both operands in shared memory, fp32 in TMEM
+//   P_t  = exp2(S_t * log2(e)/sqrt(hd) - m_t)
+//                           softmax warpgroup t, one thread per row: S read from TMEM,
+//                           P written back as bf16 over the first 64 columns of S_t
+//   O_t += P_t V_j          tensor core, A operand (P) from TMEM, V^T from shared memory
+// The tensor core runs one CTA's MMAs in issue order, so S_t(j+1) (issued after
+// O_t += P_t(j) V_j) overwrites P_t only after it was read, and S_t(j+1) landing means
+// O_t is idle: the softmax may rescale it in TMEM without another wait. The running max
+// is raised only when a row's tile max exceeds it by more than 2^8, so most tiles skip
+// the rescale. The two tiles ping-pong: the tensor core runs one tile's products while
+// the other tile's softmax runs.
 // Epilogue: O_t / l_t * sigmoid(g) -> bf16 [T, n_q*hd].
 //
 // Warps 0-3: softmax/epilogue for tile 0, warps 4-7: tile 1, warp 8: TMA loads,
-// warp 9: TMEM allocation + MMA issue. TMEM: S_0, S_1, O_0, O_1 (4 x 128 columns).
-// Shared memory: Q_0, Q_1 (32 KB each), a 3-slot ring of 32 KB K or V^T tiles, P_0, P_1.
+// warp 9: TMEM allocation + MMA issue. TMEM: S_0/P_0, S_1/P_1, O_0, O_1 (4 x 128
+// columns). Shared memory: Q_0, Q_1 (32 KB each) and a 5-slot ring of 32 KB K or V^T
+// tiles (224 KB).
 #include "common.cuh"
 #include "internal.h"
 
@@ -30,12 +35,11 @@ constexpr int BQ = 128;            // query rows per tile
 constexpr int BKV = 128;           // keys per K/V tile
 constexpr int TILE_BYTES = 128 * 128 * 2;  // one 128 x 128 bf16 operand (two 64-col swizzled halves)
 constexpr int HALF_BYTES = TILE_BYTES / 2;
-constexpr int NSLOT = 3;
+constexpr int NSLOT = 5;
 constexpr int NUM_THREADS = 320;
 constexpr int SMEM_Q = 0;
 constexpr int SMEM_KV = SMEM_Q + 2 * TILE_BYTES;
-constexpr int SMEM_P = SMEM_KV + NSLOT * TILE_BYTES;
-constexpr int SMEM_BAR = SMEM_P + 2 * TILE_BYTES;
+constexpr int SMEM_BAR = SMEM_KV + NSLOT * TILE_BYTES;
 constexpr int SMEM_BYTES = SMEM_BAR + 256 + 1024;
 constexpr float RESCALE_THRESHOLD = 8.0f;  // log2 units: rescale O only if the max grows by > 2^8
 
@@ -69,12 +73,6 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, int* 
   }
 }
 
-// Byte offset of the 16-byte chunk `c16` (8 bf16 of K) of row `r` inside a 128-row x
-// 64-column K-major tile with the 128-byte swizzle (the layout TMA writes).
-__device__ __forceinline__ uint32_t sw128_off(int r, int c16) {
-  return static_cast<uint32_t>(r * 128 + ((c16 ^ (r & 7)) << 4));
-}
-
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_vt, AttnArgs a) {
@@ -82,11 +80,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + SMEM_BAR);
   uint64_t* bar_q = bar + 0;
-  uint64_t* kv_full = bar + 1;          // [NSLOT]
-  uint64_t* kv_empty = bar + 1 + NSLOT; // [NSLOT]
-  uint64_t* s_full = bar + 1 + 2 * NSLOT;   // [2]
-  uint64_t* p_full = s_full + 2;            // [2]
-  uint64_t* o_done = p_full + 2;            // [2]
+  uint64_t* kv_full = bar + 1;              // [NSLOT]
+  uint64_t* kv_empty = kv_full + NSLOT;     // [NSLOT]
+  uint64_t* s_full = kv_empty + NSLOT;      // [2] S_t(j) landed (and every earlier MMA with it)
+  uint64_t* p_full = s_full + 2;            // [2] P_t(j) written to TMEM by all 128 rows
+  uint64_t* o_done = p_full + 2;            // [2] the last O_t += P_t V landed
   uint64_t* done = o_done + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -131,6 +129,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   if (warp == 8) {
     // ------------------------------------------------------------ TMA loads
+    // Order K_0, V_0, K_1, V_1, ... (load n: K_{n/2} if n is even, V_{n/2} if odd): the
+    // order the MMA warp consumes them. With 5 slots each tile is fetched about two
+    // iterations before it is needed.
     if (lane == 0) {
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
@@ -141,23 +142,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           tma_load_3d(smem + SMEM_Q + t * TILE_BYTES + kh * HALF_BYTES, &tm_q, bar_q, kh * 64, tile_qt(t) * BQ,
                       b * a.n_q + tile_head(t));
       int n = 0;
-      bool ok = true;
-      for (int j = 0; ok && j < nkt; ++j) {
-        for (int which = 0; which < 2; ++which, ++n) {  // 0: K_j, 1: V_j^T
-          const int slot = n % NSLOT;
-          const uint32_t ph = static_cast<uint32_t>((n / NSLOT) & 1);
-          if (!mbar_wait(&kv_empty[slot], ph ^ 1, wc, SITE_ATTN_LOAD)) {
-            ok = false;
-            break;
-          }
-          uint8_t* dst = smem + SMEM_KV + slot * TILE_BYTES;
-          mbar_arrive_expect_tx(&kv_full[slot], TILE_BYTES);
-          for (int h2 = 0; h2 < 2; ++h2) {
-            if (which == 0)
-              tma_load_3d(dst + h2 * HALF_BYTES, &tm_k, &kv_full[slot], h2 * 64, j * BKV, bk);
-            else
-              tma_load_3d(dst + h2 * HALF_BYTES, &tm_vt, &kv_full[slot], j * BKV + h2 * 64, 0, bk);
-          }
+      for (; n < 2 * nkt; ++n) {
+        const int m = n >> 1;
+        const int slot = n % NSLOT;
+        const uint32_t ph = static_cast<uint32_t>((n / NSLOT) & 1);
+        if (!mbar_wait(&kv_empty[slot], ph ^ 1, wc, SITE_ATTN_LOAD)) break;
+        uint8_t* dst = smem + SMEM_KV + slot * TILE_BYTES;
+        mbar_arrive_expect_tx(&kv_full[slot], TILE_BYTES);
+        for (int h2 = 0; h2 < 2; ++h2) {
+          if ((n & 1) == 0)
+            tma_load_3d(dst + h2 * HALF_BYTES, &tm_k, &kv_full[slot], h2 * 64, m * BKV, bk);
+          else
+            tma_load_3d(dst + h2 * HALF_BYTES, &tm_vt, &kv_full[slot], m * BKV + h2 * 64, 0, bk);
         }
       }
       // every copy started here has landed before the CTA exits
@@ -170,8 +166,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_bf16_f32(128, 128);
       const int nt = has1 ? 2 : 1;
-      const uint32_t sQ = smem_u32(smem + SMEM_Q), sKV = smem_u32(smem + SMEM_KV), sP = smem_u32(smem + SMEM_P);
-      auto issue_s = [&](int t, int slot) {  // S_t = Q_t K^T
+      const uint32_t sQ = smem_u32(smem + SMEM_Q), sKV = smem_u32(smem + SMEM_KV);
+      auto issue_s = [&](int t, int slot) {  // S_t = Q_t K^T (both operands in shared memory)
         const uint32_t d = tmem + t * 128;
 #pragma unroll
         for (int kh = 0; kh < 2; ++kh)
@@ -181,19 +177,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         sdesc_kmajor_sw128(sKV + slot * TILE_BYTES + kh * HALF_BYTES + ks * 32), idesc,
                         (kh | ks) != 0 ? 1u : 0u);
       };
-      auto issue_pv = [&](int t, int slot, bool acc) {  // O_t += P_t V
+      auto issue_pv = [&](int t, int slot, bool acc) {  // O_t += P_t V (P from TMEM)
         const uint32_t d = tmem + 256 + t * 128;
+        const uint32_t ap = tmem + t * 128;  // P_t: 64 columns of bf16 pairs over S_t
 #pragma unroll
-        for (int kh = 0; kh < 2; ++kh)
-#pragma unroll
-          for (int ks = 0; ks < 4; ++ks)
-            mma_bf16_ss(d, sdesc_kmajor_sw128(sP + t * TILE_BYTES + kh * HALF_BYTES + ks * 32),
-                        sdesc_kmajor_sw128(sKV + slot * TILE_BYTES + kh * HALF_BYTES + ks * 32), idesc,
-                        (acc || (kh | ks) != 0) ? 1u : 0u);
+        for (int ks = 0; ks < 8; ++ks)       // 16 keys per step: 8 TMEM columns of P
+          mma_bf16_ts(d, ap + ks * 8,
+                      sdesc_kmajor_sw128(sKV + slot * TILE_BYTES + (ks >> 2) * HALF_BYTES + (ks & 3) * 32), idesc,
+                      (acc || ks != 0) ? 1u : 0u);
       };
+      auto kv_ph = [](int n) { return static_cast<uint32_t>((n / NSLOT) & 1); };
       bool ok = mbar_wait(bar_q, 0, wc, SITE_ATTN_MMA);
-      // K_0 is load 0
-      if (ok) ok = mbar_wait(&kv_full[0], 0, wc, SITE_ATTN_MMA);
+      if (ok) ok = mbar_wait(&kv_full[0], 0, wc, SITE_ATTN_MMA);  // K_0 is load 0
       if (ok) {
         tc_fence_after();
         for (int t = 0; t < nt; ++t) {
@@ -205,62 +200,52 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       for (int j = 0; ok && j < nkt; ++j) {
         const int nv = 2 * j + 1, nk = 2 * j + 2;  // load indices of V_j and K_{j+1}
         const int sv = nv % NSLOT, sk = nk % NSLOT;
-        const uint32_t pj = static_cast<uint32_t>(j & 1);
+        const bool more = j + 1 < nkt;
+        if (!mbar_wait(&kv_full[sv], kv_ph(nv), wc, SITE_ATTN_MMA)) break;
+        if (more && !mbar_wait(&kv_full[sk], kv_ph(nk), wc, SITE_ATTN_MMA)) break;
         for (int t = 0; ok && t < nt; ++t) {
-          if (!mbar_wait(&p_full[t], pj, wc, SITE_ATTN_MMA)) { ok = false; break; }
-          if (t == 0 && !mbar_wait(&kv_full[sv], static_cast<uint32_t>((nv / NSLOT) & 1), wc, SITE_ATTN_MMA)) {
+          if (!mbar_wait(&p_full[t], static_cast<uint32_t>(j & 1), wc, SITE_ATTN_MMA)) {
             ok = false;
             break;
           }
           tc_fence_after();
           issue_pv(t, sv, j > 0);
-          mma_commit(&o_done[t]);
-          if (j + 1 < nkt) {
-            if (t == 0 &&
-                !mbar_wait(&kv_full[sk], static_cast<uint32_t>((nk / NSLOT) & 1), wc, SITE_ATTN_MMA)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            issue_s(t, sk);
+          if (!more) mma_commit(&o_done[t]);
+          if (more) {
+            issue_s(t, sk);  // after the P V above: it overwrites P_t only once P_t was read
             mma_commit(&s_full[t]);
           }
         }
         if (!ok) break;
         mma_commit(&kv_empty[sv]);
-        if (j + 1 < nkt) mma_commit(&kv_empty[sk]);
+        if (more) mma_commit(&kv_empty[sk]);
       }
       mma_commit(done);
       drain_wait(done, 0, a.err, SITE_ATTN_TEARDOWN);
     }
   } else {
     // ------------------------------------------------------------ softmax + epilogue
-    const int t = warp >> 2;         // query tile of this warpgroup
-    const int quad = warp & 3;       // TMEM lane quadrant
+    const int t = warp >> 2;           // query tile of this warpgroup
+    const int quad = warp & 3;         // TMEM lane quadrant
     const int row = quad * 32 + lane;  // row inside the query tile
     if (t == 0 || has1) {
       const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
       const uint32_t tS = tmem + lane_off + t * 128;
       const uint32_t tO = tmem + lane_off + 256 + t * 128;
-      uint8_t* pbuf = smem + SMEM_P + t * TILE_BYTES;
       float m_run = -INFINITY, l_run = 0.f;
       bool ok = true;
       for (int j = 0; j < nkt; ++j) {
         const bool got = mbar_wait(&s_full[t], static_cast<uint32_t>(j & 1), wc, SITE_ATTN_SOFTMAX);
         if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
         tc_fence_after();
-        const int kvalid = a.L - j * BKV;  // keys of this tile inside the sequence (>= 1)
         uint32_t sv[128];
-        // S row of this thread; keys past L (ragged last tile, same for the whole warp) -> -inf
-        auto load_s = [&]() {
-          tmem_ld128(tS, sv);
-          if (kvalid < BKV) {
+        tmem_ld128(tS, sv);
+        const int kvalid = a.L - j * BKV;  // keys of this tile inside the sequence (>= 1)
+        if (kvalid < BKV) {  // ragged last tile (same for the whole warp): keys past L get -inf
 #pragma unroll
-            for (int i = 0; i < 128; ++i)
-              if (i >= kvalid) sv[i] = __float_as_uint(-INFINITY);
-          }
-        };
-        load_s();
+          for (int i = 0; i < 128; ++i)
+            if (i >= kvalid) sv[i] = __float_as_uint(-INFINITY);
+        }
         float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};  // 4 independent chains
 #pragma unroll
         for (int i = 0; i < 128; i += 8)
@@ -268,19 +253,36 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           for (int q = 0; q < 4; ++q)
             mq[q] = max3f(mq[q], __uint_as_float(sv[i + 2 * q]), __uint_as_float(sv[i + 2 * q + 1]));
         const float mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3])) * a.scale_log2;
-        bool waited = false;
+        // Lazy rescale: raise the running max only when some row's tile max exceeds it by
+        // more than 2^8. The decision is warp-uniform because the O rescale uses
+        // warp-collective TMEM accesses; each row moves to its own new max (alpha = 1 for
+        // a row whose max did not grow).
+        bool rescale = false;
+        float m_new = m_run;
         if (j == 0) {
-          m_run = mx;
+          m_new = mx;
         } else if (__any_sync(0xffffffffu, mx > m_run + RESCALE_THRESHOLD)) {
-          // Some row's max grew by more than 2^8: the whole warp rescales (the TMEM
-          // accesses are warp-collective), each row to its own new max (alpha = 1 for a
-          // row whose max did not grow), after the previous P V has landed. S is read
-          // again afterwards so the S row and the O chunk are never live together.
-          const bool w2 = mbar_wait(&o_done[t], static_cast<uint32_t>((j - 1) & 1), wc, SITE_ATTN_SOFTMAX);
-          if (!__all_sync(0xffffffffu, w2)) { ok = false; break; }
-          waited = true;
-          tc_fence_after();
-          const float m_new = fmaxf(m_run, mx);
+          rescale = true;
+          m_new = fmaxf(m_run, mx);
+        }
+        // P = exp2(s * scale - m), bf16 pairs; row sum in fp32
+        const float2 sc2 = make_float2(a.scale_log2, a.scale_log2);
+        const float2 nm2 = make_float2(-m_new, -m_new);
+        float2 sum2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                          make_float2(0.f, 0.f)};  // 4 independent chains
+        uint32_t pk[64];
+#pragma unroll
+        for (int i2 = 0; i2 < 64; ++i2) {
+          const float2 x = __ffma2_rn(make_float2(__uint_as_float(sv[2 * i2]), __uint_as_float(sv[2 * i2 + 1])),
+                                      sc2, nm2);
+          const float2 pr = make_float2(ex2(x.x), ex2(x.y));
+          sum2[i2 & 3] = __fadd2_rn(sum2[i2 & 3], pr);
+          pk[i2] = pack_bf16x2(pr.x, pr.y);
+        }
+        tmem_st64(tS, pk);  // P_t over the first 64 columns of S_t
+        const float2 s01 = __fadd2_rn(sum2[0], sum2[1]), s23 = __fadd2_rn(sum2[2], sum2[3]);
+        const float sum = (s01.x + s01.y) + (s23.x + s23.y);
+        if (rescale) {  // O_t is idle: S_t(j) landing means O_t += P_t(j-1) V landed too
           const float alpha = ex2(m_run - m_new);
           l_run *= alpha;
           uint32_t r[32];
@@ -291,45 +293,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
             tmem_st32(tO + c * 32, r);
           }
-          tmem_st_wait();
-          m_run = m_new;
-          load_s();
         }
-        // the previous P V must have read the P buffer before it is overwritten
-        if (j > 0 && !waited) {
-          const bool w3 = mbar_wait(&o_done[t], static_cast<uint32_t>((j - 1) & 1), wc, SITE_ATTN_SOFTMAX);
-          if (!__all_sync(0xffffffffu, w3)) { ok = false; break; }
-          tc_fence_after();
-        }
-        // P = exp2(s * scale - m) in bf16 into the swizzled P tile; row sum in fp32
-        const float2 sc2 = make_float2(a.scale_log2, a.scale_log2);
-        const float2 nm2 = make_float2(-m_run, -m_run);
-        float2 sum2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
-                          make_float2(0.f, 0.f)};  // 4 independent chains
-#pragma unroll
-        for (int c16 = 0; c16 < 16; ++c16) {  // 16-byte chunks of 8 keys
-          uint32_t pk[4];
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const int i = c16 * 8 + 2 * q;
-            const float2 x = __ffma2_rn(make_float2(__uint_as_float(sv[i]), __uint_as_float(sv[i + 1])), sc2, nm2);
-            const float2 pr = make_float2(ex2(x.x), ex2(x.y));
-            sum2[q] = __fadd2_rn(sum2[q], pr);
-            pk[q] = pack_bf16x2(pr.x, pr.y);
-          }
-          *reinterpret_cast<uint4*>(pbuf + (c16 >> 3) * HALF_BYTES + sw128_off(row, c16 & 7)) =
-              make_uint4(pk[0], pk[1], pk[2], pk[3]);
-        }
-        const float2 s01 = __fadd2_rn(sum2[0], sum2[1]), s23 = __fadd2_rn(sum2[2], sum2[3]);
-        const float sum = (s01.x + s01.y) + (s23.x + s23.y);
+        m_run = m_new;
         l_run += sum;
-        fence_proxy_async_smem();  // P visible to the tensor core
-        tc_fence_before();         // S reads (and any O rescale) ordered before the MMA
+        tmem_st_wait();   // P (and any O rescale) written
+        tc_fence_before();
         mbar_arrive(&p_full[t]);
       }
       // ---- epilogue: wait for the last P V, O / l * sigmoid(g) -> og
       if (ok) {
-        const bool w4 = mbar_wait(&o_done[t], static_cast<uint32_t>((nkt - 1) & 1), wc, SITE_ATTN_SOFTMAX);
+        const bool w4 = mbar_wait(&o_done[t], 0, wc, SITE_ATTN_SOFTMAX);
         ok = __all_sync(0xffffffffu, w4);
       }
       if (ok) {
@@ -337,7 +310,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int ql = tile_qt(t) * BQ + row;  // query position in the sequence
         const bool valid = ql < a.L;
         const float inv_l = 1.0f / l_run;
-        const size_t off = (static_cast<size_t>(b) * a.L + (valid ? ql : 0)) * (a.n_q * HD) + tile_head(t) * HD;
+        const size_t off =
+            (static_cast<size_t>(b) * a.L + (valid ? ql : 0)) * (a.n_q * HD) + tile_head(t) * HD;
         uint32_t r[32];
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {
