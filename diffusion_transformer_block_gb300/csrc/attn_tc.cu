@@ -21,9 +21,13 @@
 // Epilogue: O_t / l_t * sigmoid(g) -> bf16 [T, n_q*hd].
 //
 // Warps 0-3: softmax/epilogue for tile 0, warps 4-7: tile 1, warp 8: TMA loads,
-// warp 9: TMEM allocation + MMA issue. TMEM: S_0/P_0, S_1/P_1, O_0, O_1 (4 x 128
-// columns). Shared memory: Q_0, Q_1 (32 KB each) and a 5-slot ring of 32 KB K or V^T
-// tiles (224 KB).
+// warp 9: TMEM allocation + MMA issue for tile 0, warp 10: MMA issue for tile 1. The
+// tensor core's instruction queue is shallow and every barrier wait costs the issuing
+// thread ~100+ cycles, so each tile has its own issuing thread, which does its K/V
+// waits ahead of time. The two issuers hand a turn back and forth, so their MMA groups
+// strictly alternate (S_0 | S_1 | P_0 V, S_0 | P_1 V, S_1 | ...): the tiles settle in
+// anti-phase, one tile's softmax running under the other tile's MMAs. TMEM: S_0/P_0, S_1/P_1, O_0, O_1 (4 x 128 columns). Shared memory:
+// Q_0, Q_1 (32 KB each) and a 5-slot ring of 32 KB K or V^T tiles (224 KB).
 #include "common.cuh"
 #include "internal.h"
 
@@ -36,7 +40,7 @@ constexpr int BKV = 128;           // keys per K/V tile
 constexpr int TILE_BYTES = 128 * 128 * 2;  // one 128 x 128 bf16 operand (two 64-col swizzled halves)
 constexpr int HALF_BYTES = TILE_BYTES / 2;
 constexpr int NSLOT = 5;
-constexpr int NUM_THREADS = 320;
+constexpr int NUM_THREADS = 352;
 constexpr int SMEM_Q = 0;
 constexpr int SMEM_KV = SMEM_Q + 2 * TILE_BYTES;
 constexpr int SMEM_BAR = SMEM_KV + NSLOT * TILE_BYTES;
@@ -85,8 +89,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   uint64_t* s_full = kv_empty + NSLOT;      // [2] S_t(j) landed (and every earlier MMA with it)
   uint64_t* p_full = s_full + 2;            // [2] P_t(j) written to TMEM by all 128 rows
   uint64_t* o_done = p_full + 2;            // [2] the last O_t += P_t V landed
-  uint64_t* done = o_done + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+  uint64_t* done = o_done + 2;              // [2] every MMA of issuing thread t finished
+  uint64_t* turn = done + 2;                // [2] turn[t]: the other issuer finished its MMAs
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(turn + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -102,18 +107,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   auto tile_qt = [&](int t) { return (2 * p + t) % a.nqt; };
   const int nkt = a.nkt;
 
+  const int nt = has1 ? 2 : 1;  // query tiles (and MMA-issuing threads) of this unit
   if (threadIdx.x == 0) {
     mbar_init(bar_q, 1);
     for (int s = 0; s < NSLOT; ++s) {
       mbar_init(&kv_full[s], 1);
-      mbar_init(&kv_empty[s], 1);
+      mbar_init(&kv_empty[s], nt);  // freed once every issuing thread's MMAs read it
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&s_full[t], 1);
       mbar_init(&p_full[t], 128);
       mbar_init(&o_done[t], 1);
+      mbar_init(&done[t], 1);
+      mbar_init(&turn[t], 1);
     }
-    mbar_init(done, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -130,7 +137,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   if (warp == 8) {
     // ------------------------------------------------------------ TMA loads
     // Order K_0, V_0, K_1, V_1, ... (load n: K_{n/2} if n is even, V_{n/2} if odd): the
-    // order the MMA warp consumes them. With 5 slots each tile is fetched about two
+    // order the MMA warps consume them. With 5 slots each tile is fetched about two
     // iterations before it is needed.
     if (lane == 0) {
       tma_prefetch_desc(&tm_q);
@@ -161,67 +168,76 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       for (int i = (n > NSLOT ? n - NSLOT : 0); i < n; ++i)
         drain_wait(&kv_full[i % NSLOT], static_cast<uint32_t>((i / NSLOT) & 1), a.err, SITE_ATTN_TEARDOWN);
     }
-  } else if (warp == 9) {
-    // ------------------------------------------------------------ MMA issue
-    if (lane == 0) {
+  } else if (warp == 9 || warp == 10) {
+    // ------------------------------------------------------------ MMA issue, tile t
+    const int t = warp - 9;
+    if (lane == 0 && t < nt) {
       constexpr uint32_t idesc = idesc_bf16_f32(128, 128);
-      const int nt = has1 ? 2 : 1;
-      const uint32_t sQ = smem_u32(smem + SMEM_Q), sKV = smem_u32(smem + SMEM_KV);
-      auto issue_s = [&](int t, int slot) {  // S_t = Q_t K^T (both operands in shared memory)
-        const uint32_t d = tmem + t * 128;
+      const uint32_t sQ = smem_u32(smem + SMEM_Q + t * TILE_BYTES), sKV = smem_u32(smem + SMEM_KV);
+      const uint32_t dS = tmem + t * 128;        // S_t, and P_t over its first 64 columns
+      const uint32_t dO = tmem + 256 + t * 128;  // O_t
+      auto issue_s = [&](int slot) {  // S_t = Q_t K^T (both operands in shared memory)
 #pragma unroll
         for (int kh = 0; kh < 2; ++kh)
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks)
-            mma_bf16_ss(d, sdesc_kmajor_sw128(sQ + t * TILE_BYTES + kh * HALF_BYTES + ks * 32),
+            mma_bf16_ss(dS, sdesc_kmajor_sw128(sQ + kh * HALF_BYTES + ks * 32),
                         sdesc_kmajor_sw128(sKV + slot * TILE_BYTES + kh * HALF_BYTES + ks * 32), idesc,
                         (kh | ks) != 0 ? 1u : 0u);
       };
-      auto issue_pv = [&](int t, int slot, bool acc) {  // O_t += P_t V (P from TMEM)
-        const uint32_t d = tmem + 256 + t * 128;
-        const uint32_t ap = tmem + t * 128;  // P_t: 64 columns of bf16 pairs over S_t
+      auto issue_pv = [&](int slot, bool acc) {  // O_t += P_t V (P from TMEM)
 #pragma unroll
-        for (int ks = 0; ks < 8; ++ks)       // 16 keys per step: 8 TMEM columns of P
-          mma_bf16_ts(d, ap + ks * 8,
+        for (int ks = 0; ks < 8; ++ks)  // 16 keys per step: 8 TMEM columns of P
+          mma_bf16_ts(dO, dS + ks * 8,
                       sdesc_kmajor_sw128(sKV + slot * TILE_BYTES + (ks >> 2) * HALF_BYTES + (ks & 3) * 32), idesc,
                       (acc || ks != 0) ? 1u : 0u);
       };
       auto kv_ph = [](int n) { return static_cast<uint32_t>((n / NSLOT) & 1); };
+      // Turns: issuer 0 runs group g = 0, 1, 2, ... after issuer 1 finished its group g - 1;
+      // issuer 1 runs group g after issuer 0 finished its group g. Group 0 is S_t(0), group
+      // j + 1 is P_t(j) V_j followed by S_t(j + 1). turn[t] phase g = "issuer t may run g".
+      const bool two = nt == 2;
+      auto take_turn = [&](int g) {
+        if (!two || (t == 0 && g == 0)) return true;
+        return mbar_wait(&turn[t], static_cast<uint32_t>((t == 0 ? g - 1 : g) & 1), wc, SITE_ATTN_MMA);
+      };
+      auto pass_turn = [&]() {
+        if (two) mbar_arrive(&turn[1 - t]);
+      };
       bool ok = mbar_wait(bar_q, 0, wc, SITE_ATTN_MMA);
       if (ok) ok = mbar_wait(&kv_full[0], 0, wc, SITE_ATTN_MMA);  // K_0 is load 0
+      if (ok) ok = take_turn(0);
       if (ok) {
         tc_fence_after();
-        for (int t = 0; t < nt; ++t) {
-          issue_s(t, 0);
-          mma_commit(&s_full[t]);
-        }
+        issue_s(0);
+        mma_commit(&s_full[t]);
         mma_commit(&kv_empty[0]);
+        pass_turn();
       }
       for (int j = 0; ok && j < nkt; ++j) {
         const int nv = 2 * j + 1, nk = 2 * j + 2;  // load indices of V_j and K_{j+1}
         const int sv = nv % NSLOT, sk = nk % NSLOT;
         const bool more = j + 1 < nkt;
+        // operands first (normally long landed), then the real dependencies
         if (!mbar_wait(&kv_full[sv], kv_ph(nv), wc, SITE_ATTN_MMA)) break;
         if (more && !mbar_wait(&kv_full[sk], kv_ph(nk), wc, SITE_ATTN_MMA)) break;
-        for (int t = 0; ok && t < nt; ++t) {
-          if (!mbar_wait(&p_full[t], static_cast<uint32_t>(j & 1), wc, SITE_ATTN_MMA)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          issue_pv(t, sv, j > 0);
-          if (!more) mma_commit(&o_done[t]);
-          if (more) {
-            issue_s(t, sk);  // after the P V above: it overwrites P_t only once P_t was read
-            mma_commit(&s_full[t]);
-          }
-        }
-        if (!ok) break;
+        if (!mbar_wait(&p_full[t], static_cast<uint32_t>(j & 1), wc, SITE_ATTN_MMA)) break;
+        if (!take_turn(j + 1)) break;
+        tc_fence_after();
+        issue_pv(sv, j > 0);
         mma_commit(&kv_empty[sv]);
-        if (more) mma_commit(&kv_empty[sk]);
+        if (!more) {
+          mma_commit(&o_done[t]);
+          pass_turn();
+          break;
+        }
+        issue_s(sk);  // after the P V above: it overwrites P_t only once P_t was read
+        mma_commit(&s_full[t]);
+        mma_commit(&kv_empty[sk]);
+        pass_turn();
       }
-      mma_commit(done);
-      drain_wait(done, 0, a.err, SITE_ATTN_TEARDOWN);
+      mma_commit(&done[t]);
+      drain_wait(&done[t], 0, a.err, SITE_ATTN_TEARDOWN);
     }
   } else {
     // ------------------------------------------------------------ softmax + epilogue
