@@ -47,7 +47,7 @@ __device__ __forceinline__ const T* row_src_ptr(const RowSrc& s, int m, int L, i
 // ---- kernels_simt.cu (both modes: norm; fp32 mode: everything else) ----
 // input -> output storage types of a norm+modulate launch
 enum class NormIO { BF16_BF16, F32_BF16, F32_F32 };
-// requires d % 8 == 0 and d / 8 <= 1024 (one thread per 8 columns)
+// requires d % 8 == 0 and d <= 8192 (a warp holds a row in registers)
 cudaError_t launch_norm_modulate(NormIO io, const Fwd& f, RowSrc src, const float* gain_w, const float* mod_shared,
                                  const float* mod_bias, int chunk_shift, int chunk_scale, void* out, int num_sms,
                                  cudaStream_t st);
