@@ -36,6 +36,7 @@ EXPORTS = [
     "krea_dit_status_string", "krea_dit_block_workspace", "krea_dit_block_set_timing",
     "krea_dit_block_kernel_times", "krea_dit_block_timing_reset", "krea_dit_block_device_status",
     "krea_dit_block_inject_fault", "krea_dit_kernel_names", "krea_dit_timestep_embed_noalloc",
+    "krea_dit_block_enable_host_io", "krea_dit_block_forward_host", "krea_dit_block_host_sync",
 ]
 
 
@@ -87,6 +88,9 @@ def lib() -> ctypes.CDLL:
         L.krea_dit_block_inject_fault.argtypes = [vp, ci]
         L.krea_dit_kernel_names.argtypes = [ctypes.POINTER(ctypes.c_char_p), ci]
         L.krea_dit_timestep_embed_noalloc.argtypes = [vp, ci, ci, ctypes.POINTER(krea_dit_temb_weights), vp, vp]
+        L.krea_dit_block_enable_host_io.argtypes = [vp]
+        L.krea_dit_block_forward_host.argtypes = L.krea_dit_block_forward.argtypes
+        L.krea_dit_block_host_sync.argtypes = [vp]
         for name in EXPORTS:
             getattr(L, name)  # every declared symbol must resolve
             if name != "krea_dit_status_string":
@@ -146,6 +150,22 @@ def krea_dit_block_forward(handle: int, x_img, x_txt, B: int, img_h: int, img_w:
                            w: krea_dit_weights, out, stream=None) -> None:
     _check(lib().krea_dit_block_forward(handle, _ptr(x_img), _ptr(x_txt), B, img_h, img_w, n_txt, _ptr(t_emb),
                                         ctypes.byref(w), _ptr(out), _stream(stream)), "krea_dit_block_forward")
+
+
+def krea_dit_block_enable_host_io(handle: int) -> None:
+    _check(lib().krea_dit_block_enable_host_io(handle), "krea_dit_block_enable_host_io")
+
+
+def krea_dit_block_forward_host(handle: int, x_img, x_txt, B: int, img_h: int, img_w: int, n_txt: int, t_emb,
+                                w: krea_dit_weights, out, stream=None) -> None:
+    """x_img, x_txt and out are host (ideally pinned) tensors or addresses."""
+    _check(lib().krea_dit_block_forward_host(handle, _ptr(x_img), _ptr(x_txt), B, img_h, img_w, n_txt, _ptr(t_emb),
+                                             ctypes.byref(w), _ptr(out), _stream(stream)),
+           "krea_dit_block_forward_host")
+
+
+def krea_dit_block_host_sync(handle: int) -> None:
+    _check(lib().krea_dit_block_host_sync(handle), "krea_dit_block_host_sync")
 
 
 def krea_dit_block_workspace(handle: int, which: str) -> Tuple[int, int]:

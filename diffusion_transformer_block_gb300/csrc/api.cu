@@ -132,6 +132,14 @@ struct krea_dit_block_s {
   double total_ms[S_COUNT] = {};
   int launches[S_COUNT] = {};
   int inject = 0;
+  // host-buffer path: two staging sets, upload / download streams, events per set
+  bool host_io = false;
+  char* stage = nullptr;
+  size_t stage_in_bytes = 0, stage_out_bytes = 0;
+  cudaStream_t up = nullptr, down = nullptr;
+  cudaEvent_t ev_in[2] = {}, ev_comp[2] = {}, ev_out[2] = {};
+  bool set_used[2] = {};
+  int next_set = 0;
 };
 
 namespace {
@@ -329,6 +337,16 @@ int krea_dit_block_destroy(krea_dit_block_t h) {
   cudaDeviceSynchronize();
   harvest(h);
   for (auto e : h->free_events) cudaEventDestroy(e);
+  if (h->host_io) {
+    for (int i = 0; i < 2; ++i) {
+      cudaEventDestroy(h->ev_in[i]);
+      cudaEventDestroy(h->ev_comp[i]);
+      cudaEventDestroy(h->ev_out[i]);
+    }
+    cudaStreamDestroy(h->up);
+    cudaStreamDestroy(h->down);
+    cudaFree(h->stage);
+  }
   cudaError_t r = cudaFree(h->ws);
   delete h;
   return r == cudaSuccess ? KREA_DIT_OK : KREA_DIT_ERR_CUDA;
@@ -473,6 +491,74 @@ int krea_dit_block_forward(krea_dit_block_t h, const void* x_img, const void* x_
   }
 #undef KD_RUN
   return e == cudaSuccess ? KREA_DIT_OK : KREA_DIT_ERR_CUDA;
+}
+
+int krea_dit_block_enable_host_io(krea_dit_block_t h) {
+  if (!h) return KREA_DIT_ERR_INVALID_ARG;
+  if (h->host_io) return KREA_DIT_OK;
+  const size_t tokens = static_cast<size_t>(h->cfg.max_batch) * h->cfg.max_seq;
+  h->stage_in_bytes = round_up(tokens * h->cfg.d_model * h->esz, 256);
+  h->stage_out_bytes = h->stage_in_bytes;
+  if (cudaMalloc(&h->stage, 2 * (h->stage_in_bytes + h->stage_out_bytes)) != cudaSuccess) return KREA_DIT_ERR_CUDA;
+  bool ok = cudaStreamCreateWithFlags(&h->up, cudaStreamNonBlocking) == cudaSuccess &&
+            cudaStreamCreateWithFlags(&h->down, cudaStreamNonBlocking) == cudaSuccess;
+  for (int i = 0; ok && i < 2; ++i)
+    ok = cudaEventCreateWithFlags(&h->ev_in[i], cudaEventDisableTiming) == cudaSuccess &&
+         cudaEventCreateWithFlags(&h->ev_comp[i], cudaEventDisableTiming) == cudaSuccess &&
+         cudaEventCreateWithFlags(&h->ev_out[i], cudaEventDisableTiming) == cudaSuccess;
+  if (!ok) return KREA_DIT_ERR_CUDA;
+  h->host_io = true;
+  return KREA_DIT_OK;
+}
+
+int krea_dit_block_forward_host(krea_dit_block_t h, const void* x_img, const void* x_txt, int B, int img_h, int img_w,
+                                int n_txt, const float* t_emb, const krea_dit_weights* w, void* out,
+                                krea_dit_stream_t stream) {
+  if (!h || !out) return KREA_DIT_ERR_INVALID_ARG;
+  if (!h->host_io) return KREA_DIT_ERR_INVALID_ARG;
+  if (B < 0 || img_h < 0 || img_w < 0 || n_txt < 0) return KREA_DIT_ERR_INVALID_ARG;
+  const long long n_img = static_cast<long long>(img_h) * img_w, L = n_img + n_txt;
+  if (B > h->cfg.max_batch || L > h->cfg.max_seq) return KREA_DIT_ERR_EXCEEDS_CREATE_LIMITS;
+  if ((n_img > 0 && !x_img) || (n_txt > 0 && !x_txt)) return KREA_DIT_ERR_INVALID_ARG;
+  if (B == 0 || L == 0) return KREA_DIT_OK;
+  const size_t row = static_cast<size_t>(h->cfg.d_model) * h->esz;
+  const size_t img_bytes = static_cast<size_t>(B) * n_img * row, txt_bytes = static_cast<size_t>(B) * n_txt * row;
+  const size_t out_bytes = static_cast<size_t>(B) * L * row;
+  const int k = h->next_set;
+  char* base = h->stage + k * (h->stage_in_bytes + h->stage_out_bytes);
+  char* d_img = base;
+  char* d_txt = base + round_up(img_bytes, 256);
+  char* d_out = base + h->stage_in_bytes;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  // upload: the set's previous forward must have finished reading its inputs
+  if (h->set_used[k] && cudaStreamWaitEvent(h->up, h->ev_comp[k], 0) != cudaSuccess) return KREA_DIT_ERR_CUDA;
+  if (img_bytes && cudaMemcpyAsync(d_img, x_img, img_bytes, cudaMemcpyHostToDevice, h->up) != cudaSuccess)
+    return KREA_DIT_ERR_CUDA;
+  if (txt_bytes && cudaMemcpyAsync(d_txt, x_txt, txt_bytes, cudaMemcpyHostToDevice, h->up) != cudaSuccess)
+    return KREA_DIT_ERR_CUDA;
+  if (cudaEventRecord(h->ev_in[k], h->up) != cudaSuccess) return KREA_DIT_ERR_CUDA;
+  // compute: inputs landed, and the set's previous download has read the output staging
+  if (cudaStreamWaitEvent(st, h->ev_in[k], 0) != cudaSuccess) return KREA_DIT_ERR_CUDA;
+  if (h->set_used[k] && cudaStreamWaitEvent(st, h->ev_out[k], 0) != cudaSuccess) return KREA_DIT_ERR_CUDA;
+  const int r = krea_dit_block_forward(h, n_img ? d_img : nullptr, n_txt ? d_txt : nullptr, B, img_h, img_w, n_txt,
+                                       t_emb, w, d_out, stream);
+  if (r != KREA_DIT_OK) return r;
+  if (cudaEventRecord(h->ev_comp[k], st) != cudaSuccess) return KREA_DIT_ERR_CUDA;
+  // download
+  if (cudaStreamWaitEvent(h->down, h->ev_comp[k], 0) != cudaSuccess) return KREA_DIT_ERR_CUDA;
+  if (cudaMemcpyAsync(out, d_out, out_bytes, cudaMemcpyDeviceToHost, h->down) != cudaSuccess) return KREA_DIT_ERR_CUDA;
+  if (cudaEventRecord(h->ev_out[k], h->down) != cudaSuccess) return KREA_DIT_ERR_CUDA;
+  h->set_used[k] = true;
+  h->next_set = 1 - k;
+  return KREA_DIT_OK;
+}
+
+int krea_dit_block_host_sync(krea_dit_block_t h) {
+  if (!h) return KREA_DIT_ERR_INVALID_ARG;
+  if (!h->host_io) return KREA_DIT_OK;
+  if (cudaStreamSynchronize(h->up) != cudaSuccess || cudaStreamSynchronize(h->down) != cudaSuccess)
+    return KREA_DIT_ERR_CUDA;
+  return KREA_DIT_OK;
 }
 
 int krea_dit_block_workspace(krea_dit_block_t h, int which, void** dev_ptr, size_t* bytes) {

@@ -29,7 +29,10 @@ constexpr int TMEM_COLS = 2 * BN;
 constexpr int NUM_EPI_WARPS = 8;
 constexpr int NUM_THREADS = 64 + NUM_EPI_WARPS * 32;
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*alignment slack*/ + 256 /*barriers*/;
-constexpr int GROUP_M = 16;  // tile raster: GROUP_M m-blocks share each n-block in turn
+#ifndef KD_GEMM_GROUP_M
+#define KD_GEMM_GROUP_M 32
+#endif
+constexpr int GROUP_M = KD_GEMM_GROUP_M;  // tile raster: GROUP_M m-blocks share each n-block in turn
 
 __device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int& mb, int& nb) {
   const int per_group = GROUP_M * num_n;

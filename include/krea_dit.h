@@ -169,6 +169,29 @@ int krea_dit_timestep_embed_noalloc(const float* t, int B, int d_model, const kr
 /* Static text for a status code. Never NULL. */
 const char* krea_dit_status_string(int status);
 
+/* ---- host-buffer forward (end-to-end path) ----------------------------------------- */
+
+/* Prepare the handle for krea_dit_block_forward_host: allocates two device staging sets
+ * (inputs and output for max_batch x max_seq tokens each), two copy streams and their
+ * events. Synchronous; call once, before any stream capture. */
+int krea_dit_block_enable_host_io(krea_dit_block_t h);
+
+/* One block forward from and to host memory. Same operation and arguments as
+ * krea_dit_block_forward except that x_img, x_txt and out are HOST pointers (pinned memory
+ * gives full copy bandwidth); t_emb and the weights stay in device memory. The inputs are
+ * copied into a staging set on the handle's upload stream, the forward runs on `stream`,
+ * and the output is copied back on the handle's download stream. Staging sets alternate
+ * between calls, so the upload of call i+1 and the download of call i-1 overlap the
+ * compute of call i. Returns after enqueueing; the host buffers of a call must stay
+ * valid and untouched until krea_dit_block_host_sync returns. */
+int krea_dit_block_forward_host(krea_dit_block_t h, const void* x_img, const void* x_txt, int B, int img_h,
+                                int img_w, int n_txt, const float* t_emb, const krea_dit_weights* w, void* out,
+                                krea_dit_stream_t stream);
+
+/* Wait until every krea_dit_block_forward_host call enqueued so far has finished,
+ * including its download. */
+int krea_dit_block_host_sync(krea_dit_block_t h);
+
 /* ---- inspection, timing and failure reporting ------------------------------------- */
 
 /* Workspace buffers written by the most recent forward (read-only views, owned by the
