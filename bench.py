@@ -77,6 +77,20 @@ def load_peaks():
     return {**FALLBACK_PEAKS, "bf16_tflops_sustained": FALLBACK_PEAKS["bf16_tflops"], "source": "fallback"}
 
 
+def profile_traffic(workload: str):
+    """Per-launch DRAM traffic (read + write bytes) per kernel from the ncu summary committed
+    under profiles/ for this workload; {} when there is none."""
+    p = os.path.join(ROOT, "profiles", f"dram_traffic_{workload}.md")
+    out = {}
+    if not os.path.exists(p):
+        return out
+    for line in open(p):
+        cells = [c.strip() for c in line.strip().strip("|").split("|")]
+        if len(cells) == 4 and cells[3].isdigit():
+            out[cells[0]] = int(cells[3])
+    return out
+
+
 def kernel_work(cfg):
     """Algorithmic work of one launch of each kernel: (bound, amount, unit).
     FLOPs count a multiply-add as 2; bytes count each tensor read or written once."""
@@ -371,7 +385,7 @@ def run_ours(args, cfg):
         "frac_of_peak": tflops / peaks["bf16_tflops"],
         "peak_source": f"{peaks['source']} bf16 {peaks['bf16_tflops']} TFLOP/s (burst)",
         "roofline": {"kernel": dom, "bound": bound, "achieved": achieved, "peak": peak, "unit": runit,
-                     "frac": achieved / peak, "traffic": None,
+                     "frac": achieved / peak, "traffic": profile_traffic(cfg.name).get(dom),
                      "algorithmic": {"amount_per_launch": amount, "unit": unit}},
         "kernels": per_kernel,
         "cpu_baseline": cpu,
