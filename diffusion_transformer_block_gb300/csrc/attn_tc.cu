@@ -176,23 +176,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const uint32_t sQ = smem_u32(smem + SMEM_Q + t * TILE_BYTES), sKV = smem_u32(smem + SMEM_KV);
       const uint32_t dS = tmem + t * 128;        // S_t, and P_t over its first 64 columns
       const uint32_t dO = tmem + 256 + t * 128;  // O_t
-      auto issue_s = [&](int slot) {  // S_t = Q_t K^T (both operands in shared memory)
-#pragma unroll
-        for (int kh = 0; kh < 2; ++kh)
-#pragma unroll
-          for (int ks = 0; ks < 4; ++ks)
-            mma_bf16_ss(dS, sdesc_kmajor_sw128(sQ + kh * HALF_BYTES + ks * 32),
-                        sdesc_kmajor_sw128(sKV + slot * TILE_BYTES + kh * HALF_BYTES + ks * 32), idesc,
-                        (kh | ks) != 0 ? 1u : 0u);
-      };
-      auto issue_pv = [&](int slot, bool acc) {  // O_t += P_t V (P from TMEM)
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks)  // 16 keys per step: 8 TMEM columns of P
-          mma_bf16_ts(dO, dS + ks * 8,
-                      sdesc_kmajor_sw128(sKV + slot * TILE_BYTES + (ks >> 2) * HALF_BYTES + (ks & 3) * 32), idesc,
-                      (acc || ks != 0) ? 1u : 0u);
-      };
-      auto kv_ph = [](int n) { return static_cast<uint32_t>((n / NSLOT) & 1); };
       // Turns: issuer 0 runs group g = 0, 1, 2, ... after issuer 1 finished its group g - 1;
       // issuer 1 runs group g after issuer 0 finished its group g. Group 0 is S_t(0), group
       // j + 1 is P_t(j) V_j followed by S_t(j + 1). turn[t] phase g = "issuer t may run g".
@@ -204,15 +187,39 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       auto pass_turn = [&]() {
         if (two) mbar_arrive(&turn[1 - t]);
       };
+      // pass_turn() is called inside the last MMA group before its final 4 MMAs: the hand-over
+      // (commit, arrive, the other issuer waking up) then overlaps the tail of this group
+      // instead of leaving the shallow MMA queue empty. The turns only steer scheduling;
+      // the two tiles never share TMEM, so no ordering between them is needed.
+      auto issue_s = [&](int slot, bool pass) {  // S_t = Q_t K^T (both operands in shared memory)
+#pragma unroll
+        for (int kh = 0; kh < 2; ++kh)
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks) {
+            if (pass && kh == 1 && ks == 0) pass_turn();
+            mma_bf16_ss(dS, sdesc_kmajor_sw128(sQ + kh * HALF_BYTES + ks * 32),
+                        sdesc_kmajor_sw128(sKV + slot * TILE_BYTES + kh * HALF_BYTES + ks * 32), idesc,
+                        (kh | ks) != 0 ? 1u : 0u);
+          }
+      };
+      auto issue_pv = [&](int slot, bool acc, bool pass) {  // O_t += P_t V (P from TMEM)
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {  // 16 keys per step: 8 TMEM columns of P
+          if (pass && ks == 4) pass_turn();
+          mma_bf16_ts(dO, dS + ks * 8,
+                      sdesc_kmajor_sw128(sKV + slot * TILE_BYTES + (ks >> 2) * HALF_BYTES + (ks & 3) * 32), idesc,
+                      (acc || ks != 0) ? 1u : 0u);
+        }
+      };
+      auto kv_ph = [](int n) { return static_cast<uint32_t>((n / NSLOT) & 1); };
       bool ok = mbar_wait(bar_q, 0, wc, SITE_ATTN_MMA);
       if (ok) ok = mbar_wait(&kv_full[0], 0, wc, SITE_ATTN_MMA);  // K_0 is load 0
       if (ok) ok = take_turn(0);
       if (ok) {
         tc_fence_after();
-        issue_s(0);
+        issue_s(0, true);
         mma_commit(&s_full[t]);
         mma_commit(&kv_empty[0]);
-        pass_turn();
       }
       for (int j = 0; ok && j < nkt; ++j) {
         const int nv = 2 * j + 1, nk = 2 * j + 2;  // load indices of V_j and K_{j+1}
@@ -224,17 +231,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (!mbar_wait(&p_full[t], static_cast<uint32_t>(j & 1), wc, SITE_ATTN_MMA)) break;
         if (!take_turn(j + 1)) break;
         tc_fence_after();
-        issue_pv(sv, j > 0);
+        issue_pv(sv, j > 0, !more);
         mma_commit(&kv_empty[sv]);
         if (!more) {
           mma_commit(&o_done[t]);
-          pass_turn();
           break;
         }
-        issue_s(sk);  // after the P V above: it overwrites P_t only once P_t was read
+        issue_s(sk, true);  // after the P V above: it overwrites P_t only once P_t was read
         mma_commit(&s_full[t]);
         mma_commit(&kv_empty[sk]);
-        pass_turn();
       }
       mma_commit(&done[t]);
       drain_wait(&done[t], 0, a.err, SITE_ATTN_TEARDOWN);
