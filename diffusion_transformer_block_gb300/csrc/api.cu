@@ -439,13 +439,13 @@ int krea_dit_block_forward(krea_dit_block_t h, const void* x_img, const void* x_
     CUtensorMap tm_xn, tm_wqkvg, tm_og, tm_wo, tm_hn, tm_wgate, tm_wup, tm_hmid, tm_wdown, tm_q, tm_k, tm_vt;
     const uint64_t T = static_cast<uint64_t>(f.T);
     bool ok = encode_2d(&tm_xn, h->xn, d, T, d, 64, 128) &&
-              encode_2d(&tm_wqkvg, w->w_qkvg, d, h->n_qkvg, d, 64, 256) &&
+              encode_2d(&tm_wqkvg, w->w_qkvg, d, h->n_qkvg, d, 64, 128) &&
               encode_2d(&tm_og, h->og, nqhd, T, nqhd, 64, 128) &&
-              encode_2d(&tm_wo, w->w_o, nqhd, d, nqhd, 64, 256) && encode_2d(&tm_hn, h->hn, d, T, d, 64, 128) &&
+              encode_2d(&tm_wo, w->w_o, nqhd, d, nqhd, 64, 128) && encode_2d(&tm_hn, h->hn, d, T, d, 64, 128) &&
               encode_2d(&tm_wgate, w->w_gate, d, c.ffn, d, 64, 128) &&
               encode_2d(&tm_wup, w->w_up, d, c.ffn, d, 64, 128) &&
               encode_2d(&tm_hmid, h->hmid, c.ffn, T, c.ffn, 64, 128) &&
-              encode_2d(&tm_wdown, w->w_down, c.ffn, d, c.ffn, 64, 256) &&
+              encode_2d(&tm_wdown, w->w_down, c.ffn, d, c.ffn, 64, 128) &&
               encode_3d(&tm_q, h->q, c.head_dim, L, static_cast<uint64_t>(B) * c.n_q, c.head_dim, 64, 128) &&
               encode_3d(&tm_k, h->k, c.head_dim, L, static_cast<uint64_t>(B) * c.n_kv, c.head_dim, 64, 128) &&
               encode_3d(&tm_vt, h->vt, L, c.head_dim, static_cast<uint64_t>(B) * c.n_kv, f.Lp, 64, 128);
