@@ -337,6 +337,50 @@ def run_ours(args, cfg):
     h2d = h_img.numel() * h_img.element_size() + h_txt.numel() * h_txt.element_size()
     d2h = h_out[0].numel() * h_out[0].element_size()
 
+    # ---- a stack of blocks (distinct weight buffers per block) in place on the joint
+    # sequence: eager launches vs one CUDA-graph launch per stack; x is reset and L2
+    # flushed before each stack, outside its events
+    stack = None
+    if args.stack_blocks > 0:
+        nb = args.stack_blocks
+        sw = blk.stack_weights([{k: v.clone() for k, v in blk.w.items()} for _ in range(nb)])
+        x0 = torch.cat([x_txt, x_img], dim=1).contiguous()
+        xs = x0.clone()
+        gstream = torch.cuda.Stream(dev)
+        torch.cuda.synchronize()
+        graph = blk.stack_graph(xs, cfg.B, cfg.img_h, cfg.img_w, cfg.n_txt, ms, sw, gstream)
+        k_stack = max(3, min(args.steps, 20))
+
+        def time_stack(run, st):
+            for _ in range(2):
+                xs.copy_(x0)
+                flush.zero_()
+                run()
+            torch.cuda.synchronize()
+            pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                     for _ in range(k_stack)]
+            for a, b in pairs:
+                with torch.cuda.stream(st):
+                    xs.copy_(x0)
+                    flush.zero_()
+                    a.record(st)
+                    run()
+                    b.record(st)
+            torch.cuda.synchronize()
+            return reduce_max(sum(a.elapsed_time(b) for a, b in pairs), world) / k_stack
+
+        eager_ms = time_stack(lambda: blk.stack_forward(xs, cfg.B, cfg.img_h, cfg.img_w, cfg.n_txt, ms, sw,
+                                                        stream=stream), stream)
+        graph_ms = time_stack(lambda: graph.launch(gstream), gstream)
+        graph.close()
+        stack = {"blocks": nb, "stacks_timed": k_stack, "eager_ms_per_stack": eager_ms,
+                 "graph_ms_per_stack": graph_ms, "graph_ms_per_block": graph_ms / nb,
+                 "tokens_per_s_graph": world * cfg.T / (graph_ms / 1000.0),
+                 "tflops_graph": world * di.config_flops(cfg) * nb / (graph_ms / 1000.0) / 1e12,
+                 "how": "krea_dit_stack_forward (eager) and one krea_dit_graph_launch of the captured stack, "
+                        "in place on the joint sequence; CUDA events around each stack"}
+        del sw
+
     # ---- numbers
     tokens_per_step = cfg.T
     ms_per_step = total_ms_max / args.steps
@@ -393,6 +437,7 @@ def run_ours(args, cfg):
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
                 "how": "krea_dit_block_forward_host per step (pinned host in/out), wall clock over the steps "
                        "with device and copy streams synchronised on both sides"},
+        "stack": stack,
         "clocks": clk,
         "gpu_launches": sum(pk["launches"] for pk in per_kernel.values()),
         "wall_s_timed_region": wall,
@@ -417,6 +462,7 @@ def main(argv=None):
     ap.add_argument("--cpu-rows", type=int, default=4608, help="query rows of the CPU-baseline oracle sample")
     ap.add_argument("--ref-rows", type=int, default=1024, help="query rows per reference-arm step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--stack-blocks", type=int, default=8, help="blocks of the stack / CUDA-graph measurement (0: skip)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -37,6 +37,8 @@ EXPORTS = [
     "krea_dit_block_kernel_times", "krea_dit_block_timing_reset", "krea_dit_block_device_status",
     "krea_dit_block_inject_fault", "krea_dit_kernel_names", "krea_dit_timestep_embed_noalloc",
     "krea_dit_block_enable_host_io", "krea_dit_block_forward_host", "krea_dit_block_host_sync",
+    "krea_dit_block_forward_joint", "krea_dit_stack_forward", "krea_dit_stack_graph_create", "krea_dit_graph_launch",
+    "krea_dit_graph_destroy",
 ]
 
 
@@ -91,6 +93,12 @@ def lib() -> ctypes.CDLL:
         L.krea_dit_block_enable_host_io.argtypes = [vp]
         L.krea_dit_block_forward_host.argtypes = L.krea_dit_block_forward.argtypes
         L.krea_dit_block_host_sync.argtypes = [vp]
+        L.krea_dit_block_forward_joint.argtypes = [vp, vp, ci, ci, ci, ci, vp, ctypes.POINTER(krea_dit_weights), vp, vp]
+        L.krea_dit_stack_forward.argtypes = [vp, vp, ci, ci, ci, ci, vp, ctypes.POINTER(krea_dit_weights), ci, vp]
+        L.krea_dit_stack_graph_create.argtypes = [vp, vp, ci, ci, ci, ci, vp, ctypes.POINTER(krea_dit_weights), ci, vp,
+                                                  ctypes.POINTER(vp)]
+        L.krea_dit_graph_launch.argtypes = [vp, vp]
+        L.krea_dit_graph_destroy.argtypes = [vp]
         for name in EXPORTS:
             getattr(L, name)  # every declared symbol must resolve
             if name != "krea_dit_status_string":
@@ -166,6 +174,41 @@ def krea_dit_block_forward_host(handle: int, x_img, x_txt, B: int, img_h: int, i
 
 def krea_dit_block_host_sync(handle: int) -> None:
     _check(lib().krea_dit_block_host_sync(handle), "krea_dit_block_host_sync")
+
+
+def krea_dit_block_forward_joint(handle: int, x, B: int, img_h: int, img_w: int, n_txt: int, t_emb,
+                                 w: krea_dit_weights, out, stream=None) -> None:
+    _check(lib().krea_dit_block_forward_joint(handle, _ptr(x), B, img_h, img_w, n_txt, _ptr(t_emb), ctypes.byref(w),
+                                              _ptr(out), _stream(stream)), "krea_dit_block_forward_joint")
+
+
+def _weights_array(ws: List[krea_dit_weights]):
+    arr = (krea_dit_weights * len(ws))(*ws)
+    return arr
+
+
+def krea_dit_stack_forward(handle: int, x, B: int, img_h: int, img_w: int, n_txt: int, t_emb,
+                           ws: List[krea_dit_weights], stream=None) -> None:
+    arr = _weights_array(ws)
+    _check(lib().krea_dit_stack_forward(handle, _ptr(x), B, img_h, img_w, n_txt, _ptr(t_emb), arr, len(ws),
+                                        _stream(stream)), "krea_dit_stack_forward")
+
+
+def krea_dit_stack_graph_create(handle: int, x, B: int, img_h: int, img_w: int, n_txt: int, t_emb,
+                                ws: List[krea_dit_weights], stream) -> int:
+    arr = _weights_array(ws)
+    g = ctypes.c_void_p()
+    _check(lib().krea_dit_stack_graph_create(handle, _ptr(x), B, img_h, img_w, n_txt, _ptr(t_emb), arr, len(ws),
+                                             _stream(stream), ctypes.byref(g)), "krea_dit_stack_graph_create")
+    return g.value
+
+
+def krea_dit_graph_launch(graph: int, stream=None) -> None:
+    _check(lib().krea_dit_graph_launch(graph, _stream(stream)), "krea_dit_graph_launch")
+
+
+def krea_dit_graph_destroy(graph: int) -> None:
+    _check(lib().krea_dit_graph_destroy(graph), "krea_dit_graph_destroy")
 
 
 def krea_dit_block_workspace(handle: int, which: str) -> Tuple[int, int]:

@@ -98,6 +98,11 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
   return a0 < b0 + nb && b0 < a0 + na;
 }
 
+struct GraphBox {
+  cudaGraph_t graph = nullptr;
+  cudaGraphExec_t exec = nullptr;
+};
+
 struct TimedLaunch {
   int slot;
   cudaEvent_t begin, end;
@@ -321,12 +326,11 @@ int krea_dit_block_create(const krea_dit_config* c, krea_dit_block_t* out) {
       return KREA_DIT_ERR_CUDA;
     }
   }
-  if (h->bf16) {
-    if (!get_encode() || kd::gemm_tc_init() != cudaSuccess || kd::attn_tc_init() != cudaSuccess) {
-      cudaFree(h->ws);
-      delete h;
-      return KREA_DIT_ERR_CUDA;
-    }
+  if (kd::norm_init(c->d_model) != cudaSuccess ||
+      (h->bf16 && (!get_encode() || kd::gemm_tc_init(sms) != cudaSuccess || kd::attn_tc_init() != cudaSuccess))) {
+    cudaFree(h->ws);
+    delete h;
+    return KREA_DIT_ERR_CUDA;
   }
   *out = h;
   return KREA_DIT_OK;
@@ -374,9 +378,14 @@ int krea_dit_timestep_embed(krea_dit_block_t h, const float* t, int B, const kre
   return e == cudaSuccess ? KREA_DIT_OK : KREA_DIT_ERR_CUDA;
 }
 
-int krea_dit_block_forward(krea_dit_block_t h, const void* x_img, const void* x_txt, int B, int img_h, int img_w,
-                           int n_txt, const float* t_emb, const krea_dit_weights* w, void* out,
-                           krea_dit_stream_t stream) {
+}  // extern "C"
+
+namespace {
+// Shared body of the split-input and joint-input forwards. `x_joint` non-null selects
+// the joint input [B, L, d] (then x_img / x_txt are ignored) and allows out == x_joint.
+int forward_impl(krea_dit_block_t h, const void* x_img, const void* x_txt, const void* x_joint, int B, int img_h,
+                 int img_w, int n_txt, const float* t_emb, const krea_dit_weights* w, void* out,
+                 krea_dit_stream_t stream) {
   if (!h || !w || !t_emb || !out) return KREA_DIT_ERR_INVALID_ARG;
   if (B < 0 || img_h < 0 || img_w < 0 || n_txt < 0) return KREA_DIT_ERR_INVALID_ARG;
   if (!w->w_qkvg || !w->w_o || !w->w_gate || !w->w_up || !w->w_down || !w->norm1_w || !w->norm2_w ||
@@ -388,17 +397,23 @@ int krea_dit_block_forward(krea_dit_block_t h, const void* x_img, const void* x_
   if (B > c.max_batch || L_ll > c.max_seq || (n_img_ll > 0 && (img_h > c.img_h_max || img_w > c.img_w_max)))
     return KREA_DIT_ERR_EXCEEDS_CREATE_LIMITS;
   const int n_img = static_cast<int>(n_img_ll), L = static_cast<int>(L_ll);
-  if ((n_img > 0 && !x_img) || (n_txt > 0 && !x_txt)) return KREA_DIT_ERR_INVALID_ARG;
+  if (x_joint) {
+    x_img = x_txt = nullptr;
+  } else if ((n_img > 0 && !x_img) || (n_txt > 0 && !x_txt)) {
+    return KREA_DIT_ERR_INVALID_ARG;
+  }
   const void* ptrs[] = {w->w_qkvg, w->w_o,     w->w_gate,   w->w_up,     w->w_down, w->norm1_w, w->norm2_w,
                         w->q_norm_w, w->k_norm_w, w->mod_bias, t_emb, out};
   for (const void* p : ptrs)
     if (!aligned16(p)) return KREA_DIT_ERR_MISALIGNED;
-  if ((x_img && !aligned16(x_img)) || (x_txt && !aligned16(x_txt))) return KREA_DIT_ERR_MISALIGNED;
+  if ((x_img && !aligned16(x_img)) || (x_txt && !aligned16(x_txt)) || (x_joint && !aligned16(x_joint)))
+    return KREA_DIT_ERR_MISALIGNED;
   const size_t es = h->esz, d = c.d_model;
   const size_t out_bytes = static_cast<size_t>(B) * L * d * es;
   if (overlaps(out, out_bytes, x_img, static_cast<size_t>(B) * n_img * d * es) ||
       overlaps(out, out_bytes, x_txt, static_cast<size_t>(B) * n_txt * d * es) ||
-      overlaps(out, out_bytes, t_emb, static_cast<size_t>(B) * 6 * d * 4))
+      overlaps(out, out_bytes, t_emb, static_cast<size_t>(B) * 6 * d * 4) ||
+      (x_joint && out != x_joint && overlaps(out, out_bytes, x_joint, out_bytes)))
     return KREA_DIT_ERR_INVALID_ARG;
   if (B == 0 || L == 0) return KREA_DIT_OK;
   if (h->inject > 0) {
@@ -425,7 +440,7 @@ int krea_dit_block_forward(krea_dit_block_t h, const void* x_img, const void* x_
   h->have_last = true;
 
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  const RowSrc xsrc{x_txt, x_img, nullptr};
+  const RowSrc xsrc{x_txt, x_img, x_joint};
   const RowSrc h1src{nullptr, nullptr, h->h1};
   const QkvgDst dst{h->q, h->k, h->vt, h->g, w->q_norm_w, w->k_norm_w, h->rope};
   const int nqhd = c.n_q * c.head_dim;
@@ -491,6 +506,88 @@ int krea_dit_block_forward(krea_dit_block_t h, const void* x_img, const void* x_
   }
 #undef KD_RUN
   return e == cudaSuccess ? KREA_DIT_OK : KREA_DIT_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int krea_dit_block_forward(krea_dit_block_t h, const void* x_img, const void* x_txt, int B, int img_h, int img_w,
+                           int n_txt, const float* t_emb, const krea_dit_weights* w, void* out,
+                           krea_dit_stream_t stream) {
+  return forward_impl(h, x_img, x_txt, nullptr, B, img_h, img_w, n_txt, t_emb, w, out, stream);
+}
+
+int krea_dit_block_forward_joint(krea_dit_block_t h, const void* x, int B, int img_h, int img_w, int n_txt,
+                                 const float* t_emb, const krea_dit_weights* w, void* out,
+                                 krea_dit_stream_t stream) {
+  if (!x) return KREA_DIT_ERR_INVALID_ARG;
+  return forward_impl(h, nullptr, nullptr, x, B, img_h, img_w, n_txt, t_emb, w, out, stream);
+}
+
+int krea_dit_stack_forward(krea_dit_block_t h, void* x, int B, int img_h, int img_w, int n_txt, const float* t_emb,
+                           const krea_dit_weights* w, int n_blocks, krea_dit_stream_t stream) {
+  if (!h || !x || n_blocks < 0 || (n_blocks > 0 && !w)) return KREA_DIT_ERR_INVALID_ARG;
+  for (int i = 0; i < n_blocks; ++i) {
+    const int r = forward_impl(h, nullptr, nullptr, x, B, img_h, img_w, n_txt, t_emb, &w[i], x, stream);
+    if (r != KREA_DIT_OK) return r;
+  }
+  return KREA_DIT_OK;
+}
+
+}  // extern "C"
+
+struct krea_dit_graph_s : GraphBox {};
+
+extern "C" {
+
+int krea_dit_stack_graph_create(krea_dit_block_t h, void* x, int B, int img_h, int img_w, int n_txt,
+                                const float* t_emb, const krea_dit_weights* w, int n_blocks, krea_dit_stream_t stream,
+                                krea_dit_graph_t* out) {
+  if (!out) return KREA_DIT_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (!h || !x || n_blocks < 0 || (n_blocks > 0 && !w) || !stream) return KREA_DIT_ERR_INVALID_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  cudaStreamCaptureStatus cs;
+  if (cudaStreamIsCapturing(st, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone)
+    return KREA_DIT_ERR_INVALID_ARG;
+  const bool timing = h->timing;
+  h->timing = false;  // no event records inside the graph
+  if (cudaStreamBeginCapture(st, cudaStreamCaptureModeThreadLocal) != cudaSuccess) {
+    h->timing = timing;
+    return KREA_DIT_ERR_CUDA;
+  }
+  const int r = krea_dit_stack_forward(h, x, B, img_h, img_w, n_txt, t_emb, w, n_blocks, stream);
+  cudaGraph_t graph = nullptr;
+  const cudaError_t ec = cudaStreamEndCapture(st, &graph);
+  h->timing = timing;
+  if (r != KREA_DIT_OK || ec != cudaSuccess) {
+    if (graph) cudaGraphDestroy(graph);
+    return r != KREA_DIT_OK ? r : KREA_DIT_ERR_CUDA;
+  }
+  krea_dit_graph_s* g = new (std::nothrow) krea_dit_graph_s();
+  if (!g || cudaGraphInstantiate(&g->exec, graph, 0) != cudaSuccess) {
+    cudaGraphDestroy(graph);
+    delete g;
+    return KREA_DIT_ERR_CUDA;
+  }
+  g->graph = graph;
+  *out = g;
+  return KREA_DIT_OK;
+}
+
+int krea_dit_graph_launch(krea_dit_graph_t g, krea_dit_stream_t stream) {
+  if (!g) return KREA_DIT_ERR_INVALID_ARG;
+  return cudaGraphLaunch(g->exec, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? KREA_DIT_OK
+                                                                                           : KREA_DIT_ERR_CUDA;
+}
+
+int krea_dit_graph_destroy(krea_dit_graph_t g) {
+  if (!g) return KREA_DIT_OK;
+  cudaGraphExecDestroy(g->exec);
+  cudaGraphDestroy(g->graph);
+  delete g;
+  return KREA_DIT_OK;
 }
 
 int krea_dit_block_enable_host_io(krea_dit_block_t h) {

@@ -426,9 +426,35 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   }
 }
 
+// Co-resident CTA pairs per instantiation, queried once by gemm_tc_init.
 template <class Epi, bool DUAL>
-cudaError_t set_smem_attr() {
-  return cudaFuncSetAttribute(gemm_tc_kernel<Epi, DUAL>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+struct MaxClusters {
+  static int value;
+};
+template <class Epi, bool DUAL>
+int MaxClusters<Epi, DUAL>::value = 0;
+
+template <class Epi, bool DUAL>
+cudaError_t set_smem_attr(int num_sms) {
+  cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<Epi, DUAL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(2 * (num_sms / 2));
+  cfg.blockDim = dim3(NUM_THREADS);
+  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  e = cudaOccupancyMaxActiveClusters(&n, gemm_tc_kernel<Epi, DUAL>, &cfg);
+  if (e != cudaSuccess) return e;
+  MaxClusters<Epi, DUAL>::value = n;
+  return cudaSuccess;
 }
 
 template <class Epi, bool DUAL>
@@ -448,14 +474,8 @@ cudaError_t launch(const CUtensorMap* a, const CUtensorMap* b, const CUtensorMap
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  // persistent grid: as many CTA pairs as fit on the device at once
-  static int max_clusters = 0;
-  if (max_clusters == 0) {
-    cfg.gridDim = dim3(2 * (num_sms / 2));
-    int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, gemm_tc_kernel<Epi, DUAL>, &cfg) != cudaSuccess || n <= 0) n = num_sms / 2;
-    max_clusters = n;
-  }
+  // persistent grid: as many CTA pairs as fit on the device at once (queried at init)
+  const int max_clusters = MaxClusters<Epi, DUAL>::value > 0 ? MaxClusters<Epi, DUAL>::value : num_sms / 2;
   const int pairs = tiles < max_clusters ? tiles : max_clusters;
   cfg.gridDim = dim3(2 * pairs);
   return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<Epi, DUAL>, *a, *b, *b2, M, num_n, K, epi, err);
@@ -465,12 +485,12 @@ cudaError_t launch(const CUtensorMap* a, const CUtensorMap* b, const CUtensorMap
 
 int gemm_tc_smem_bytes() { return SMEM_BYTES; }
 
-cudaError_t gemm_tc_init() {
+cudaError_t gemm_tc_init(int num_sms) {
   cudaError_t e;
-  if ((e = set_smem_attr<EpiQKVG, false>()) != cudaSuccess) return e;
-  if ((e = set_smem_attr<EpiResidAttn, false>()) != cudaSuccess) return e;
-  if ((e = set_smem_attr<EpiResidMlp, false>()) != cudaSuccess) return e;
-  if ((e = set_smem_attr<EpiSwiGLU, true>()) != cudaSuccess) return e;
+  if ((e = set_smem_attr<EpiQKVG, false>(num_sms)) != cudaSuccess) return e;
+  if ((e = set_smem_attr<EpiResidAttn, false>(num_sms)) != cudaSuccess) return e;
+  if ((e = set_smem_attr<EpiResidMlp, false>(num_sms)) != cudaSuccess) return e;
+  if ((e = set_smem_attr<EpiSwiGLU, true>(num_sms)) != cudaSuccess) return e;
   return cudaSuccess;
 }
 

@@ -45,6 +45,8 @@ __device__ __forceinline__ const T* row_src_ptr(const RowSrc& s, int m, int L, i
 #endif
 
 // ---- kernels_simt.cu (both modes: norm; fp32 mode: everything else) ----
+// sets the norm kernels' shared-memory limit for width d (once per handle, before capture)
+cudaError_t norm_init(int d);
 // input -> output storage types of a norm+modulate launch
 enum class NormIO { BF16_BF16, F32_BF16, F32_F32 };
 // requires d % 8 == 0 and d <= 8192 (a warp holds a row in registers)
@@ -68,7 +70,9 @@ cudaError_t launch_swiglu_f32(const Fwd& f, const float* a, const float* u, floa
 
 // ---- gemm_tc.cu (bf16 mode, tcgen05 + TMA) ----
 int gemm_tc_smem_bytes();
-cudaError_t gemm_tc_init();  // sets the kernels' dynamic shared-memory limit (once per process)
+// sets the kernels' dynamic shared-memory limit and queries co-resident CTA pairs (once per
+// handle, before any stream capture)
+cudaError_t gemm_tc_init(int num_sms);
 // xn[T,d] x W_qkvg^T -> QK-norm, RoPE, scatter to Q / K / V^T / G
 cudaError_t launch_gemm_qkvg(const Fwd& f, const CUtensorMap* tm_a, const CUtensorMap* tm_b, int N,
                              const QkvgDst& dst, int num_sms, int* err, cudaStream_t st);

@@ -164,14 +164,7 @@ __global__ void __launch_bounds__(NM_WARPS * 32, 1) norm_modulate_kernel(
 template <class Tin, class Tout, int NV>
 cudaError_t launch_nm(const Fwd& f, RowSrc src, const float* gain_w, const float* mod_shared, const float* mod_bias,
                       int chunk_shift, int chunk_scale, Tout* out, int num_sms, cudaStream_t st) {
-  const size_t smem = static_cast<size_t>(4) * f.d * sizeof(float);
-  static bool attr_set = false;  // one device per process in practice; setting twice is harmless
-  if (!attr_set || smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(norm_modulate_kernel<Tin, Tout, NV>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  const size_t smem = static_cast<size_t>(4) * f.d * sizeof(float);  // limit set by norm_init
   const int ctas = num_sms;  // one CTA (16 warps) per SM: the parameter fill is paid once per SM
   int rows = (f.T + ctas - 1) / ctas;
   rows = (rows + NM_WARPS - 1) / NM_WARPS * NM_WARPS;
@@ -179,6 +172,38 @@ cudaError_t launch_nm(const Fwd& f, RowSrc src, const float* gain_w, const float
   norm_modulate_kernel<Tin, Tout, NV><<<grid, NM_WARPS * 32, smem, st>>>(f, src, gain_w, mod_shared, mod_bias,
                                                                         chunk_shift, chunk_scale, rows, out);
   return cudaGetLastError();
+}
+
+template <class Tin, class Tout, int NV>
+cudaError_t init_nm(int d) {
+  return cudaFuncSetAttribute(norm_modulate_kernel<Tin, Tout, NV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              4 * d * static_cast<int>(sizeof(float)));
+}
+
+template <class Tin, class Tout>
+cudaError_t init_nm_all(int d) {
+  const int nv = (d / 8 + 31) / 32;
+#define KD_NMI(N) \
+  if (nv <= N) return init_nm<Tin, Tout, N>(d)
+  KD_NMI(1);
+  KD_NMI(2);
+  KD_NMI(3);
+  KD_NMI(4);
+  KD_NMI(6);
+  KD_NMI(8);
+  KD_NMI(12);
+  KD_NMI(16);
+  KD_NMI(24);
+  KD_NMI(32);
+#undef KD_NMI
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t norm_init(int d) {
+  cudaError_t e;
+  if ((e = init_nm_all<bf16, bf16>(d)) != cudaSuccess) return e;
+  if ((e = init_nm_all<float, bf16>(d)) != cudaSuccess) return e;
+  return init_nm_all<float, float>(d);
 }
 
 template <class Tin, class Tout>

@@ -10,8 +10,9 @@ from typing import Dict, Optional, Sequence
 import torch
 
 from . import (KREA_DIT_BF16, KREA_DIT_FP32, krea_dit_block_create, krea_dit_block_destroy,
-               krea_dit_block_forward, krea_dit_block_workspace, krea_dit_timestep_embed, make_config,
-               make_temb_weights, make_weights)
+               krea_dit_block_forward, krea_dit_block_forward_joint, krea_dit_block_workspace,
+               krea_dit_graph_destroy, krea_dit_graph_launch, krea_dit_stack_forward, krea_dit_stack_graph_create,
+               krea_dit_timestep_embed, make_config, make_temb_weights, make_weights)
 
 WEIGHT_KEYS = ("w_qkvg", "w_o", "w_gate", "w_up", "w_down", "norm1_w", "norm2_w", "q_norm_w", "k_norm_w",
                "mod_bias")
@@ -72,6 +73,32 @@ class DitBlock:
                                stream or torch.cuda.current_stream(self.device))
         return out
 
+    def forward_joint(self, x: torch.Tensor, B: int, img_h: int, img_w: int, n_txt: int, t_emb: torch.Tensor,
+                      out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+        """One block on the joint [text; image] sequence x [B, L, d]; ``out`` may be x."""
+        if out is None:
+            out = torch.empty_like(x)
+        krea_dit_block_forward_joint(self.handle, x, B, img_h, img_w, n_txt, t_emb, self._wstruct, out,
+                                     stream or torch.cuda.current_stream(self.device))
+        return out
+
+    def stack_weights(self, blocks: Sequence[Dict[str, torch.Tensor]]) -> "StackWeights":
+        """Device copies of per-block weight dicts, for stack_forward / stack_graph."""
+        return StackWeights(blocks, self.device)
+
+    def stack_forward(self, x: torch.Tensor, B: int, img_h: int, img_w: int, n_txt: int, t_emb: torch.Tensor,
+                      sw: "StackWeights", stream=None) -> torch.Tensor:
+        """Applies the blocks of ``sw`` in turn, in place on x [B, L, d]."""
+        krea_dit_stack_forward(self.handle, x, B, img_h, img_w, n_txt, t_emb, sw.structs,
+                               stream or torch.cuda.current_stream(self.device))
+        return x
+
+    def stack_graph(self, x: torch.Tensor, B: int, img_h: int, img_w: int, n_txt: int, t_emb: torch.Tensor,
+                    sw: "StackWeights", stream: torch.cuda.Stream) -> "StackGraph":
+        """Captures stack_forward with these buffers into a CUDA graph on ``stream``."""
+        g = krea_dit_stack_graph_create(self.handle, x, B, img_h, img_w, n_txt, t_emb, sw.structs, stream)
+        return StackGraph(g, (self, x, t_emb, sw))
+
     def workspace(self, name: str, shape: Sequence[int]) -> torch.Tensor:
         """Copy of a workspace buffer of the last forward, viewed with ``shape``
         (H1 is fp32 in both modes, every other buffer is in the storage dtype)."""
@@ -94,6 +121,36 @@ class DitBlock:
         if getattr(self, "handle", None):
             krea_dit_block_destroy(self.handle)
             self.handle = None
+
+    def __del__(self):  # pragma: no cover - best effort
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+class StackWeights:
+    """Device weights of a stack of blocks (one dict per block, keys as DitBlock.set_weights)."""
+
+    def __init__(self, blocks: Sequence[Dict[str, torch.Tensor]], device: torch.device):
+        self.tensors = [{k: w[k].to(device).contiguous() for k in WEIGHT_KEYS} for w in blocks]
+        self.structs = [make_weights(w) for w in self.tensors]
+
+
+class StackGraph:
+    """An instantiated stack graph; keeps the buffers it was captured on alive."""
+
+    def __init__(self, graph: int, keep):
+        self.graph = graph
+        self._keep = keep
+
+    def launch(self, stream=None) -> None:
+        krea_dit_graph_launch(self.graph, stream or torch.cuda.current_stream())
+
+    def close(self) -> None:
+        if self.graph:
+            krea_dit_graph_destroy(self.graph)
+            self.graph = None
 
     def __del__(self):  # pragma: no cover - best effort
         try:

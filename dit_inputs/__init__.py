@@ -178,6 +178,13 @@ def make_case(cfg: Config, *, qk_gain: float = 0.0, x_scale: float = 1.0,
     )
 
 
+def make_stack(cfg: Config, n_blocks: int, **kw) -> List[Case]:
+    """Inputs for a stack of ``n_blocks`` blocks: entry 0 is make_case(cfg) (its timestep,
+    timestep-MLP weights and token inputs drive the stack); entry i > 0 draws block i's
+    weights the same way from seed ``cfg.seed + 7919 * i`` (only its weights are used)."""
+    return [make_case(cfg if i == 0 else cfg.replace(seed=cfg.seed + 7919 * i), **kw) for i in range(n_blocks)]
+
+
 def sample_rows(cfg: Config, n_per_batch: int, seed: int = 1234) -> List[np.ndarray]:
     """Stratified row sample per batch element (joint-sequence indices, text rows
     first): first/last text rows, the four image corners, image-edge rows, then

@@ -166,6 +166,47 @@ int krea_dit_block_forward(krea_dit_block_t h, const void* x_img, const void* x_
 int krea_dit_timestep_embed_noalloc(const float* t, int B, int d_model, const krea_dit_temb_weights* w,
                                     float* mod_shared, krea_dit_stream_t stream);
 
+/* ---- joint-layout forward and stacks of blocks ------------------------------------ */
+
+/* One block forward whose input is the joint sequence itself (Krea 2 Technical Report,
+ * "Modality streams": text and image tokens form one sequence through every block).
+ *  x    device dtype [B, L, d], L = n_txt + img_h*img_w, text rows first (the layout
+ *       krea_dit_block_forward writes)
+ *  out  device dtype [B, L, d]; may be x itself (the block reads x only before writing
+ *       out), otherwise must not overlap it.
+ * Other arguments and errors as krea_dit_block_forward. */
+int krea_dit_block_forward_joint(krea_dit_block_t h, const void* x, int B, int img_h, int img_w, int n_txt,
+                                 const float* t_emb, const krea_dit_weights* w, void* out, krea_dit_stream_t stream);
+
+/* A stack of n_blocks blocks applied in place to the joint sequence x [B, L, d]: block i
+ * uses weights w[i] (host array of n_blocks structs, read during the call only; may be NULL
+ * when n_blocks is 0) and the shared t_emb (each block adds its own mod_bias). One handle's
+ * workspace serves every block in turn. Enqueues 7 * n_blocks kernels (bf16 mode) and
+ * stops at the first block whose arguments fail a check, returning that block's status
+ * (earlier blocks stay enqueued). Capturable in a CUDA graph (krea_dit_stack_graph_create). */
+int krea_dit_stack_forward(krea_dit_block_t h, void* x, int B, int img_h, int img_w, int n_txt, const float* t_emb,
+                           const krea_dit_weights* w, int n_blocks, krea_dit_stream_t stream);
+
+/* Capture krea_dit_stack_forward with these exact arguments into a CUDA graph and
+ * instantiate it, so that a whole stack replays with one launch call.
+ *  stream  a created (non-default) stream that is not capturing already; the capture is
+ *          thread-local, and per-kernel timing is suspended while it runs.
+ *  out     receives the graph; set to NULL on any error.
+ * The graph records device pointers only: x, t_emb, every weight buffer and the handle
+ * (its workspace) must outlive it, and each launch reruns the stack in place on whatever
+ * those buffers hold then. Launches on one handle must not overlap another forward on the
+ * same handle (they share its workspace). Argument errors are those of
+ * krea_dit_stack_forward, plus KREA_DIT_ERR_INVALID_ARG for a NULL or capturing stream;
+ * KREA_DIT_ERR_CUDA if capture or instantiation fails.
+ * krea_dit_graph_launch enqueues the graph on `stream` (any stream, NULL = legacy default).
+ * krea_dit_graph_destroy frees it (NULL is a no-op). */
+typedef struct krea_dit_graph_s* krea_dit_graph_t;
+int krea_dit_stack_graph_create(krea_dit_block_t h, void* x, int B, int img_h, int img_w, int n_txt,
+                                const float* t_emb, const krea_dit_weights* w, int n_blocks, krea_dit_stream_t stream,
+                                krea_dit_graph_t* out);
+int krea_dit_graph_launch(krea_dit_graph_t g, krea_dit_stream_t stream);
+int krea_dit_graph_destroy(krea_dit_graph_t g);
+
 /* Static text for a status code. Never NULL. */
 const char* krea_dit_status_string(int status);
 

@@ -20,6 +20,7 @@ from .block import (  # noqa: F401
     round_to_bf16,
     rms_norm,
     rope_angles,
+    stack_forward,
     swiglu,
     timestep_embedding,
     timestep_mlp,
@@ -45,4 +46,16 @@ def run_case(case, rows: Optional[Sequence[np.ndarray]] = None, *, rope_on: bool
         case.x_txt, case.x_img, (cfg.img_h, cfg.img_w), ms, case.w,
         n_q=cfg.n_q, n_kv=cfg.n_kv, hd=cfg.hd, eps=cfg.eps, rope_base=cfg.rope_base,
         gate_on=cfg.gate_on, rope_on=rope_on, rows=rows, store=store,
+    )
+
+
+def run_stack(case, blocks, *, mod_shared: Optional[np.ndarray] = None, store=None) -> np.ndarray:
+    """Timestep embedding plus a stack of blocks for a seeded case; ``blocks`` is a list of
+    weight dicts (block 0's is normally ``case.w``). Returns the final joint output."""
+    cfg = case.cfg
+    ms = mod_shared_for(case) if mod_shared is None else mod_shared
+    return stack_forward(
+        case.x_txt, case.x_img, (cfg.img_h, cfg.img_w), ms, blocks,
+        n_q=cfg.n_q, n_kv=cfg.n_kv, hd=cfg.hd, eps=cfg.eps, rope_base=cfg.rope_base,
+        gate_on=cfg.gate_on, store=store,
     )

@@ -320,3 +320,29 @@ def block_forward(
         res["hmid"].append(hmid)
         res["out"].append(out)
     return res
+
+
+def stack_forward(
+    x_txt: np.ndarray,
+    x_img: np.ndarray,
+    img_hw: Sequence[int],
+    mod_shared: np.ndarray,
+    ws: Sequence[Dict[str, np.ndarray]],
+    *,
+    store=None,
+    **kw,
+) -> np.ndarray:
+    """A stack of single-stream blocks: block i (weights ``ws[i]``, its own mod_bias on
+    the shared timestep modulation) maps the joint sequence to the next one ("架构 › 模态流" /
+    Modality streams: text and image tokens pass through every block as one sequence).
+    Returns the last block's output [B, L, d] (text rows first). ``store`` and the other
+    keywords are block_forward's; with ``store`` set, each block's output is rounded where
+    an implementation stores it, so the next block reads the rounded value."""
+    x_txt = np.asarray(x_txt, F64)
+    x_img = np.asarray(x_img, F64)
+    Nt = x_txt.shape[1]
+    X = np.concatenate([x_txt, x_img], axis=1)
+    for w in ws:
+        out = block_forward(X[:, :Nt], X[:, Nt:], img_hw, mod_shared, w, store=store, **kw)["out"]
+        X = np.stack(out, axis=0)
+    return X

@@ -438,3 +438,62 @@ def test_storage_rounded_oracle_stores_representable_values():
     exact = oracle.run_case(case)
     err = np.abs(np.stack(r["out"]) - np.stack(exact["out"])).max()
     assert 0 < err < 0.05
+
+
+# --------------------------------------------------------------- stacks of blocks
+def _textbook_stack(cfg, blocks, ms, x_joint, *, text_first=True):
+    """Textbook blocks applied in turn; ``text_first=False`` plants a chain that hands the
+    next block its image rows as if they were the text rows."""
+    import types
+    X = x_joint
+    Nt = cfg.n_txt
+    for c in blocks:
+        if text_first:
+            xt, xi = X[:, :Nt], X[:, Nt:]
+        else:
+            xt, xi = X[:, -Nt:], X[:, :-Nt]
+        step = types.SimpleNamespace(cfg=cfg, w=c.w, x_txt=xt, x_img=xi)
+        X = textbook_dit_block(step, _mod_from_shared(c, ms), gate_on=cfg.gate_on)
+    return X
+
+
+def test_stack_matches_textbook_blocks_in_turn():
+    """A stack is the blocks composed in order, each with its own weights and mod_bias on
+    the shared modulation, on the joint sequence with text rows first."""
+    blocks = di.make_stack(_small_cfg(), 3)
+    case = blocks[0]
+    ms = oracle.mod_shared_for(case) * 20.0
+    got = oracle.run_stack(case, [c.w for c in blocks], mod_shared=ms)
+    ref = _textbook_stack(case.cfg, blocks, ms, _joint(case))
+    np.testing.assert_allclose(got, ref, rtol=1e-11, atol=1e-11)
+    # the blocks differ, so a chain that reorders or reuses them would not match
+    assert np.max(np.abs(got - _textbook_stack(case.cfg, blocks[::-1], ms, _joint(case)))) > 1e-6
+    # a chain that swaps the text and image rows between blocks would not match either
+    bad = _textbook_stack(case.cfg, blocks, ms, _joint(case), text_first=False)
+    assert np.max(np.abs(got - bad)) > 1e-6
+
+
+def test_stack_skips_a_zero_gate_block_exactly():
+    """A block whose gates are zero passes the sequence through unchanged, so inserting it
+    anywhere in a stack changes nothing, bit for bit."""
+    blocks = di.make_stack(_small_cfg(B=1), 3)
+    case = blocks[0]
+    ms = oracle.mod_shared_for(case)
+    zero = dict(blocks[1].w)
+    zero["mod_bias"] = zero["mod_bias"].copy()
+    zero["mod_bias"][2] = -ms[0, 2]
+    zero["mod_bias"][5] = -ms[0, 5]
+    a, c = blocks[0].w, blocks[2].w
+    np.testing.assert_array_equal(oracle.run_stack(case, [a, zero, c], mod_shared=ms),
+                                  oracle.run_stack(case, [a, c], mod_shared=ms))
+    np.testing.assert_array_equal(oracle.run_stack(case, [zero], mod_shared=ms), _joint(case))
+
+
+def test_stack_of_one_is_the_block_and_storage_rounds_every_output():
+    blocks = di.make_stack(_small_cfg(dtype="bf16"), 2)
+    case = blocks[0]
+    ms = oracle.mod_shared_for(case)
+    one = oracle.run_stack(case, [case.w], mod_shared=ms)
+    np.testing.assert_array_equal(one, np.stack(oracle.run_case(case, mod_shared=ms)["out"]))
+    st = oracle.run_stack(case, [c.w for c in blocks], mod_shared=ms, store="bf16")
+    np.testing.assert_array_equal(st, ob.round_to_bf16(st))
