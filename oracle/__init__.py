@@ -4,7 +4,8 @@ TEST INFRASTRUCTURE ONLY: imported by ``tests/``, by ``__graft_entry__.smoke()``
 and by the benchmark's CPU-baseline leg, never by the library. It shares no code
 with the CUDA path. Parity pins: every function here is pinned by the CPU tests
 (textbook library routines, closed forms, invariants, brute force on tiny
-inputs); none is "parity unpinned".
+inputs); none is "parity unpinned". ``oracle.gemm8`` adds the block with 8-bit
+(e4m3, scaled) GEMM operands, pinned in ``tests/test_oracle_gemm8.py``.
 """
 from __future__ import annotations
 
