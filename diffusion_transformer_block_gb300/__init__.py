@@ -28,7 +28,10 @@ KREA_DIT_ERR_SCRATCH_TOO_SMALL = -9
 KREA_DIT_NOALLOC_SCRATCH_FLOATS = 262144
 KREA_DIT_BF16 = 0
 KREA_DIT_FP32 = 1
-BUFFERS = {"XN": 0, "Q": 1, "K": 2, "VT": 3, "G": 4, "OG": 5, "H1": 6, "HN": 7, "HMID": 8}
+KREA_DIT_FP8_TENSOR = 2
+KREA_DIT_FP8_ROW = 3
+BUFFERS = {"XN": 0, "Q": 1, "K": 2, "VT": 3, "G": 4, "OG": 5, "H1": 6, "HN": 7, "HMID": 8, "XN8": 9, "OG8": 10,
+           "HN8": 11, "HMID8": 12, "DQ_XN": 13, "DQ_OG": 14, "DQ_HN": 15, "DQ_HMID": 16}
 
 # C symbols the header declares (checked by the CPU tests against the built library)
 EXPORTS = [
@@ -38,7 +41,7 @@ EXPORTS = [
     "krea_dit_block_inject_fault", "krea_dit_kernel_names", "krea_dit_timestep_embed_noalloc",
     "krea_dit_block_enable_host_io", "krea_dit_block_forward_host", "krea_dit_block_host_sync",
     "krea_dit_block_forward_joint", "krea_dit_stack_forward", "krea_dit_stack_graph_create", "krea_dit_graph_launch",
-    "krea_dit_graph_destroy",
+    "krea_dit_graph_destroy", "krea_dit_weights8_quantize", "krea_dit_block_forward8",
 ]
 
 
@@ -58,6 +61,11 @@ class krea_dit_config(ctypes.Structure):
 class krea_dit_weights(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in (
         "w_qkvg", "w_o", "w_gate", "w_up", "w_down", "norm1_w", "norm2_w", "q_norm_w", "k_norm_w", "mod_bias")]
+
+
+class krea_dit_weights8(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in (
+        "w_qkvg", "w_o", "w_gate", "w_up", "w_down", "dq_qkvg", "dq_o", "dq_gate", "dq_up", "dq_down")]
 
 
 class krea_dit_temb_weights(ctypes.Structure):
@@ -99,6 +107,10 @@ def lib() -> ctypes.CDLL:
                                                   ctypes.POINTER(vp)]
         L.krea_dit_graph_launch.argtypes = [vp, vp]
         L.krea_dit_graph_destroy.argtypes = [vp]
+        L.krea_dit_weights8_quantize.argtypes = [vp, ctypes.POINTER(krea_dit_weights), ctypes.POINTER(krea_dit_weights8),
+                                                 vp]
+        L.krea_dit_block_forward8.argtypes = [vp, vp, vp, ci, ci, ci, ci, vp, ctypes.POINTER(krea_dit_weights),
+                                              ctypes.POINTER(krea_dit_weights8), vp, vp]
         for name in EXPORTS:
             getattr(L, name)  # every declared symbol must resolve
             if name != "krea_dit_status_string":
@@ -158,6 +170,18 @@ def krea_dit_block_forward(handle: int, x_img, x_txt, B: int, img_h: int, img_w:
                            w: krea_dit_weights, out, stream=None) -> None:
     _check(lib().krea_dit_block_forward(handle, _ptr(x_img), _ptr(x_txt), B, img_h, img_w, n_txt, _ptr(t_emb),
                                         ctypes.byref(w), _ptr(out), _stream(stream)), "krea_dit_block_forward")
+
+
+def krea_dit_weights8_quantize(handle: int, w: krea_dit_weights, q: krea_dit_weights8, stream=None) -> None:
+    _check(lib().krea_dit_weights8_quantize(handle, ctypes.byref(w), ctypes.byref(q), _stream(stream)),
+           "krea_dit_weights8_quantize")
+
+
+def krea_dit_block_forward8(handle: int, x_img, x_txt, B: int, img_h: int, img_w: int, n_txt: int, t_emb,
+                            w: krea_dit_weights, q: krea_dit_weights8, out, stream=None) -> None:
+    _check(lib().krea_dit_block_forward8(handle, _ptr(x_img), _ptr(x_txt), B, img_h, img_w, n_txt, _ptr(t_emb),
+                                         ctypes.byref(w), ctypes.byref(q), _ptr(out), _stream(stream)),
+           "krea_dit_block_forward8")
 
 
 def krea_dit_block_enable_host_io(handle: int) -> None:
@@ -262,8 +286,14 @@ def make_config(*, max_batch: int, max_seq: int, d_model: int, n_q: int, n_kv: i
 
 
 def make_weights(t: Dict[str, object]) -> krea_dit_weights:
-    """Weights struct from a dict of device tensors keyed by the struct's field names."""
-    return krea_dit_weights(*[_ptr(t[n]) for n, _ in krea_dit_weights._fields_])
+    """Weights struct from a dict of device tensors keyed by the struct's field names
+    (a missing key is passed as NULL)."""
+    return krea_dit_weights(*[_ptr(t.get(n)) for n, _ in krea_dit_weights._fields_])
+
+
+def make_weights8(t: Dict[str, object]) -> krea_dit_weights8:
+    """8-bit weights struct from a dict of device tensors keyed by the struct's field names."""
+    return krea_dit_weights8(*[_ptr(t[n]) for n, _ in krea_dit_weights8._fields_])
 
 
 def make_temb_weights(t: Dict[str, object]) -> krea_dit_temb_weights:

@@ -40,6 +40,12 @@ enum Slot {
   S_TEMB_SIN,
   S_TEMB_MLP1,
   S_TEMB_MLP2,
+  S_NORM1_AMAX,
+  S_QUANT_OG,
+  S_NORM2_AMAX,
+  S_QUANT_HMID,
+  S_W8_AMAX,
+  S_W8_QUANT,
   S_COUNT
 };
 const char* const kSlotNames[S_COUNT] = {
@@ -47,7 +53,9 @@ const char* const kSlotNames[S_COUNT] = {
     "norm2_modulate",       "upgate_gemm_swiglu",    "down_gemm_residual", "qkvg_gemm_f32",
     "qkvg_qknorm_rope_f32", "oproj_gemm_f32",        "residual_attn_f32", "gate_gemm_f32",
     "up_gemm_f32",          "swiglu_f32",            "down_gemm_f32",   "residual_mlp_f32",
-    "temb_sinusoid",        "temb_mlp1",             "temb_mlp2"};
+    "temb_sinusoid",        "temb_mlp1",             "temb_mlp2",       "norm1_amax",
+    "quant_og_e4m3",        "norm2_amax",            "quant_hmid_e4m3", "weights8_row_amax",
+    "weights8_quant_e4m3"};
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
@@ -89,6 +97,18 @@ bool encode_3d(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, u
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2D tensor map of bytes (e4m3 codes) over a row-major [rows, cols] matrix, pitch = cols,
+// box = 128 x box_rows (128-byte rows, matching the 128-byte swizzle).
+bool encode_2d_u8(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint32_t box_rows) {
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols};
+  cuuint32_t box[2] = {128, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 inline size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -113,7 +133,8 @@ struct TimedLaunch {
 struct krea_dit_block_s {
   krea_dit_config cfg{};
   int device = 0, num_sms = 0;
-  bool bf16 = true;
+  bool bf16 = true;  // bf16 storage (also in the 8-bit modes)
+  int mode8 = 0;     // 0: no 8-bit GEMMs, 1: tensor-wise scaling, 2: row-wise scaling
   size_t esz = 2;
   size_t max_T = 0;
   int n_qkvg = 0;
@@ -126,6 +147,10 @@ struct krea_dit_block_s {
   size_t sz_xn = 0, sz_q = 0, sz_k = 0, sz_vt = 0, sz_g = 0, sz_og = 0, sz_h1 = 0, sz_hn = 0, sz_hmid = 0;
   float *raw_qkvg = nullptr, *raw_o = nullptr, *raw_a = nullptr, *raw_u = nullptr, *raw_down = nullptr;
   float *temb_e = nullptr, *temb_h = nullptr;
+  // 8-bit modes: e4m3 GEMM operands, their dequantisation factors, row amax accumulators
+  void *xn8 = nullptr, *og8 = nullptr, *hn8 = nullptr, *hmid8 = nullptr;
+  float *dq_xn = nullptr, *dq_og = nullptr, *dq_hn = nullptr, *dq_hmid = nullptr;
+  float *am_xn = nullptr, *am_og = nullptr, *am_hn = nullptr, *am_hmid = nullptr, *am_w = nullptr;
   float2* rope = nullptr;
   int* err = nullptr;
   Fwd last{};
@@ -229,7 +254,9 @@ int krea_dit_block_create(const krea_dit_config* c, krea_dit_block_t* out) {
   if (!out) return KREA_DIT_ERR_INVALID_ARG;
   *out = nullptr;
   if (!c) return KREA_DIT_ERR_INVALID_ARG;
-  if (c->mode != KREA_DIT_BF16 && c->mode != KREA_DIT_FP32) return KREA_DIT_ERR_INVALID_ARG;
+  if (c->mode != KREA_DIT_BF16 && c->mode != KREA_DIT_FP32 && c->mode != KREA_DIT_FP8_TENSOR &&
+      c->mode != KREA_DIT_FP8_ROW)
+    return KREA_DIT_ERR_INVALID_ARG;
   if (c->max_batch < 1 || c->max_seq < 1 || c->img_h_max < 0 || c->img_w_max < 0) return KREA_DIT_ERR_INVALID_ARG;
   if (!(c->eps > 0.f) || !(c->rope_base > 0.f) || (c->gate_on != 0 && c->gate_on != 1))
     return KREA_DIT_ERR_INVALID_ARG;
@@ -237,7 +264,10 @@ int krea_dit_block_create(const krea_dit_config* c, krea_dit_block_t* out) {
   if (c->d_model % 64 || c->ffn % 64 || c->n_q % c->n_kv) return KREA_DIT_ERR_UNSUPPORTED_SHAPE;
   if (c->d_model > 8192) return KREA_DIT_ERR_UNSUPPORTED_SHAPE;  // norm kernel: one thread per 8 columns
   if (c->head_dim != 64 && c->head_dim != 128) return KREA_DIT_ERR_UNSUPPORTED_SHAPE;
-  if (c->mode == KREA_DIT_BF16 && c->head_dim != 128) return KREA_DIT_ERR_UNSUPPORTED_SHAPE;
+  if (c->mode != KREA_DIT_FP32 && c->head_dim != 128) return KREA_DIT_ERR_UNSUPPORTED_SHAPE;
+  // the norm kernel's e4m3 output holds rows of up to 3072 columns
+  if ((c->mode == KREA_DIT_FP8_TENSOR || c->mode == KREA_DIT_FP8_ROW) && c->d_model > 3072)
+    return KREA_DIT_ERR_UNSUPPORTED_SHAPE;
   // 32-bit index arithmetic inside the kernels
   const double big = static_cast<double>(c->max_batch) * c->max_seq *
                      (c->ffn > (2 * c->n_q + 2 * c->n_kv) * c->head_dim ? c->ffn
@@ -253,7 +283,8 @@ int krea_dit_block_create(const krea_dit_config* c, krea_dit_block_t* out) {
   h->cfg = *c;
   h->device = dev;
   h->num_sms = sms;
-  h->bf16 = c->mode == KREA_DIT_BF16;
+  h->bf16 = c->mode != KREA_DIT_FP32;
+  h->mode8 = c->mode == KREA_DIT_FP8_TENSOR ? 1 : (c->mode == KREA_DIT_FP8_ROW ? 2 : 0);
   h->esz = h->bf16 ? 2 : 4;
   h->max_T = static_cast<size_t>(c->max_batch) * c->max_seq;
   h->n_qkvg = ((c->gate_on ? 2 : 1) * c->n_q + 2 * c->n_kv) * c->head_dim;
@@ -287,6 +318,19 @@ int krea_dit_block_create(const krea_dit_config* c, krea_dit_block_t* out) {
     items.push_back({reinterpret_cast<void**>(&h->raw_a), T * F * 4, nullptr});
     items.push_back({reinterpret_cast<void**>(&h->raw_u), T * F * 4, nullptr});
     items.push_back({reinterpret_cast<void**>(&h->raw_down), T * d * 4, nullptr});
+  }
+  if (h->mode8) {
+    const size_t nqhd = static_cast<size_t>(c->n_q) * hd;
+    size_t wrows = static_cast<size_t>(h->n_qkvg);
+    if (d > wrows) wrows = d;
+    if (F > wrows) wrows = F;
+    items.push_back({&h->xn8, T * d, nullptr});
+    items.push_back({&h->og8, T * nqhd, nullptr});
+    items.push_back({&h->hn8, T * d, nullptr});
+    items.push_back({&h->hmid8, T * F, nullptr});
+    for (float** p : {&h->dq_xn, &h->dq_og, &h->dq_hn, &h->dq_hmid, &h->am_xn, &h->am_og, &h->am_hn, &h->am_hmid})
+      items.push_back({reinterpret_cast<void**>(p), T * 4, nullptr});
+    items.push_back({reinterpret_cast<void**>(&h->am_w), wrows * 4, nullptr});
   }
   items.push_back({reinterpret_cast<void**>(&h->temb_e), static_cast<size_t>(c->max_batch) * 256 * 4, nullptr});
   items.push_back({reinterpret_cast<void**>(&h->temb_h), static_cast<size_t>(c->max_batch) * d * 4, nullptr});
@@ -384,13 +428,22 @@ namespace {
 // Shared body of the split-input and joint-input forwards. `x_joint` non-null selects
 // the joint input [B, L, d] (then x_img / x_txt are ignored) and allows out == x_joint.
 int forward_impl(krea_dit_block_t h, const void* x_img, const void* x_txt, const void* x_joint, int B, int img_h,
-                 int img_w, int n_txt, const float* t_emb, const krea_dit_weights* w, void* out,
-                 krea_dit_stream_t stream) {
+                 int img_w, int n_txt, const float* t_emb, const krea_dit_weights* w, const krea_dit_weights8* w8,
+                 void* out, krea_dit_stream_t stream) {
   if (!h || !w || !t_emb || !out) return KREA_DIT_ERR_INVALID_ARG;
+  if ((h->mode8 != 0) != (w8 != nullptr)) return KREA_DIT_ERR_INVALID_ARG;  // 8-bit handles need forward8
   if (B < 0 || img_h < 0 || img_w < 0 || n_txt < 0) return KREA_DIT_ERR_INVALID_ARG;
-  if (!w->w_qkvg || !w->w_o || !w->w_gate || !w->w_up || !w->w_down || !w->norm1_w || !w->norm2_w ||
-      !w->q_norm_w || !w->k_norm_w || !w->mod_bias)
+  if (!w->norm1_w || !w->norm2_w || !w->q_norm_w || !w->k_norm_w || !w->mod_bias) return KREA_DIT_ERR_INVALID_ARG;
+  if (w8) {
+    const void* p8[] = {w8->w_qkvg, w8->w_o,    w8->w_gate, w8->w_up,    w8->w_down,
+                        w8->dq_qkvg, w8->dq_o, w8->dq_gate, w8->dq_up, w8->dq_down};
+    for (const void* p : p8) {
+      if (!p) return KREA_DIT_ERR_INVALID_ARG;
+      if (!aligned16(p)) return KREA_DIT_ERR_MISALIGNED;
+    }
+  } else if (!w->w_qkvg || !w->w_o || !w->w_gate || !w->w_up || !w->w_down) {
     return KREA_DIT_ERR_INVALID_ARG;
+  }
   const krea_dit_config& c = h->cfg;
   const long long n_img_ll = static_cast<long long>(img_h) * img_w;
   const long long L_ll = n_img_ll + n_txt;
@@ -405,7 +458,7 @@ int forward_impl(krea_dit_block_t h, const void* x_img, const void* x_txt, const
   const void* ptrs[] = {w->w_qkvg, w->w_o,     w->w_gate,   w->w_up,     w->w_down, w->norm1_w, w->norm2_w,
                         w->q_norm_w, w->k_norm_w, w->mod_bias, t_emb, out};
   for (const void* p : ptrs)
-    if (!aligned16(p)) return KREA_DIT_ERR_MISALIGNED;
+    if (p && !aligned16(p)) return KREA_DIT_ERR_MISALIGNED;
   if ((x_img && !aligned16(x_img)) || (x_txt && !aligned16(x_txt)) || (x_joint && !aligned16(x_joint)))
     return KREA_DIT_ERR_MISALIGNED;
   const size_t es = h->esz, d = c.d_model;
@@ -450,7 +503,54 @@ int forward_impl(krea_dit_block_t h, const void* x_img, const void* x_txt, const
     if (e == cudaSuccess) e = timed(h, slot, st, [&] { return (expr); }); \
   } while (0)
 
-  if (h->bf16) {
+  if (h->mode8) {
+    const int per_row = h->mode8 == 2;
+    const uint64_t T = static_cast<uint64_t>(f.T);
+    CUtensorMap tm_xn8, tm_wqkvg, tm_og8, tm_wo, tm_hn8, tm_wgate, tm_wup, tm_hmid8, tm_wdown, tm_q, tm_k, tm_vt;
+    bool ok = encode_2d_u8(&tm_xn8, h->xn8, d, T, 128) && encode_2d_u8(&tm_wqkvg, w8->w_qkvg, d, h->n_qkvg, 128) &&
+              encode_2d_u8(&tm_og8, h->og8, nqhd, T, 128) && encode_2d_u8(&tm_wo, w8->w_o, nqhd, d, 128) &&
+              encode_2d_u8(&tm_hn8, h->hn8, d, T, 128) && encode_2d_u8(&tm_wgate, w8->w_gate, d, c.ffn, 128) &&
+              encode_2d_u8(&tm_wup, w8->w_up, d, c.ffn, 128) && encode_2d_u8(&tm_hmid8, h->hmid8, c.ffn, T, 128) &&
+              encode_2d_u8(&tm_wdown, w8->w_down, c.ffn, d, 128) &&
+              encode_3d(&tm_q, h->q, c.head_dim, L, static_cast<uint64_t>(B) * c.n_q, c.head_dim, 64, 128) &&
+              encode_3d(&tm_k, h->k, c.head_dim, L, static_cast<uint64_t>(B) * c.n_kv, c.head_dim, 64, 128) &&
+              encode_3d(&tm_vt, h->vt, L, c.head_dim, static_cast<uint64_t>(B) * c.n_kv, f.Lp, 64, 128);
+    if (!ok) return KREA_DIT_ERR_CUDA;
+    const int sms = h->num_sms;
+    // row amax accumulators of the attention and SwiGLU outputs (atomic max from zero)
+    e = cudaMemsetAsync(h->am_og, 0, T * sizeof(float), st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(h->am_hmid, 0, T * sizeof(float), st);
+    const kd::NormQ qmode = per_row ? kd::NormQ::ROW : kd::NormQ::TENSOR;
+    const kd::NormQOut q_amax1{kd::NormQ::AMAX, nullptr, nullptr, h->am_xn};
+    const kd::NormQOut q_xn{qmode, h->xn8, h->dq_xn, h->am_xn};
+    const kd::NormQOut q_amax2{kd::NormQ::AMAX, nullptr, nullptr, h->am_hn};
+    const kd::NormQOut q_hn{qmode, h->hn8, h->dq_hn, h->am_hn};
+    const kd::Deq dq_qkvg{h->dq_xn, w8->dq_qkvg, nullptr, per_row};
+    const kd::Deq dq_o{h->dq_og, w8->dq_o, nullptr, per_row};
+    const kd::Deq dq_ff{h->dq_hn, w8->dq_gate, w8->dq_up, per_row};
+    const kd::Deq dq_down{h->dq_hmid, w8->dq_down, nullptr, per_row};
+    if (!per_row)
+      KD_RUN(S_NORM1_AMAX, kd::launch_norm_modulate(kd::NormIO::BF16_BF16, f, xsrc, w->norm1_w, t_emb, w->mod_bias, 0,
+                                                    1, nullptr, sms, st, &q_amax1));
+    KD_RUN(S_NORM1, kd::launch_norm_modulate(kd::NormIO::BF16_BF16, f, xsrc, w->norm1_w, t_emb, w->mod_bias, 0, 1,
+                                             nullptr, sms, st, &q_xn));
+    KD_RUN(S_QKVG_TC, kd::launch_gemm_qkvg(f, &tm_xn8, &tm_wqkvg, h->n_qkvg, dst, &dq_qkvg, sms, h->err, st));
+    KD_RUN(S_ATTN, kd::launch_attn_tc(f, &tm_q, &tm_k, &tm_vt, h->g, h->og, h->am_og, sms, h->err, st));
+    KD_RUN(S_QUANT_OG, kd::launch_quant_e4m3(h->og, f.T, nqhd, h->am_og, per_row, h->og8, h->dq_og, sms, st));
+    KD_RUN(S_OPROJ_TC, kd::launch_gemm_resid_attn(f, &tm_og8, &tm_wo, nqhd, xsrc, t_emb, w->mod_bias,
+                                                  static_cast<float*>(h->h1), &dq_o, sms, h->err, st));
+    if (!per_row)
+      KD_RUN(S_NORM2_AMAX, kd::launch_norm_modulate(kd::NormIO::F32_BF16, f, h1src, w->norm2_w, t_emb, w->mod_bias, 3,
+                                                    4, nullptr, sms, st, &q_amax2));
+    KD_RUN(S_NORM2, kd::launch_norm_modulate(kd::NormIO::F32_BF16, f, h1src, w->norm2_w, t_emb, w->mod_bias, 3, 4,
+                                             nullptr, sms, st, &q_hn));
+    KD_RUN(S_UPGATE_TC, kd::launch_gemm_swiglu(f, &tm_hn8, &tm_wgate, &tm_wup, h->hmid, h->am_hmid, &dq_ff, sms,
+                                               h->err, st));
+    KD_RUN(S_QUANT_HMID,
+           kd::launch_quant_e4m3(h->hmid, f.T, c.ffn, h->am_hmid, per_row, h->hmid8, h->dq_hmid, sms, st));
+    KD_RUN(S_DOWN_TC, kd::launch_gemm_resid_mlp(f, &tm_hmid8, &tm_wdown, c.ffn, static_cast<const float*>(h->h1),
+                                                t_emb, w->mod_bias, out, &dq_down, sms, h->err, st));
+  } else if (h->bf16) {
     CUtensorMap tm_xn, tm_wqkvg, tm_og, tm_wo, tm_hn, tm_wgate, tm_wup, tm_hmid, tm_wdown, tm_q, tm_k, tm_vt;
     const uint64_t T = static_cast<uint64_t>(f.T);
     bool ok = encode_2d(&tm_xn, h->xn, d, T, d, 64, 128) &&
@@ -468,15 +568,16 @@ int forward_impl(krea_dit_block_t h, const void* x_img, const void* x_txt, const
     const int sms = h->num_sms;
     KD_RUN(S_NORM1, kd::launch_norm_modulate(kd::NormIO::BF16_BF16, f, xsrc, w->norm1_w, t_emb, w->mod_bias, 0, 1,
                                              h->xn, sms, st));
-    KD_RUN(S_QKVG_TC, kd::launch_gemm_qkvg(f, &tm_xn, &tm_wqkvg, h->n_qkvg, dst, sms, h->err, st));
-    KD_RUN(S_ATTN, kd::launch_attn_tc(f, &tm_q, &tm_k, &tm_vt, h->g, h->og, sms, h->err, st));
+    KD_RUN(S_QKVG_TC, kd::launch_gemm_qkvg(f, &tm_xn, &tm_wqkvg, h->n_qkvg, dst, nullptr, sms, h->err, st));
+    KD_RUN(S_ATTN, kd::launch_attn_tc(f, &tm_q, &tm_k, &tm_vt, h->g, h->og, nullptr, sms, h->err, st));
     KD_RUN(S_OPROJ_TC, kd::launch_gemm_resid_attn(f, &tm_og, &tm_wo, nqhd, xsrc, t_emb, w->mod_bias,
-                                                  static_cast<float*>(h->h1), sms, h->err, st));
+                                                  static_cast<float*>(h->h1), nullptr, sms, h->err, st));
     KD_RUN(S_NORM2, kd::launch_norm_modulate(kd::NormIO::F32_BF16, f, h1src, w->norm2_w, t_emb, w->mod_bias, 3, 4,
                                              h->hn, sms, st));
-    KD_RUN(S_UPGATE_TC, kd::launch_gemm_swiglu(f, &tm_hn, &tm_wgate, &tm_wup, h->hmid, sms, h->err, st));
+    KD_RUN(S_UPGATE_TC, kd::launch_gemm_swiglu(f, &tm_hn, &tm_wgate, &tm_wup, h->hmid, nullptr, nullptr, sms,
+                                               h->err, st));
     KD_RUN(S_DOWN_TC, kd::launch_gemm_resid_mlp(f, &tm_hmid, &tm_wdown, c.ffn, static_cast<const float*>(h->h1),
-                                                t_emb, w->mod_bias, out, sms, h->err, st));
+                                                t_emb, w->mod_bias, out, nullptr, sms, h->err, st));
   } else {
     const int T = f.T;
     const float* wq = static_cast<const float*>(w->w_qkvg);
@@ -515,21 +616,62 @@ extern "C" {
 int krea_dit_block_forward(krea_dit_block_t h, const void* x_img, const void* x_txt, int B, int img_h, int img_w,
                            int n_txt, const float* t_emb, const krea_dit_weights* w, void* out,
                            krea_dit_stream_t stream) {
-  return forward_impl(h, x_img, x_txt, nullptr, B, img_h, img_w, n_txt, t_emb, w, out, stream);
+  return forward_impl(h, x_img, x_txt, nullptr, B, img_h, img_w, n_txt, t_emb, w, nullptr, out, stream);
+}
+
+int krea_dit_block_forward8(krea_dit_block_t h, const void* x_img, const void* x_txt, int B, int img_h, int img_w,
+                            int n_txt, const float* t_emb, const krea_dit_weights* w, const krea_dit_weights8* q,
+                            void* out, krea_dit_stream_t stream) {
+  if (!q) return KREA_DIT_ERR_INVALID_ARG;
+  return forward_impl(h, x_img, x_txt, nullptr, B, img_h, img_w, n_txt, t_emb, w, q, out, stream);
+}
+
+int krea_dit_weights8_quantize(krea_dit_block_t h, const krea_dit_weights* w, const krea_dit_weights8* q,
+                               krea_dit_stream_t stream) {
+  if (!h || !w || !q || !h->mode8) return KREA_DIT_ERR_INVALID_ARG;
+  const krea_dit_config& c = h->cfg;
+  const int d = c.d_model, F = c.ffn, nqhd = c.n_q * c.head_dim;
+  struct Mat {
+    const void* src;
+    int rows, cols;
+    void* codes;
+    float* dq;
+  };
+  const Mat mats[5] = {{w->w_qkvg, h->n_qkvg, d, q->w_qkvg, q->dq_qkvg},
+                       {w->w_o, d, nqhd, q->w_o, q->dq_o},
+                       {w->w_gate, F, d, q->w_gate, q->dq_gate},
+                       {w->w_up, F, d, q->w_up, q->dq_up},
+                       {w->w_down, d, F, q->w_down, q->dq_down}};
+  for (const Mat& m : mats) {
+    if (!m.src || !m.codes || !m.dq) return KREA_DIT_ERR_INVALID_ARG;
+    if (!aligned16(m.src) || !aligned16(m.codes) || !aligned16(m.dq)) return KREA_DIT_ERR_MISALIGNED;
+  }
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const int per_row = h->mode8 == 2;
+  cudaError_t e = cudaSuccess;
+  for (const Mat& m : mats) {
+    if (e == cudaSuccess)
+      e = timed(h, S_W8_AMAX, st, [&] { return kd::launch_row_amax(m.src, m.rows, m.cols, h->am_w, h->num_sms, st); });
+    if (e == cudaSuccess)
+      e = timed(h, S_W8_QUANT, st, [&] {
+        return kd::launch_quant_e4m3(m.src, m.rows, m.cols, h->am_w, per_row, m.codes, m.dq, h->num_sms, st);
+      });
+  }
+  return e == cudaSuccess ? KREA_DIT_OK : KREA_DIT_ERR_CUDA;
 }
 
 int krea_dit_block_forward_joint(krea_dit_block_t h, const void* x, int B, int img_h, int img_w, int n_txt,
                                  const float* t_emb, const krea_dit_weights* w, void* out,
                                  krea_dit_stream_t stream) {
   if (!x) return KREA_DIT_ERR_INVALID_ARG;
-  return forward_impl(h, nullptr, nullptr, x, B, img_h, img_w, n_txt, t_emb, w, out, stream);
+  return forward_impl(h, nullptr, nullptr, x, B, img_h, img_w, n_txt, t_emb, w, nullptr, out, stream);
 }
 
 int krea_dit_stack_forward(krea_dit_block_t h, void* x, int B, int img_h, int img_w, int n_txt, const float* t_emb,
                            const krea_dit_weights* w, int n_blocks, krea_dit_stream_t stream) {
   if (!h || !x || n_blocks < 0 || (n_blocks > 0 && !w)) return KREA_DIT_ERR_INVALID_ARG;
   for (int i = 0; i < n_blocks; ++i) {
-    const int r = forward_impl(h, nullptr, nullptr, x, B, img_h, img_w, n_txt, t_emb, &w[i], x, stream);
+    const int r = forward_impl(h, nullptr, nullptr, x, B, img_h, img_w, n_txt, t_emb, &w[i], nullptr, x, stream);
     if (r != KREA_DIT_OK) return r;
   }
   return KREA_DIT_OK;
@@ -677,6 +819,19 @@ int krea_dit_block_workspace(krea_dit_block_t h, int which, void** dev_ptr, size
     case KREA_DIT_BUF_H1: *dev_ptr = h->h1; *bytes = T * h->cfg.d_model * 4; break;
     case KREA_DIT_BUF_HN: *dev_ptr = h->hn; *bytes = T * h->cfg.d_model * es; break;
     case KREA_DIT_BUF_HMID: *dev_ptr = h->hmid; *bytes = T * h->cfg.ffn * es; break;
+    case KREA_DIT_BUF_XN8: *dev_ptr = h->xn8; *bytes = h->mode8 ? T * h->cfg.d_model : 0; break;
+    case KREA_DIT_BUF_OG8: *dev_ptr = h->og8; *bytes = h->mode8 ? T * h->cfg.n_q * hd : 0; break;
+    case KREA_DIT_BUF_HN8: *dev_ptr = h->hn8; *bytes = h->mode8 ? T * h->cfg.d_model : 0; break;
+    case KREA_DIT_BUF_HMID8: *dev_ptr = h->hmid8; *bytes = h->mode8 ? T * h->cfg.ffn : 0; break;
+    case KREA_DIT_BUF_DQ_XN:
+    case KREA_DIT_BUF_DQ_OG:
+    case KREA_DIT_BUF_DQ_HN:
+    case KREA_DIT_BUF_DQ_HMID: {
+      float* const dqs[4] = {h->dq_xn, h->dq_og, h->dq_hn, h->dq_hmid};
+      *dev_ptr = dqs[which - KREA_DIT_BUF_DQ_XN];
+      *bytes = h->mode8 ? (h->mode8 == 2 ? T : (T ? 1 : 0)) * sizeof(float) : 0;
+      break;
+    }
     default: return KREA_DIT_ERR_INVALID_ARG;
   }
   return KREA_DIT_OK;

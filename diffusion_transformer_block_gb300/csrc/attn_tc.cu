@@ -52,6 +52,7 @@ struct AttnArgs {
   float scale_log2;  // log2(e) / sqrt(hd)
   const bf16* g;     // [T, n_q*hd] gate pre-activation
   bf16* og;          // [T, n_q*hd]
+  float* rowamax;    // optional [T]: largest |og| of each row, as stored (for an 8-bit o_proj)
   int* err;
 };
 
@@ -333,6 +334,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const float inv_l = 1.0f / l_run;
         const size_t off =
             (static_cast<size_t>(b) * a.L + (valid ? ql : 0)) * (a.n_q * HD) + tile_head(t) * HD;
+        float amax = 0.0f;
         uint32_t r[32];
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {
@@ -360,8 +362,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             for (int q4 = 0; q4 < 4; ++q4)
               o4[q4] = make_uint4(pack_bf16x2(o[8 * q4 + 0], o[8 * q4 + 1]), pack_bf16x2(o[8 * q4 + 2], o[8 * q4 + 3]),
                                   pack_bf16x2(o[8 * q4 + 4], o[8 * q4 + 5]), pack_bf16x2(o[8 * q4 + 6], o[8 * q4 + 7]));
+            if (a.rowamax) {
+#pragma unroll
+              for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(o[i]));
+            }
           }
         }
+        // bf16 rounding is monotone, so the largest stored magnitude is the rounded largest
+        if (a.rowamax && valid)
+          atomic_max_nonneg(a.rowamax + static_cast<size_t>(b) * a.L + ql, round_bf16(amax));
       }
       tc_fence_before();
     }
@@ -381,7 +390,7 @@ cudaError_t attn_tc_init() {
 }
 
 cudaError_t launch_attn_tc(const Fwd& f, const CUtensorMap* tm_q, const CUtensorMap* tm_k, const CUtensorMap* tm_vt,
-                           const void* g, void* og, int num_sms, int* err, cudaStream_t st) {
+                           const void* g, void* og, float* rowamax, int num_sms, int* err, cudaStream_t st) {
   (void)num_sms;
   AttnArgs a;
   a.B = f.B;
@@ -396,6 +405,7 @@ cudaError_t launch_attn_tc(const Fwd& f, const CUtensorMap* tm_q, const CUtensor
   a.scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(HD));
   a.g = reinterpret_cast<const bf16*>(g);
   a.og = reinterpret_cast<bf16*>(og);
+  a.rowamax = rowamax;
   a.err = err;
   const long long units = static_cast<long long>(f.B) * f.n_kv * a.npairs;
   if (units == 0) return cudaSuccess;

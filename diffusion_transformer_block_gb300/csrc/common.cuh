@@ -229,6 +229,23 @@ __device__ __forceinline__ void mma_bf16_ss(uint32_t d_tmem, uint64_t a_desc, ui
 }
 // D[tmem] (+)= A[tmem] * B[smem]^T: A (M x K, K-major) read from tensor memory, two
 // consecutive 16-bit elements of a row per 32-bit column; one CTA, single thread.
+// e4m3 x e4m3 -> fp32 (A and B both e4m3: format code 0 in both fields)
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N) {
+  return (1u << 4)                                  // D format: fp32
+         | (static_cast<uint32_t>(N >> 3) << 17)    // N / 8
+         | (static_cast<uint32_t>(M >> 4) << 24);   // M / 16
+}
+// One 8-bit MMA step: K = 32 elements (32 bytes of each K-major operand row).
+__device__ __forceinline__ void mma_e4m3_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 __device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
                                             uint32_t accumulate) {
   asm volatile(
@@ -311,3 +328,37 @@ __device__ __forceinline__ void tmem_st64(uint32_t taddr, const uint32_t (&r)[64
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 }  // namespace kd
+
+// ------------------------------------------------------------------ e4m3 casts
+// Scaled e4m3 operands: a group (a tensor, or one row) with largest magnitude amax is
+// multiplied by 2^k, k the largest integer with amax 2^k <= 448 (k = 0 for amax = 0,
+// capped at 125), cast to e4m3 (nearest, ties to even, saturating), and dequantised by
+// 2^-k. Power-of-two scales make the scaling exact.
+__device__ __forceinline__ int e4m3_scale_exp(float amax) {
+  if (!(amax > 0.0f)) return 0;
+  int e = 0;
+  const float m = frexpf(amax, &e);  // amax = m 2^e, 0.5 <= m < 1
+  const int k = (m <= 0.875f ? 9 : 8) - e;
+  return k < 125 ? k : 125;
+}
+__device__ __forceinline__ float pow2f(int k) {  // 2^k for -126 <= k <= 127
+  return __int_as_float((127 + k) << 23);
+}
+// Two fp32 values -> two e4m3 codes (lo in the low byte).
+__device__ __forceinline__ uint16_t cvt_e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+// Eight fp32 values -> eight e4m3 codes in a uint2 (element 0 in the lowest byte).
+__device__ __forceinline__ uint2 cvt_e4m3x8(const float (&v)[8]) {
+  const uint32_t a = cvt_e4m3x2(v[0], v[1]) | (static_cast<uint32_t>(cvt_e4m3x2(v[2], v[3])) << 16);
+  const uint32_t b = cvt_e4m3x2(v[4], v[5]) | (static_cast<uint32_t>(cvt_e4m3x2(v[6], v[7])) << 16);
+  return make_uint2(a, b);
+}
+// bf16 rounding of an fp32 value, returned as fp32 (the value a bf16 store keeps)
+__device__ __forceinline__ float round_bf16(float x) { return __bfloat162float(__float2bfloat16_rn(x)); }
+// atomic max of a non-negative float (as its bit pattern, which orders the same way)
+__device__ __forceinline__ void atomic_max_nonneg(float* p, float v) {
+  atomicMax(reinterpret_cast<unsigned int*>(p), __float_as_uint(v));
+}

@@ -1,4 +1,5 @@
-// Tensor-core GEMMs of the DiT block (bf16 in, fp32 accumulate), tcgen05 + TMA, sm_103a.
+// Tensor-core GEMMs of the DiT block (bf16 or scaled e4m3 in, fp32 accumulate), tcgen05 +
+// TMA, sm_103a.
 //
 // One persistent, warp-specialised kernel template with three fused epilogues:
 //   * QKVG  : xn W_qkvg^T -> per-head QK-RMSNorm, 2D axial RoPE, scatter to Q, K, V^T, G
@@ -10,8 +11,12 @@
 //   * SWIGLU: silu(hn W_gate^T) * (hn W_up^T), both products in one 128x256 accumulator
 //             ("Transformer block": SwiGLU MLP)
 //
-// Tile 128 x 256 x 64: A tile 16 KB + B tile 32 KB per stage, 4 stages in shared memory,
-// written by TMA with the 128-byte swizzle. The accumulator is double-buffered in TMEM
+// Tile 128 x 256 x 64 (bf16) or 128 x 256 x 128 (e4m3): either way 128-byte operand rows,
+// A tile 16 KB + B tile 32 KB per stage, 4 stages in shared memory, written by TMA with the
+// 128-byte swizzle; one stage is four MMAs of 32 bytes of K (kind::f16, K = 16, or
+// kind::f8f6f4, K = 32). The 8-bit GEMMs ("训练 › 预训练" / Training › Pretraining: 8-bit
+// training with tensor-wise or row-wise scaling) multiply e4m3 codes and dequantise each
+// accumulator by the power-of-two factors of its row and column in the epilogue. The accumulator is double-buffered in TMEM
 // (2 x 256 columns), so the epilogue of one tile overlaps the main loop of the next.
 // Warp roles: warp 0 = TMA producer (one thread), warp 1 = TMEM allocator + MMA issuer
 // (one thread), warps 2..9 = epilogue (two warpgroups, one per 128-column half).
@@ -29,9 +34,9 @@
 namespace kd {
 namespace {
 
-constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
-constexpr int A_BYTES = BM * BK * 2;
-constexpr int B_BYTES = BN * BK * 2;
+constexpr int BM = 128, BN = 256, BK_BYTES = 128, STAGES = 4;
+constexpr int A_BYTES = BM * BK_BYTES;
+constexpr int B_BYTES = BN * BK_BYTES;
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int TMEM_COLS = 2 * BN;
 constexpr int NUM_EPI_WARPS = 8;
@@ -67,15 +72,47 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, int* 
 
 __device__ __forceinline__ float u2f(uint32_t u) { return __uint_as_float(u); }
 
+// Dequantise 32 accumulator columns col .. col+31 of one row (8-bit GEMMs only):
+// fa = the row's factor, bp = the column factors. Products of powers of two: exact.
+template <bool S8>
+__device__ __forceinline__ void deq32(uint32_t (&r)[32], const Deq& dq, float fa, const float* bp, int col) {
+  if constexpr (S8) {
+    if (dq.per_row) {
+      const float4* b4 = reinterpret_cast<const float4*>(bp + col);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const float4 b = __ldg(b4 + q);
+        r[4 * q + 0] = __float_as_uint(u2f(r[4 * q + 0]) * (fa * b.x));
+        r[4 * q + 1] = __float_as_uint(u2f(r[4 * q + 1]) * (fa * b.y));
+        r[4 * q + 2] = __float_as_uint(u2f(r[4 * q + 2]) * (fa * b.z));
+        r[4 * q + 3] = __float_as_uint(u2f(r[4 * q + 3]) * (fa * b.w));
+      }
+    } else {
+      const float s = fa * __ldg(bp);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(u2f(r[i]) * s);
+    }
+  }
+}
+// the row's factor (0 for rows past M, whose results are discarded)
+template <bool S8>
+__device__ __forceinline__ float deq_row(const Deq& dq, int row, bool ok) {
+  if constexpr (S8) return ok ? __ldg(dq.a + (dq.per_row ? row : 0)) : 0.0f;
+  return 1.0f;
+}
+
 // ------------------------------------------------------------------ epilogues
 // apply(): called by one epilogue warp for its 32 rows (one per lane) and one 128-column
 // half of the 256-column accumulator. `taddr` = TMEM address of the lane's row at
 // accumulator column 0. TMEM loads are warp-collective; stores are masked by row < M.
 
-struct EpiQKVG {
+template <bool S8>
+struct EpiQKVGT {
+  static constexpr bool kS8 = S8;
   Fwd f;
   QkvgDst dst;
   int N;  // rows of W_qkvg
+  Deq dq;
   __device__ __forceinline__ void apply(int row, int nb, int half, uint32_t taddr, int M) const {
     constexpr int HD = 128;
     const int n0 = nb * BN + half * HD;
@@ -90,6 +127,7 @@ struct EpiQKVG {
     const int b = ok ? row / f.L : 0;
     const int l = ok ? row - b * f.L : 0;
     const uint32_t t0 = taddr + half * HD;
+    const float fa = deq_row<S8>(dq, row, ok);
     uint32_t r[32];
 
     if (kind <= 1) {
@@ -97,6 +135,7 @@ struct EpiQKVG {
 #pragma unroll 1
       for (int c = 0; c < 4; ++c) {
         tmem_ld32(t0 + c * 32, r);
+        deq32<S8>(r, dq, fa, dq.b, n0 + c * 32);
 #pragma unroll
         for (int i = 0; i < 32; ++i) ss = fmaf(u2f(r[i]), u2f(r[i]), ss);
       }
@@ -115,6 +154,7 @@ struct EpiQKVG {
 #pragma unroll 1
       for (int c = 0; c < 4; ++c) {
         tmem_ld32(t0 + c * 32, r);
+        deq32<S8>(r, dq, fa, dq.b, n0 + c * 32);
         float v[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) v[i] = u2f(r[i]) * rstd * (1.0f + __ldg(w + c * 32 + i));
@@ -144,6 +184,7 @@ struct EpiQKVG {
 #pragma unroll 1
       for (int c = 0; c < 4; ++c) {
         tmem_ld32(t0 + c * 32, r);
+        deq32<S8>(r, dq, fa, dq.b, n0 + c * 32);
         if (ok) {
 #pragma unroll
           for (int i = 0; i < 32; ++i) vt[static_cast<size_t>(c * 32 + i) * f.Lp] = __float2bfloat16_rn(u2f(r[i]));
@@ -154,6 +195,7 @@ struct EpiQKVG {
 #pragma unroll 1
       for (int c = 0; c < 4; ++c) {
         tmem_ld32(t0 + c * 32, r);
+        deq32<S8>(r, dq, fa, dq.b, n0 + c * 32);
         if (ok) {
           uint4* o4 = reinterpret_cast<uint4*>(g + c * 32);
 #pragma unroll
@@ -190,14 +232,16 @@ __device__ __forceinline__ void store_out8(float* p, const float (&v)[8]) {
 // out = res + gate * acc. The attention residual reads the bf16 block input from the
 // caller's split text/image buffers and writes the fp32 residual stream h1; the MLP
 // residual reads h1 and writes the bf16 block output.
-template <class TRes, class TOut>
+template <class TRes, class TOut, bool S8>
 struct EpiResid {
+  static constexpr bool kS8 = S8;
   Fwd f;
   RowSrc res;
   const float* mod_shared;
   const float* mod_bias;
   int chunk;   // modulation chunk of the gate (2 = gate_a, 5 = gate_m)
   TOut* out;   // [T, d]
+  Deq dq;
   __device__ __forceinline__ void apply(int row, int nb, int half, uint32_t taddr, int M) const {
     const int N = f.d;
     const int n0 = nb * BN + half * 128;
@@ -207,12 +251,14 @@ struct EpiResid {
     const TRes* x = ok ? row_src_ptr<TRes>(res, row, f.L, f.n_txt, f.n_img, f.d) : nullptr;
     const float* gs = mod_shared + (static_cast<size_t>(b) * 6 + chunk) * N;
     const float* gb = mod_bias + static_cast<size_t>(chunk) * N;
+    const float fa = deq_row<S8>(dq, row, ok);
     uint32_t r[32];
 #pragma unroll 1
     for (int c = 0; c < 4; ++c) {
       const int col = n0 + c * 32;
       if (col >= N) break;
       tmem_ld32(taddr + half * 128 + c * 32, r);
+      deq32<S8>(r, dq, fa, dq.b, col);
       if (ok) {
         const float4* gs4 = reinterpret_cast<const float4*>(gs + col);
         const float4* gb4 = reinterpret_cast<const float4*>(gb + col);
@@ -234,32 +280,49 @@ struct EpiResid {
     }
   }
 };
-using EpiResidAttn = EpiResid<bf16, float>;
-using EpiResidMlp = EpiResid<float, bf16>;
+template <bool S8>
+using EpiResidAttnT = EpiResid<bf16, float, S8>;
+template <bool S8>
+using EpiResidMlpT = EpiResid<float, bf16, S8>;
 
-struct EpiSwiGLU {
+template <bool S8>
+struct EpiSwiGLUT {
+  static constexpr bool kS8 = S8;
   int F;
-  bf16* hmid;  // [T, F]
+  bf16* hmid;      // [T, F]
+  float* rowamax;  // optional [T] (8-bit GEMMs only): largest |hmid| of each row, as stored
+  Deq dq;
   // accumulator columns [0,128) = hn W_gate^T, [128,256) = hn W_up^T for F-columns nb*128 ..
   __device__ __forceinline__ void apply(int row, int nb, int half, uint32_t taddr, int M) const {
     const int f0 = nb * 128 + half * 64;
     if (f0 >= F) return;
     const bool ok = row < M;
+    const float fa = deq_row<S8>(dq, row, ok);
+    float amax = 0.0f;
     uint32_t rg[32], ru[32];
 #pragma unroll 1
     for (int c = 0; c < 2; ++c) {
       tmem_ld32x2(taddr + half * 64 + c * 32, taddr + 128 + half * 64 + c * 32, rg, ru);
+      deq32<S8>(rg, dq, fa, dq.b, f0 + c * 32);
+      deq32<S8>(ru, dq, fa, dq.b2, f0 + c * 32);
       if (ok) {
         uint4* o4 = reinterpret_cast<uint4*>(hmid + static_cast<size_t>(row) * F + f0 + c * 32);
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4) {
           float h[8];
 #pragma unroll
-          for (int i = 0; i < 8; ++i) h[i] = siluf_(u2f(rg[8 * q4 + i])) * u2f(ru[8 * q4 + i]);
+          for (int i = 0; i < 8; ++i) {
+            h[i] = siluf_(u2f(rg[8 * q4 + i])) * u2f(ru[8 * q4 + i]);
+            if constexpr (S8) amax = fmaxf(amax, fabsf(h[i]));
+          }
           o4[q4] = make_uint4(pack_bf16x2(h[0], h[1]), pack_bf16x2(h[2], h[3]), pack_bf16x2(h[4], h[5]),
                               pack_bf16x2(h[6], h[7]));
         }
       }
+    }
+    // bf16 rounding is monotone, so the largest stored magnitude is the rounded largest
+    if constexpr (S8) {
+      if (rowamax && ok) atomic_max_nonneg(rowamax + row, round_bf16(amax));
     }
   }
 };
@@ -269,6 +332,8 @@ template <class Epi, bool DUAL>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                    const __grid_constant__ CUtensorMap tm_b2, int M, int num_n, int K, Epi epi, int* err) {
+  constexpr bool FP8 = Epi::kS8;
+  constexpr int BK = FP8 ? 128 : 64;  // K elements per stage (128 bytes of each operand row)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
@@ -354,7 +419,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   } else if (warp == 1) {
     if (lane == 0) {
       // ---------------- MMA issuer
-      constexpr uint32_t idesc = idesc_bf16_f32(BM, BN);
+      constexpr uint32_t idesc = FP8 ? idesc_e4m3_f32(BM, BN) : idesc_bf16_f32(BM, BN);
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
@@ -373,9 +438,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const uint32_t sa = smem_u32(smem + stage * STAGE_BYTES);
           const uint32_t sb = sa + A_BYTES;
 #pragma unroll
-          for (int k = 0; k < BK / 16; ++k)
-            mma_bf16_ss(d_tmem, sdesc_kmajor_sw128(sa + k * 32), sdesc_kmajor_sw128(sb + k * 32), idesc,
-                        (kb | k) != 0 ? 1u : 0u);
+          for (int k = 0; k < 4; ++k) {  // 32 bytes of K per MMA
+            if constexpr (FP8)
+              mma_e4m3_ss(d_tmem, sdesc_kmajor_sw128(sa + k * 32), sdesc_kmajor_sw128(sb + k * 32), idesc,
+                          (kb | k) != 0 ? 1u : 0u);
+            else
+              mma_bf16_ss(d_tmem, sdesc_kmajor_sw128(sa + k * 32), sdesc_kmajor_sw128(sb + k * 32), idesc,
+                          (kb | k) != 0 ? 1u : 0u);
+          }
           mma_commit_mc(&empty[stage], 0x3);  // frees the stage (in both CTAs) once these MMAs read it
           if (++stage == STAGES) {
             stage = 0;
@@ -485,39 +555,66 @@ cudaError_t launch(const CUtensorMap* a, const CUtensorMap* b, const CUtensorMap
 
 int gemm_tc_smem_bytes() { return SMEM_BYTES; }
 
-cudaError_t gemm_tc_init(int num_sms) {
+template <bool S8>
+cudaError_t gemm_tc_init_set(int num_sms) {
   cudaError_t e;
-  if ((e = set_smem_attr<EpiQKVG, false>(num_sms)) != cudaSuccess) return e;
-  if ((e = set_smem_attr<EpiResidAttn, false>(num_sms)) != cudaSuccess) return e;
-  if ((e = set_smem_attr<EpiResidMlp, false>(num_sms)) != cudaSuccess) return e;
-  if ((e = set_smem_attr<EpiSwiGLU, true>(num_sms)) != cudaSuccess) return e;
-  return cudaSuccess;
+  if ((e = set_smem_attr<EpiQKVGT<S8>, false>(num_sms)) != cudaSuccess) return e;
+  if ((e = set_smem_attr<EpiResidAttnT<S8>, false>(num_sms)) != cudaSuccess) return e;
+  if ((e = set_smem_attr<EpiResidMlpT<S8>, false>(num_sms)) != cudaSuccess) return e;
+  return set_smem_attr<EpiSwiGLUT<S8>, true>(num_sms);
+}
+
+cudaError_t gemm_tc_init(int num_sms) {
+  cudaError_t e = gemm_tc_init_set<false>(num_sms);
+  return e != cudaSuccess ? e : gemm_tc_init_set<true>(num_sms);
 }
 
 cudaError_t launch_gemm_qkvg(const Fwd& f, const CUtensorMap* tm_a, const CUtensorMap* tm_b, int N,
-                             const QkvgDst& dst, int num_sms, int* err, cudaStream_t st) {
-  EpiQKVG epi{f, dst, N};
-  return launch<EpiQKVG, false>(tm_a, tm_b, tm_b, f.T, (N + BN - 1) / BN, f.d, epi, num_sms, err, st);
+                             const QkvgDst& dst, const Deq* dq, int num_sms, int* err, cudaStream_t st) {
+  const int num_n = (N + BN - 1) / BN;
+  if (dq) {
+    EpiQKVGT<true> epi{f, dst, N, *dq};
+    return launch<EpiQKVGT<true>, false>(tm_a, tm_b, tm_b, f.T, num_n, f.d, epi, num_sms, err, st);
+  }
+  EpiQKVGT<false> epi{f, dst, N, Deq{}};
+  return launch<EpiQKVGT<false>, false>(tm_a, tm_b, tm_b, f.T, num_n, f.d, epi, num_sms, err, st);
 }
 
 cudaError_t launch_gemm_resid_attn(const Fwd& f, const CUtensorMap* tm_a, const CUtensorMap* tm_b, int K, RowSrc x,
-                                   const float* mod_shared, const float* mod_bias, float* h1, int num_sms, int* err,
-                                   cudaStream_t st) {
-  EpiResidAttn epi{f, x, mod_shared, mod_bias, 2, h1};
-  return launch<EpiResidAttn, false>(tm_a, tm_b, tm_b, f.T, (f.d + BN - 1) / BN, K, epi, num_sms, err, st);
+                                   const float* mod_shared, const float* mod_bias, float* h1, const Deq* dq,
+                                   int num_sms, int* err, cudaStream_t st) {
+  const int num_n = (f.d + BN - 1) / BN;
+  if (dq) {
+    EpiResidAttnT<true> epi{f, x, mod_shared, mod_bias, 2, h1, *dq};
+    return launch<EpiResidAttnT<true>, false>(tm_a, tm_b, tm_b, f.T, num_n, K, epi, num_sms, err, st);
+  }
+  EpiResidAttnT<false> epi{f, x, mod_shared, mod_bias, 2, h1, Deq{}};
+  return launch<EpiResidAttnT<false>, false>(tm_a, tm_b, tm_b, f.T, num_n, K, epi, num_sms, err, st);
 }
 
 cudaError_t launch_gemm_resid_mlp(const Fwd& f, const CUtensorMap* tm_a, const CUtensorMap* tm_b, int K,
                                   const float* h1, const float* mod_shared, const float* mod_bias, void* out,
-                                  int num_sms, int* err, cudaStream_t st) {
-  EpiResidMlp epi{f, RowSrc{nullptr, nullptr, h1}, mod_shared, mod_bias, 5, reinterpret_cast<bf16*>(out)};
-  return launch<EpiResidMlp, false>(tm_a, tm_b, tm_b, f.T, (f.d + BN - 1) / BN, K, epi, num_sms, err, st);
+                                  const Deq* dq, int num_sms, int* err, cudaStream_t st) {
+  const int num_n = (f.d + BN - 1) / BN;
+  const RowSrc res{nullptr, nullptr, h1};
+  if (dq) {
+    EpiResidMlpT<true> epi{f, res, mod_shared, mod_bias, 5, reinterpret_cast<bf16*>(out), *dq};
+    return launch<EpiResidMlpT<true>, false>(tm_a, tm_b, tm_b, f.T, num_n, K, epi, num_sms, err, st);
+  }
+  EpiResidMlpT<false> epi{f, res, mod_shared, mod_bias, 5, reinterpret_cast<bf16*>(out), Deq{}};
+  return launch<EpiResidMlpT<false>, false>(tm_a, tm_b, tm_b, f.T, num_n, K, epi, num_sms, err, st);
 }
 
 cudaError_t launch_gemm_swiglu(const Fwd& f, const CUtensorMap* tm_a, const CUtensorMap* tm_gate,
-                               const CUtensorMap* tm_up, void* hmid, int num_sms, int* err, cudaStream_t st) {
-  EpiSwiGLU epi{f.F, reinterpret_cast<bf16*>(hmid)};
-  return launch<EpiSwiGLU, true>(tm_a, tm_gate, tm_up, f.T, (f.F + 127) / 128, f.d, epi, num_sms, err, st);
+                               const CUtensorMap* tm_up, void* hmid, float* rowamax, const Deq* dq, int num_sms,
+                               int* err, cudaStream_t st) {
+  const int num_n = (f.F + 127) / 128;
+  if (dq) {
+    EpiSwiGLUT<true> epi{f.F, reinterpret_cast<bf16*>(hmid), rowamax, *dq};
+    return launch<EpiSwiGLUT<true>, true>(tm_a, tm_gate, tm_up, f.T, num_n, f.d, epi, num_sms, err, st);
+  }
+  EpiSwiGLUT<false> epi{f.F, reinterpret_cast<bf16*>(hmid), rowamax, Deq{}};
+  return launch<EpiSwiGLUT<false>, true>(tm_a, tm_gate, tm_up, f.T, num_n, f.d, epi, num_sms, err, st);
 }
 
 }  // namespace kd

@@ -33,6 +33,15 @@ struct QkvgDst {
   const float2* rope;  // [pos][hd/4] (cos, sin)
 };
 
+// Dequantisation factors of an 8-bit GEMM (powers of two): row m, column n of the
+// product is scaled by a[m] * b[n] (per_row) or a[0] * b[0] (per tensor).
+struct Deq {
+  const float* a;   // A (activation) factors: [M] or [1]
+  const float* b;   // B (weight) factors: [N] or [1]
+  const float* b2;  // second B of the SwiGLU GEMM (W_up)
+  int per_row;
+};
+
 #ifdef __CUDACC__
 // Pointer to row m of a block input (see RowSrc).
 template <class T>
@@ -49,10 +58,23 @@ __device__ __forceinline__ const T* row_src_ptr(const RowSrc& s, int m, int L, i
 cudaError_t norm_init(int d);
 // input -> output storage types of a norm+modulate launch
 enum class NormIO { BF16_BF16, F32_BF16, F32_F32 };
-// requires d % 8 == 0 and d <= 8192 (a warp holds a row in registers)
+// e4m3 output of a norm+modulate launch (the bf16-rounded row cast to e4m3):
+//   NONE   : plain output (`out`, type from NormIO)
+//   ROW    : row-wise scaled codes -> q8 [T, d], dq [T]
+//   AMAX   : no output; rowamax[m] = largest |bf16 row value|
+//   TENSOR : codes with one scale from max(rowamax[0..T)) -> q8, dq [1]
+enum class NormQ { NONE, ROW, AMAX, TENSOR };
+struct NormQOut {
+  NormQ mode;
+  void* q8;
+  float* dq;
+  float* rowamax;
+};
+// requires d % 8 == 0 and d <= 8192 (a warp holds a row in registers); e4m3 modes need
+// NormIO::BF16_BF16 or F32_BF16 (the row is rounded to bf16 before the cast) and d <= 3072
 cudaError_t launch_norm_modulate(NormIO io, const Fwd& f, RowSrc src, const float* gain_w, const float* mod_shared,
                                  const float* mod_bias, int chunk_shift, int chunk_scale, void* out, int num_sms,
-                                 cudaStream_t st);
+                                 cudaStream_t st, const NormQOut* q8 = nullptr);
 cudaError_t launch_temb_sinusoid(const float* t, int B, float* e, cudaStream_t st);
 // C[M,N] = act(A[M,K] * W[N,K]^T + bias), fp32, act = 1 -> silu
 cudaError_t launch_gemm_simt_f32(const float* A, const float* W, float* C, int M, int N, int K, const float* bias,
@@ -68,29 +90,44 @@ cudaError_t launch_residual_f32(const Fwd& f, RowSrc res, const float* acc, cons
 // fp32 mode: hmid = silu(a) * u
 cudaError_t launch_swiglu_f32(const Fwd& f, const float* a, const float* u, float* hmid, cudaStream_t st);
 
-// ---- gemm_tc.cu (bf16 mode, tcgen05 + TMA) ----
+// ---- gemm_tc.cu (bf16 and e4m3 operands, tcgen05 + TMA) ----
+// Every launcher takes `dq`: nullptr = bf16 operands (tensor maps of bf16), otherwise
+// e4m3 operands (tensor maps of bytes) whose products are dequantised by dq.
 int gemm_tc_smem_bytes();
 // sets the kernels' dynamic shared-memory limit and queries co-resident CTA pairs (once per
 // handle, before any stream capture)
 cudaError_t gemm_tc_init(int num_sms);
 // xn[T,d] x W_qkvg^T -> QK-norm, RoPE, scatter to Q / K / V^T / G
 cudaError_t launch_gemm_qkvg(const Fwd& f, const CUtensorMap* tm_a, const CUtensorMap* tm_b, int N,
-                             const QkvgDst& dst, int num_sms, int* err, cudaStream_t st);
+                             const QkvgDst& dst, const Deq* dq, int num_sms, int* err, cudaStream_t st);
 // h1[T,d] (fp32) = x (bf16, split buffers) + gate_a * (A W^T)
 cudaError_t launch_gemm_resid_attn(const Fwd& f, const CUtensorMap* tm_a, const CUtensorMap* tm_b, int K, RowSrc x,
-                                   const float* mod_shared, const float* mod_bias, float* h1, int num_sms, int* err,
-                                   cudaStream_t st);
+                                   const float* mod_shared, const float* mod_bias, float* h1, const Deq* dq,
+                                   int num_sms, int* err, cudaStream_t st);
 // out[T,d] (bf16) = h1 (fp32) + gate_m * (A W^T)
 cudaError_t launch_gemm_resid_mlp(const Fwd& f, const CUtensorMap* tm_a, const CUtensorMap* tm_b, int K,
                                   const float* h1, const float* mod_shared, const float* mod_bias, void* out,
-                                  int num_sms, int* err, cudaStream_t st);
-// hmid[T,F] = silu(hn W_gate^T) * (hn W_up^T)
+                                  const Deq* dq, int num_sms, int* err, cudaStream_t st);
+// hmid[T,F] = silu(hn W_gate^T) * (hn W_up^T); rowamax (optional, pre-zeroed [T]) gets
+// each row's largest |hmid| as stored (bf16)
 cudaError_t launch_gemm_swiglu(const Fwd& f, const CUtensorMap* tm_a, const CUtensorMap* tm_gate,
-                               const CUtensorMap* tm_up, void* hmid, int num_sms, int* err, cudaStream_t st);
+                               const CUtensorMap* tm_up, void* hmid, float* rowamax, const Deq* dq, int num_sms,
+                               int* err, cudaStream_t st);
 
 // ---- attn_tc.cu (bf16 mode, tcgen05 + TMA) ----
 cudaError_t attn_tc_init();
+// og = softmax(q k^T / sqrt(hd)) v * sigmoid(g); rowamax (optional, pre-zeroed [T]) gets
+// each row's largest |og| as stored (bf16)
 cudaError_t launch_attn_tc(const Fwd& f, const CUtensorMap* tm_q, const CUtensorMap* tm_k, const CUtensorMap* tm_vt,
-                           const void* g, void* og, int num_sms, int* err, cudaStream_t st);
+                           const void* g, void* og, float* rowamax, int num_sms, int* err, cudaStream_t st);
+
+// ---- quant8.cu (e4m3 casts of GEMM operands) ----
+// Scaled e4m3 cast of a bf16 matrix src [R, K] (K % 16 == 0) into codes q [R, K]:
+// per_row: row r uses rowamax[r], per tensor: the largest rowamax over all rows. dq gets
+// the dequantisation factors 2^-k ([R] or [1]).
+cudaError_t launch_quant_e4m3(const void* src, int R, int K, const float* rowamax, int per_row, void* q, float* dq,
+                              int num_sms, cudaStream_t st);
+// rowamax[r] = max_k |src[r, k]| of a bf16 matrix [R, K] (K % 8 == 0)
+cudaError_t launch_row_amax(const void* src, int R, int K, float* rowamax, int num_sms, cudaStream_t st);
 
 }  // namespace kd

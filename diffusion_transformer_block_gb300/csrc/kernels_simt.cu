@@ -1,8 +1,5 @@
-// CUDA-core kernels of the DiT block library.
+// CUDA-core kernels of the DiT block library (the norm kernel lives in norm.cu).
 //
-//  * norm_modulate  (both modes): zero-centred RMSNorm + shift/scale modulation with the
-//    per-block bias (Krea 2 Technical Report, "Normalisation" and "Timestep
-//    conditioning"). HBM-bound: 16-byte vector loads/stores, fp32 math.
 //  * temb_sinusoid  (both modes): the sinusoidal timestep embedding ("Timestep
 //    conditioning"), argument and sin/cos in fp64 then rounded to fp32.
 //  * fp32 check mode: a plain tiled fp32 GEMM, the QK-norm + RoPE scatter, the GQA
@@ -14,234 +11,6 @@
 #include "internal.h"
 
 namespace kd {
-
-// ============================================================== norm + modulate
-// y = x / sqrt(mean(x^2) + eps) * (1 + w) * (1 + scale) + shift,
-// scale/shift = mod_shared[b, chunk] + mod_bias[chunk].
-//
-// One warp per row: lane l holds columns 8(l + 32c) .. +7 for c < NV, so all of a row's
-// 16-byte loads are in flight at once and the sum of squares is a warp reduction. A CTA
-// owns a contiguous range of rows; the per-column factors A = (1 + w)(1 + scale) and
-// S = shift of the batch elements it meets are computed once into shared memory (two
-// sets, refreshed when the rows move to a batch element not in them).
-template <class T>
-__device__ __forceinline__ void store8(T* p, const float (&v)[8]);
-template <>
-__device__ __forceinline__ void store8<bf16>(bf16* p, const float (&v)[8]) {
-  *reinterpret_cast<uint4*>(p) = make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]),
-                                            pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7]));
-}
-template <>
-__device__ __forceinline__ void store8<float>(float* p, const float (&v)[8]) {
-  reinterpret_cast<float4*>(p)[0] = make_float4(v[0], v[1], v[2], v[3]);
-  reinterpret_cast<float4*>(p)[1] = make_float4(v[4], v[5], v[6], v[7]);
-}
-
-constexpr int NM_WARPS = 16;
-
-// A row chunk of 8 values kept as loaded (packed bf16 or fp32) between the two passes.
-template <class T>
-struct Raw8;
-template <>
-struct Raw8<bf16> {
-  uint4 u;
-  __device__ __forceinline__ void load(const bf16* p) { u = *reinterpret_cast<const uint4*>(p); }
-  __device__ __forceinline__ void zero() { u = make_uint4(0, 0, 0, 0); }
-  __device__ __forceinline__ void get(float (&v)[8]) const {
-    const float2 a = unpack_bf16x2(u.x), b = unpack_bf16x2(u.y), c = unpack_bf16x2(u.z), e = unpack_bf16x2(u.w);
-    v[0] = a.x; v[1] = a.y; v[2] = b.x; v[3] = b.y; v[4] = c.x; v[5] = c.y; v[6] = e.x; v[7] = e.y;
-  }
-};
-template <>
-struct Raw8<float> {
-  float4 a, b;
-  __device__ __forceinline__ void load(const float* p) {
-    a = reinterpret_cast<const float4*>(p)[0];
-    b = reinterpret_cast<const float4*>(p)[1];
-  }
-  __device__ __forceinline__ void zero() { a = b = make_float4(0.f, 0.f, 0.f, 0.f); }
-  __device__ __forceinline__ void get(float (&v)[8]) const {
-    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
-  }
-};
-
-template <class Tin, class Tout, int NV>
-__global__ void __launch_bounds__(NM_WARPS * 32, 1) norm_modulate_kernel(
-    Fwd f, RowSrc src, const float* __restrict__ gain_w, const float* __restrict__ mod_shared,
-    const float* __restrict__ mod_bias, int chunk_shift, int chunk_scale, int rows_per_cta, Tout* __restrict__ out) {
-  extern __shared__ float nm_smem[];  // [2 sets][A | S][d]
-  __shared__ int set_b[2];
-  const int d = f.d;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int r0 = blockIdx.x * rows_per_cta;
-  const int r1 = min(r0 + rows_per_cta, f.T);
-  auto fill = [&](int set, int b) {  // A, S of batch element b into set (all threads)
-    float* A = nm_smem + set * 2 * d;
-    float* S = A + d;
-    const float* sc_s = mod_shared + (static_cast<size_t>(b) * 6 + chunk_scale) * d;
-    const float* sh_s = mod_shared + (static_cast<size_t>(b) * 6 + chunk_shift) * d;
-    const float* sc_b = mod_bias + static_cast<size_t>(chunk_scale) * d;
-    const float* sh_b = mod_bias + static_cast<size_t>(chunk_shift) * d;
-    for (int c = threadIdx.x; c < d; c += blockDim.x) {
-      A[c] = (1.0f + gain_w[c]) * (1.0f + (sc_s[c] + sc_b[c]));
-      S[c] = sh_s[c] + sh_b[c];
-    }
-  };
-  if (threadIdx.x == 0) {
-    set_b[0] = -1;
-    set_b[1] = -1;
-  }
-  __syncthreads();
-  for (int g0 = r0; g0 < r1; g0 += NM_WARPS) {
-    // batch elements of this group's rows: [g0 / L, (g1 - 1) / L]
-    const int g1 = min(g0 + NM_WARPS, r1);
-    const int blo = g0 / f.L, bhi = (g1 - 1) / f.L;
-    if (set_b[0] != blo || (bhi != blo && set_b[1] != bhi)) {
-      __syncthreads();  // every warp is done with the old sets
-      if (set_b[0] != blo) fill(0, blo);
-      if (bhi != blo && set_b[1] != bhi) fill(1, bhi);
-      __syncthreads();
-      if (threadIdx.x == 0) {
-        set_b[0] = blo;
-        if (bhi != blo) set_b[1] = bhi;
-      }
-      __syncthreads();
-    }
-    const int m = g0 + warp;
-    if (m >= g1) continue;
-    const int b = m / f.L;
-    const Tin* x = row_src_ptr<Tin>(src, m, f.L, f.n_txt, f.n_img, d);
-    Raw8<Tin> raw[NV];
-    float ss = 0.f;
-#pragma unroll
-    for (int c = 0; c < NV; ++c) {
-      const int col = (lane + 32 * c) * 8;
-      if (col < d) raw[c].load(x + col);
-      else raw[c].zero();
-    }
-#pragma unroll
-    for (int c = 0; c < NV; ++c) {
-      float v[8];
-      raw[c].get(v);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) ss = fmaf(v[i], v[i], ss);
-    }
-    ss = warp_sum(ss);
-    const float rstd = 1.0f / sqrtf(ss / static_cast<float>(d) + f.eps);
-    const bool in_sets = b == set_b[0] || b == set_b[1];  // false only when L < 8 (a group spans 3+ batch elements)
-    const float* A = nm_smem + (b == set_b[0] ? 0 : 2 * d);
-    const float* S = A + d;
-    Tout* y = out + static_cast<size_t>(m) * d;
-#pragma unroll
-    for (int c = 0; c < NV; ++c) {
-      const int col = (lane + 32 * c) * 8;
-      if (col < d) {
-        float av[8], sv[8];
-        if (in_sets) {
-          const float4 a0 = *reinterpret_cast<const float4*>(A + col), a1 = *reinterpret_cast<const float4*>(A + col + 4);
-          const float4 s0 = *reinterpret_cast<const float4*>(S + col), s1 = *reinterpret_cast<const float4*>(S + col + 4);
-          av[0] = a0.x; av[1] = a0.y; av[2] = a0.z; av[3] = a0.w; av[4] = a1.x; av[5] = a1.y; av[6] = a1.z; av[7] = a1.w;
-          sv[0] = s0.x; sv[1] = s0.y; sv[2] = s0.z; sv[3] = s0.w; sv[4] = s1.x; sv[5] = s1.y; sv[6] = s1.z; sv[7] = s1.w;
-        } else {
-          const float* sc_s = mod_shared + (static_cast<size_t>(b) * 6 + chunk_scale) * d;
-          const float* sh_s = mod_shared + (static_cast<size_t>(b) * 6 + chunk_shift) * d;
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            av[i] = (1.0f + gain_w[col + i]) * (1.0f + (sc_s[col + i] + mod_bias[chunk_scale * d + col + i]));
-            sv[i] = sh_s[col + i] + mod_bias[chunk_shift * d + col + i];
-          }
-        }
-        float v[8], o[8];
-        raw[c].get(v);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) o[i] = fmaf(v[i] * rstd, av[i], sv[i]);
-        store8<Tout>(y + col, o);
-      }
-    }
-  }
-}
-
-template <class Tin, class Tout, int NV>
-cudaError_t launch_nm(const Fwd& f, RowSrc src, const float* gain_w, const float* mod_shared, const float* mod_bias,
-                      int chunk_shift, int chunk_scale, Tout* out, int num_sms, cudaStream_t st) {
-  const size_t smem = static_cast<size_t>(4) * f.d * sizeof(float);  // limit set by norm_init
-  const int ctas = num_sms;  // one CTA (16 warps) per SM: the parameter fill is paid once per SM
-  int rows = (f.T + ctas - 1) / ctas;
-  rows = (rows + NM_WARPS - 1) / NM_WARPS * NM_WARPS;
-  const int grid = (f.T + rows - 1) / rows;
-  norm_modulate_kernel<Tin, Tout, NV><<<grid, NM_WARPS * 32, smem, st>>>(f, src, gain_w, mod_shared, mod_bias,
-                                                                        chunk_shift, chunk_scale, rows, out);
-  return cudaGetLastError();
-}
-
-template <class Tin, class Tout, int NV>
-cudaError_t init_nm(int d) {
-  return cudaFuncSetAttribute(norm_modulate_kernel<Tin, Tout, NV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              4 * d * static_cast<int>(sizeof(float)));
-}
-
-template <class Tin, class Tout>
-cudaError_t init_nm_all(int d) {
-  const int nv = (d / 8 + 31) / 32;
-#define KD_NMI(N) \
-  if (nv <= N) return init_nm<Tin, Tout, N>(d)
-  KD_NMI(1);
-  KD_NMI(2);
-  KD_NMI(3);
-  KD_NMI(4);
-  KD_NMI(6);
-  KD_NMI(8);
-  KD_NMI(12);
-  KD_NMI(16);
-  KD_NMI(24);
-  KD_NMI(32);
-#undef KD_NMI
-  return cudaErrorInvalidValue;
-}
-
-cudaError_t norm_init(int d) {
-  cudaError_t e;
-  if ((e = init_nm_all<bf16, bf16>(d)) != cudaSuccess) return e;
-  if ((e = init_nm_all<float, bf16>(d)) != cudaSuccess) return e;
-  return init_nm_all<float, float>(d);
-}
-
-template <class Tin, class Tout>
-cudaError_t dispatch_nm(const Fwd& f, RowSrc src, const float* gain_w, const float* mod_shared, const float* mod_bias,
-                        int chunk_shift, int chunk_scale, Tout* out, int num_sms, cudaStream_t st) {
-  const int nv = (f.d / 8 + 31) / 32;  // 8-column chunks per lane
-#define KD_NM(N) \
-  if (nv <= N) return launch_nm<Tin, Tout, N>(f, src, gain_w, mod_shared, mod_bias, chunk_shift, chunk_scale, out, num_sms, st)
-  KD_NM(1);
-  KD_NM(2);
-  KD_NM(3);
-  KD_NM(4);
-  KD_NM(6);
-  KD_NM(8);
-  KD_NM(12);
-  KD_NM(16);
-  KD_NM(24);
-  KD_NM(32);
-#undef KD_NM
-  return cudaErrorInvalidValue;
-}
-
-cudaError_t launch_norm_modulate(NormIO io, const Fwd& f, RowSrc src, const float* gain_w, const float* mod_shared,
-                                 const float* mod_bias, int chunk_shift, int chunk_scale, void* out, int num_sms,
-                                 cudaStream_t st) {
-  switch (io) {
-    case NormIO::BF16_BF16:
-      return dispatch_nm<bf16, bf16>(f, src, gain_w, mod_shared, mod_bias, chunk_shift, chunk_scale,
-                                     reinterpret_cast<bf16*>(out), num_sms, st);
-    case NormIO::F32_BF16:
-      return dispatch_nm<float, bf16>(f, src, gain_w, mod_shared, mod_bias, chunk_shift, chunk_scale,
-                                      reinterpret_cast<bf16*>(out), num_sms, st);
-    case NormIO::F32_F32:
-      return dispatch_nm<float, float>(f, src, gain_w, mod_shared, mod_bias, chunk_shift, chunk_scale,
-                                       reinterpret_cast<float*>(out), num_sms, st);
-  }
-  return cudaErrorInvalidValue;
-}
 
 // ============================================================== timestep sinusoid
 // e[b] = [cos(1000 t w_i) | sin(1000 t w_i)], w_i = 10000^(-i/128), i < 128.

@@ -9,14 +9,17 @@ from typing import Dict, Optional, Sequence
 
 import torch
 
-from . import (KREA_DIT_BF16, KREA_DIT_FP32, krea_dit_block_create, krea_dit_block_destroy,
-               krea_dit_block_forward, krea_dit_block_forward_joint, krea_dit_block_workspace,
+from . import (KREA_DIT_BF16, KREA_DIT_FP8_ROW, KREA_DIT_FP8_TENSOR, KREA_DIT_FP32, krea_dit_block_create,
+               krea_dit_block_destroy, krea_dit_block_forward, krea_dit_block_forward8, krea_dit_block_forward_joint,
+               krea_dit_block_workspace, krea_dit_weights8_quantize, make_weights8,
                krea_dit_graph_destroy, krea_dit_graph_launch, krea_dit_stack_forward, krea_dit_stack_graph_create,
                krea_dit_timestep_embed, make_config, make_temb_weights, make_weights)
 
 WEIGHT_KEYS = ("w_qkvg", "w_o", "w_gate", "w_up", "w_down", "norm1_w", "norm2_w", "q_norm_w", "k_norm_w",
                "mod_bias")
 TEMB_KEYS = ("w1", "b1", "w2", "b2")
+MATRIX_KEYS = ("w_qkvg", "w_o", "w_gate", "w_up", "w_down")
+MODES = {"bf16": KREA_DIT_BF16, "fp32": KREA_DIT_FP32, "fp8_tensor": KREA_DIT_FP8_TENSOR, "fp8_row": KREA_DIT_FP8_ROW}
 
 
 class _DevView:
@@ -28,28 +31,44 @@ class _DevView:
 
 
 class DitBlock:
-    """One block handle. ``mode`` is "bf16" or "fp32" (the storage / arithmetic mode)."""
+    """One block handle. ``mode`` is "bf16", "fp32" (the storage / arithmetic mode) or
+    "fp8_tensor" / "fp8_row" (bf16 storage, 8-bit GEMMs with tensor-wise / row-wise scales)."""
 
     def __init__(self, *, max_batch: int, max_seq: int, d: int, n_q: int, n_kv: int, hd: int, F: int,
                  img_h_max: int, img_w_max: int, gate_on: bool = True, mode: str = "bf16", eps: float = 1e-6,
                  rope_base: float = 10000.0, device: str = "cuda:0"):
         self.device = torch.device(device)
         self.mode = mode
-        self.dtype = torch.bfloat16 if mode == "bf16" else torch.float32
+        self.mode8 = mode.startswith("fp8")
+        self.dtype = torch.float32 if mode == "fp32" else torch.bfloat16
         self.dims = dict(d=d, n_q=n_q, n_kv=n_kv, hd=hd, F=F, gate_on=gate_on)
         cfg = make_config(max_batch=max_batch, max_seq=max_seq, d_model=d, n_q=n_q, n_kv=n_kv, head_dim=hd, ffn=F,
                           img_h_max=img_h_max, img_w_max=img_w_max, eps=eps, rope_base=rope_base, gate_on=gate_on,
-                          mode=KREA_DIT_BF16 if mode == "bf16" else KREA_DIT_FP32)
+                          mode=MODES[mode])
         with torch.cuda.device(self.device):
             self.handle = krea_dit_block_create(cfg)
         self.w: Dict[str, torch.Tensor] = {}
         self.tw: Dict[str, torch.Tensor] = {}
         self._wstruct = None
         self._twstruct = None
+        self.w8: Dict[str, torch.Tensor] = {}
+        self._w8struct = None
 
-    def set_weights(self, w: Dict[str, torch.Tensor]) -> None:
+    def set_weights(self, w: Dict[str, torch.Tensor], stream=None) -> None:
+        """Uploads the weights; in an 8-bit mode also casts the matrices to e4m3 codes."""
         self.w = {k: w[k].to(self.device).contiguous() for k in WEIGHT_KEYS}
         self._wstruct = make_weights(self.w)
+        if self.mode8:
+            per_row = self.mode == "fp8_row"
+            w8: Dict[str, torch.Tensor] = {}
+            for k in MATRIX_KEYS:
+                m = self.w[k]
+                w8[k] = torch.empty(m.shape, device=self.device, dtype=torch.uint8)
+                w8["dq_" + k[2:]] = torch.empty(m.shape[0] if per_row else 1, device=self.device, dtype=torch.float32)
+            self.w8 = w8
+            self._w8struct = make_weights8(w8)
+            krea_dit_weights8_quantize(self.handle, self._wstruct, self._w8struct,
+                                       stream or torch.cuda.current_stream(self.device))
 
     def set_temb_weights(self, tw: Dict[str, torch.Tensor]) -> None:
         self.tw = {k: tw[k].to(self.device, torch.float32).contiguous() for k in TEMB_KEYS}
@@ -69,8 +88,12 @@ class DitBlock:
             out = torch.empty(B, L, self.dims["d"], device=self.device, dtype=self.dtype)
         xi = x_img if (x_img is not None and img_h * img_w > 0) else None
         xt = x_txt if (x_txt is not None and n_txt > 0) else None
-        krea_dit_block_forward(self.handle, xi, xt, B, img_h, img_w, n_txt, t_emb, self._wstruct, out,
-                               stream or torch.cuda.current_stream(self.device))
+        st = stream or torch.cuda.current_stream(self.device)
+        if self.mode8:
+            krea_dit_block_forward8(self.handle, xi, xt, B, img_h, img_w, n_txt, t_emb, self._wstruct, self._w8struct,
+                                    out, st)
+        else:
+            krea_dit_block_forward(self.handle, xi, xt, B, img_h, img_w, n_txt, t_emb, self._wstruct, out, st)
         return out
 
     def forward_joint(self, x: torch.Tensor, B: int, img_h: int, img_w: int, n_txt: int, t_emb: torch.Tensor,
@@ -101,9 +124,15 @@ class DitBlock:
 
     def workspace(self, name: str, shape: Sequence[int]) -> torch.Tensor:
         """Copy of a workspace buffer of the last forward, viewed with ``shape``
-        (H1 is fp32 in both modes, every other buffer is in the storage dtype)."""
+        (H1 and the DQ_* factors are fp32, the *8 e4m3 codes are returned as uint8, every
+        other buffer is in the storage dtype)."""
         ptr, nbytes = krea_dit_block_workspace(self.handle, name)
-        esz = 2 if (self.mode == "bf16" and name != "H1") else 4
+        if name.endswith("8"):
+            esz = 1
+        elif name == "H1" or name.startswith("DQ_") or self.mode == "fp32":
+            esz = 4
+        else:
+            esz = 2
         n = 1
         for s in shape:
             n *= s
@@ -111,7 +140,7 @@ class DitBlock:
             raise ValueError(f"{name}: {n * esz} bytes requested, {nbytes} available")
         if n == 0:
             return torch.empty(tuple(shape), device=self.device, dtype=self.dtype)
-        view = torch.as_tensor(_DevView(ptr, (n,), "<i2" if esz == 2 else "<f4"), device=self.device)
+        view = torch.as_tensor(_DevView(ptr, (n,), {1: "|u1", 2: "<i2", 4: "<f4"}[esz]), device=self.device)
         t = view.clone()
         if esz == 2:
             t = t.view(torch.bfloat16)

@@ -61,6 +61,13 @@ extern "C" {
 /* ---- modes -------------------------------------------------------------------------- */
 #define KREA_DIT_BF16 0
 #define KREA_DIT_FP32 1
+/* 8-bit GEMM modes (Krea 2 Technical Report, "Training" > "Pretraining": the 256px stage
+ * trains with 8-bit matrix multiplications under tensor-wise scaling, the 512px stage
+ * under row-wise scaling). Activations, outputs and the non-GEMM steps are as in
+ * KREA_DIT_BF16; the four GEMMs (fused QKV+gate, attention output, SwiGLU gate/up, down)
+ * take e4m3 operands, see krea_dit_block_forward8. */
+#define KREA_DIT_FP8_TENSOR 2
+#define KREA_DIT_FP8_ROW 3
 
 typedef struct krea_dit_block_s* krea_dit_block_t;
 /* Same object as cudaStream_t / CUstream. NULL means the legacy default stream. */
@@ -76,7 +83,9 @@ typedef struct CUstream_st* krea_dit_stream_t;
  *  eps                 : RMSNorm epsilon (the block uses 1e-6)
  *  rope_base           : RoPE base (10000)
  *  gate_on             : 1 = sigmoid output gate on attention, 0 = off (then w_qkvg has no g rows)
- *  mode                : KREA_DIT_BF16 or KREA_DIT_FP32 */
+ *  mode                : KREA_DIT_BF16, KREA_DIT_FP32, KREA_DIT_FP8_TENSOR or
+ *                        KREA_DIT_FP8_ROW (the 8-bit modes need head_dim 128, like BF16,
+ *                        and d_model <= 3072) */
 typedef struct {
   int max_batch, max_seq;
   int d_model, n_q, n_kv, head_dim, ffn;
@@ -107,6 +116,28 @@ typedef struct {
   const float* k_norm_w;
   const float* mod_bias;
 } krea_dit_weights;
+
+/* 8-bit GEMM weights of one block (modes KREA_DIT_FP8_TENSOR / KREA_DIT_FP8_ROW), all
+ * device memory, caller-owned, filled by krea_dit_weights8_quantize.
+ *  w_qkvg, w_o, w_gate, w_up, w_down : e4m3 codes (one byte each), same shapes and row
+ *          order as the bf16 matrices of krea_dit_weights
+ *  dq_*    fp32 dequantisation factors 2^-k: one per matrix row (FP8_ROW: [rows] floats)
+ *          or one per matrix (FP8_TENSOR: [1] float); matrix row r is codes * dq[r].
+ * Scaling rule: a group (row or matrix) with largest magnitude amax is multiplied by 2^k,
+ * k the largest integer with amax * 2^k <= 448 (k = 0 if amax = 0, k <= 125), then cast
+ * to e4m3 (round to nearest, ties to even, saturating at +-448). */
+typedef struct {
+  void* w_qkvg;
+  void* w_o;
+  void* w_gate;
+  void* w_up;
+  void* w_down;
+  float* dq_qkvg;
+  float* dq_o;
+  float* dq_gate;
+  float* dq_up;
+  float* dq_down;
+} krea_dit_weights8;
 
 /* Shared timestep-MLP weights, fp32 device memory: w1 [d, 256], b1 [d], w2 [6d, d], b2 [6d]. */
 typedef struct {
@@ -165,6 +196,30 @@ int krea_dit_block_forward(krea_dit_block_t h, const void* x_img, const void* x_
 #define KREA_DIT_NOALLOC_SCRATCH_FLOATS 262144
 int krea_dit_timestep_embed_noalloc(const float* t, int B, int d_model, const krea_dit_temb_weights* w,
                                     float* mod_shared, krea_dit_stream_t stream);
+
+/* ---- 8-bit GEMM forward (modes KREA_DIT_FP8_TENSOR, KREA_DIT_FP8_ROW) ----------------- */
+
+/* Cast the bf16 GEMM weights of w (w_qkvg, w_o, w_gate, w_up, w_down) to e4m3 codes with
+ * the handle's scaling (per row, or one scale per matrix) into the caller's buffers of q.
+ * Enqueued on `stream`; the other fields of w are not read. Errors: INVALID_ARG for a
+ * NULL pointer or a handle not in an 8-bit mode, MISALIGNED for an unaligned pointer. */
+int krea_dit_weights8_quantize(krea_dit_block_t h, const krea_dit_weights* w, const krea_dit_weights8* q,
+                               krea_dit_stream_t stream);
+
+/* krea_dit_block_forward with 8-bit GEMM operands. Each of the four GEMMs casts its
+ * activation operand (the bf16 value the BF16 mode stores there: xn, o_g, hn, hmid) to
+ * e4m3 with the handle's scaling (FP8_ROW: one scale per token row; FP8_TENSOR: one
+ * scale for the whole [B L, K] activation of the call) and multiplies it by the e4m3
+ * weight codes of q; each product is dequantised by its row and column factors and
+ * accumulated in fp32. x_img, x_txt, t_emb, out and every other argument are as in
+ * krea_dit_block_forward; from w only norm1_w, norm2_w, q_norm_w, k_norm_w and mod_bias
+ * are read (its matrix pointers may be NULL). Errors as krea_dit_block_forward, plus
+ * INVALID_ARG when the handle is not in an 8-bit mode or q has a NULL pointer. A handle
+ * in an 8-bit mode rejects krea_dit_block_forward and the joint / stack calls
+ * (INVALID_ARG). */
+int krea_dit_block_forward8(krea_dit_block_t h, const void* x_img, const void* x_txt, int B, int img_h, int img_w,
+                            int n_txt, const float* t_emb, const krea_dit_weights* w, const krea_dit_weights8* q,
+                            void* out, krea_dit_stream_t stream);
 
 /* ---- joint-layout forward and stacks of blocks ------------------------------------ */
 
@@ -256,6 +311,16 @@ int krea_dit_block_host_sync(krea_dit_block_t h);
 #define KREA_DIT_BUF_H1 6
 #define KREA_DIT_BUF_HN 7
 #define KREA_DIT_BUF_HMID 8
+/* 8-bit modes: the e4m3 GEMM operands (codes) and their dequantisation factors (fp32,
+ * [T] row-wise or [1] tensor-wise) of the last forward */
+#define KREA_DIT_BUF_XN8 9
+#define KREA_DIT_BUF_OG8 10
+#define KREA_DIT_BUF_HN8 11
+#define KREA_DIT_BUF_HMID8 12
+#define KREA_DIT_BUF_DQ_XN 13
+#define KREA_DIT_BUF_DQ_OG 14
+#define KREA_DIT_BUF_DQ_HN 15
+#define KREA_DIT_BUF_DQ_HMID 16
 int krea_dit_block_workspace(krea_dit_block_t h, int which, void** dev_ptr, size_t* bytes);
 
 /* Per-kernel timing. When enabled, each forward records a CUDA event before and after
