@@ -11,33 +11,35 @@
 //   * SWIGLU: silu(hn W_gate^T) * (hn W_up^T), both products in one 128x256 accumulator
 //             ("Transformer block": SwiGLU MLP)
 //
-// Tile 128 x 256 x 64 (bf16) or 128 x 256 x 128 (e4m3): either way 128-byte operand rows,
-// A tile 16 KB + B tile 32 KB per stage, 4 stages in shared memory, written by TMA with the
-// 128-byte swizzle; one stage is four MMAs of 32 bytes of K (kind::f16, K = 16, or
-// kind::f8f6f4, K = 32). The 8-bit GEMMs ("训练 › 预训练" / Training › Pretraining: 8-bit
+// CTAs run in clusters of two; the pair computes one 256 x 256 output tile (m-blocks 2p and
+// 2p + 1 of one N-block) with pair MMAs (tcgen05 cta_group::2, M = 256, N = 256): each CTA
+// holds its 128 rows of A and one 128-row half of the B tile, and receives its 128 rows of
+// the accumulator in its own tensor memory. A k-step is 128-byte operand rows (64 bf16 or
+// 128 e4m3 of K): 16 KB of A + 16 KB of B per CTA per stage, 6 stages in shared memory
+// written by TMA with the 128-byte swizzle; one stage is four MMAs of 32 bytes of K
+// (kind::f16, K = 16, or kind::f8f6f4, K = 32), issued by one thread of the even CTA. The 8-bit GEMMs ("训练 › 预训练" / Training › Pretraining: 8-bit
 // training with tensor-wise or row-wise scaling) multiply e4m3 codes and dequantise each
 // accumulator by the power-of-two factors of its row and column in the epilogue. The accumulator is double-buffered in TMEM
 // (2 x 256 columns), so the epilogue of one tile overlaps the main loop of the next.
 // Warp roles: warp 0 = TMA producer (one thread), warp 1 = TMEM allocator + MMA issuer
 // (one thread), warps 2..9 = epilogue (two warpgroups, one per 128-column half).
 //
-// CTAs run in clusters of two that work on vertically adjacent tiles (m-blocks 2p and
-// 2p + 1) of the same N-block: each CTA loads its own A tile and one 128-row half of the
-// shared B tile, multicast into both CTAs' shared memory. Per CTA and k-block that is
-// 32 KB fetched instead of 48 KB, so the 4-stage ring covers a third more L2 latency (the
-// single-CTA version's MMA thread waited for data a third of the time). A stage is freed
-// when both CTAs' MMAs have read it: each MMA commit arrives on the stage's "empty"
-// barrier in both CTAs.
+// Both CTAs' TMA loads of a stage complete on the even CTA's "full" barrier (one expected
+// byte count for the pair), the MMA commit frees the stage in both CTAs, each accumulator
+// is announced to both CTAs' epilogues, and both CTAs' epilogue warps release it on the
+// even CTA's barrier. Against one CTA per tile (the pair sharing B by multicast), a stage
+// takes 32 KB of shared memory instead of 48 KB, so six stages fit instead of four and
+// cover half as much again of the L2 latency.
 #include "common.cuh"
 #include "internal.h"
 
 namespace kd {
 namespace {
 
-constexpr int BM = 128, BN = 256, BK_BYTES = 128, STAGES = 4;
-constexpr int A_BYTES = BM * BK_BYTES;
-constexpr int B_BYTES = BN * BK_BYTES;
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int BM = 128, BN = 256, BK_BYTES = 128, STAGES = 6;
+constexpr int A_BYTES = BM * BK_BYTES;             // this CTA's 128 rows of A
+constexpr int BH_BYTES = (BN / 2) * BK_BYTES;      // this CTA's 128-row half of the B tile
+constexpr int STAGE_BYTES = A_BYTES + BH_BYTES;
 constexpr int TMEM_COLS = 2 * BN;
 constexpr int NUM_EPI_WARPS = 8;
 constexpr int NUM_THREADS = 64 + NUM_EPI_WARPS * 32;
@@ -354,25 +356,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 2);  // this CTA's and the peer's MMAs both read the stage
+      mbar_init(&full[s], 1);   // even CTA: its producer's arrive + both CTAs' bytes
+      mbar_init(&empty[s], 1);  // the pair MMA's commit
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], NUM_EPI_WARPS);
+      mbar_init(&tempty[a], 2 * NUM_EPI_WARPS);  // even CTA: both CTAs' epilogue warps
     }
     mbar_init(done, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, TMEM_COLS);
-    tmem_relinquish();
+    tmem_alloc_pair(tmem_slot, TMEM_COLS);
+    tmem_relinquish_pair();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  cluster_sync();  // the peer's barriers are initialised before any multicast reaches them
+  cluster_sync();  // both CTAs' barriers are initialised before the peer signals any of them
   const uint32_t tmem_base = *tmem_slot;
   const WaitCtx wc{abort_flag, err};
 
@@ -389,6 +391,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       // B half of this CTA: rows [128 rank, 128 rank + 128) of the 256-row B tile (for the
       // SwiGLU GEMM: W_gate rows for rank 0, W_up rows for rank 1)
       const CUtensorMap* map_b = (DUAL && rank == 1) ? &tm_b2 : &tm_b;
+      const uint32_t full0 = mapa_shared(smem_u32(full), 0);  // the even CTA's full barriers
       for (int tile = pair; ok && tile < num_tiles; tile += npairs) {
         int mp, nb;
         tile_coords(tile, num_mp, num_n, mp, nb);
@@ -401,10 +404,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
           uint8_t* sa = smem + stage * STAGE_BYTES;
           uint8_t* sb = sa + A_BYTES;
-          // own A (16 KB) + own B half (16 KB) + the peer's B half (16 KB, multicast)
-          mbar_arrive_expect_tx(&full[stage], STAGE_BYTES);
-          tma_load_2d(sa, &tm_a, &full[stage], kb * BK, mb * BM);
-          tma_load_2d_mc(sb + rank * (B_BYTES / 2), map_b, &full[stage], kb * BK, yb, 0x3);
+          // own A (16 KB) + own B half (16 KB), completing on the even CTA's barrier, which
+          // expects both CTAs' bytes
+          if (rank == 0) mbar_arrive_expect_tx(&full[stage], 2 * STAGE_BYTES);
+          const uint32_t fb = full0 + static_cast<uint32_t>(stage * sizeof(uint64_t));
+          tma_load_2d_pair(sa, &tm_a, fb, kb * BK, mb * BM);
+          tma_load_2d_pair(sb, map_b, fb, kb * BK, yb);
           ++issued;
           if (++stage == STAGES) {
             stage = 0;
@@ -412,14 +417,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
         }
       }
-      // every copy this thread started has landed before the CTA exits
+      // every copy this thread started has landed before the CTA exits: on the even CTA
+      // its full barriers count both CTAs' bytes; the odd CTA sees its stages freed by the
+      // MMA, which reads them only after they landed
       for (long long i = (issued > STAGES ? issued - STAGES : 0); i < issued; ++i)
-        drain_wait(&full[i % STAGES], static_cast<uint32_t>((i / STAGES) & 1), err, SITE_GEMM_TEARDOWN);
+        drain_wait(rank == 0 ? &full[i % STAGES] : &empty[i % STAGES], static_cast<uint32_t>((i / STAGES) & 1),
+                   err, SITE_GEMM_TEARDOWN);
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      // ---------------- MMA issuer
-      constexpr uint32_t idesc = FP8 ? idesc_e4m3_f32(BM, BN) : idesc_bf16_f32(BM, BN);
+    if (lane == 0 && rank == 0) {
+      // ---------------- MMA issuer (even CTA): pair MMAs, M = 256 across the two CTAs
+      constexpr uint32_t idesc = FP8 ? idesc_e4m3_f32(2 * BM, BN) : idesc_bf16_f32(2 * BM, BN);
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
@@ -440,26 +448,26 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
           for (int k = 0; k < 4; ++k) {  // 32 bytes of K per MMA
             if constexpr (FP8)
-              mma_e4m3_ss(d_tmem, sdesc_kmajor_sw128(sa + k * 32), sdesc_kmajor_sw128(sb + k * 32), idesc,
-                          (kb | k) != 0 ? 1u : 0u);
+              mma_e4m3_ss_pair(d_tmem, sdesc_kmajor_sw128(sa + k * 32), sdesc_kmajor_sw128(sb + k * 32), idesc,
+                               (kb | k) != 0 ? 1u : 0u);
             else
-              mma_bf16_ss(d_tmem, sdesc_kmajor_sw128(sa + k * 32), sdesc_kmajor_sw128(sb + k * 32), idesc,
-                          (kb | k) != 0 ? 1u : 0u);
+              mma_bf16_ss_pair(d_tmem, sdesc_kmajor_sw128(sa + k * 32), sdesc_kmajor_sw128(sb + k * 32), idesc,
+                               (kb | k) != 0 ? 1u : 0u);
           }
-          mma_commit_mc(&empty[stage], 0x3);  // frees the stage (in both CTAs) once these MMAs read it
+          mma_commit_pair_mc(&empty[stage], 0x3);  // frees the stage in both CTAs once these MMAs read it
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1;
           }
         }
         if (!ok) break;
-        mma_commit(&tfull[acc]);  // accumulator ready for the epilogue
+        mma_commit_pair_mc(&tfull[acc], 0x3);  // accumulator ready for both CTAs' epilogues
         if (++acc == 2) {
           acc = 0;
           acc_phase ^= 1;
         }
       }
-      mma_commit(done);  // completes when every MMA issued above has finished
+      mma_commit_pair_mc(done, 0x1);  // completes when every MMA issued above has finished
       drain_wait(done, 0, err, SITE_GEMM_TEARDOWN);
     }
   } else {
@@ -468,6 +476,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int half = (warp - 2) / 4;           // 128-column half of the accumulator
     int acc = 0;
     uint32_t acc_phase = 0;
+    const uint32_t tempty0 = mapa_shared(smem_u32(tempty), 0);  // the even CTA's tempty barriers
     for (int tile = pair; tile < num_tiles; tile += npairs) {
       int mp, nb;
       tile_coords(tile, num_mp, num_n, mp, nb);
@@ -480,7 +489,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       epi.apply(row, nb, half, taddr, M);
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&tempty[acc]);
+      if (lane == 0) mbar_arrive_cluster(tempty0 + static_cast<uint32_t>(acc * sizeof(uint64_t)));
       if (++acc == 2) {
         acc = 0;
         acc_phase ^= 1;
@@ -488,11 +497,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
   }
   __syncthreads();
-  cluster_sync();  // no CTA leaves while the peer may still multicast into it or commit to it
+  cluster_sync();  // no CTA leaves while the pair's MMAs, copies or arrivals may still reach it
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
-    tmem_dealloc(tmem_base, TMEM_COLS);
+    tmem_dealloc_pair(tmem_base, TMEM_COLS);
   }
 }
 
