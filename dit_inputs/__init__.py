@@ -97,6 +97,9 @@ CONFIGS["small_b"] = _cfg("small_b", 1, 16, 20, 37, 384, 4, 1, 128, 1088, "bf16"
 CONFIGS["small_c"] = _cfg("small_c", 3, 12, 16, 64, 768, 6, 6, 128, 2048, "bf16", 12)
 CONFIGS["small_imgonly"] = _cfg("small_imgonly", 2, 10, 13, 0, 512, 4, 2, 128, 1408, "bf16", 13)
 CONFIGS["small_txtonly"] = _cfg("small_txtonly", 2, 0, 0, 45, 512, 4, 2, 128, 1408, "bf16", 14)
+# Odd number of query tiles per KV group (G = 3, 3 tiles): one-tile attention units, and
+# 160 units (more than one per SM), so a persistent CTA meets both kinds in one sequence.
+CONFIGS["units_odd"] = _cfg("units_odd", 32, 16, 16, 44, 384, 3, 1, 128, 1024, "bf16", 17)
 CONFIGS["tiny_ragged32"] = _cfg("tiny_ragged32", 2, 5, 7, 9, 192, 3, 1, 64, 320, "fp32", 15)
 CONFIGS["small_fp32_hd128"] = _cfg("small_fp32_hd128", 1, 9, 11, 13, 256, 2, 1, 128, 704, "fp32", 16)
 
