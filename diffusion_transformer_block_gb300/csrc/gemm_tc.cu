@@ -36,7 +36,10 @@
 namespace kd {
 namespace {
 
-constexpr int BM = 128, BN = 256, BK_BYTES = 128, STAGES = 6;
+#ifndef KD_GEMM_STAGES
+#define KD_GEMM_STAGES 6
+#endif
+constexpr int BM = 128, BN = 256, BK_BYTES = 128, STAGES = KD_GEMM_STAGES;
 constexpr int A_BYTES = BM * BK_BYTES;             // this CTA's 128 rows of A
 constexpr int BH_BYTES = (BN / 2) * BK_BYTES;      // this CTA's 128-row half of the B tile
 constexpr int STAGE_BYTES = A_BYTES + BH_BYTES;

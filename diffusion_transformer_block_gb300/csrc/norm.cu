@@ -85,9 +85,27 @@ __global__ void __launch_bounds__(NM_WARPS * 32, 1) norm_modulate_kernel(
     const float* sh_s = mod_shared + (static_cast<size_t>(b) * 6 + chunk_shift) * d;
     const float* sc_b = mod_bias + static_cast<size_t>(chunk_scale) * d;
     const float* sh_b = mod_bias + static_cast<size_t>(chunk_shift) * d;
-    for (int c = threadIdx.x; c < d; c += blockDim.x) {
-      A[c] = (1.0f + gain_w[c]) * (1.0f + (sc_s[c] + sc_b[c]));
-      S[c] = sh_s[c] + sh_b[c];
+    // four columns per thread per pass, so that their twenty loads are in flight together
+    for (int c0 = threadIdx.x; c0 < d; c0 += 4 * blockDim.x) {
+      float g[4], ss_[4], sb_[4], hs[4], hb[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int c = c0 + k * blockDim.x;
+        const bool in = c < d;
+        g[k] = in ? gain_w[c] : 0.f;
+        ss_[k] = in ? sc_s[c] : 0.f;
+        sb_[k] = in ? sc_b[c] : 0.f;
+        hs[k] = in ? sh_s[c] : 0.f;
+        hb[k] = in ? sh_b[c] : 0.f;
+      }
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int c = c0 + k * blockDim.x;
+        if (c < d) {
+          A[c] = (1.0f + g[k]) * (1.0f + (ss_[k] + sb_[k]));
+          S[c] = hs[k] + hb[k];
+        }
+      }
     }
   };
   if (threadIdx.x == 0) {
@@ -129,21 +147,21 @@ __global__ void __launch_bounds__(NM_WARPS * 32, 1) norm_modulate_kernel(
     const int b = m / f.L;
     const Tin* x = row_src_ptr<Tin>(src, m, f.L, f.n_txt, f.n_img, d);
     Raw8<Tin> raw[NV];
-    float ss = 0.f;
 #pragma unroll
     for (int c = 0; c < NV; ++c) {
       const int col = (lane + 32 * c) * 8;
       if (col < d) raw[c].load(x + col);
       else raw[c].zero();
     }
+    float ss4[4] = {0.f, 0.f, 0.f, 0.f};  // independent chains
 #pragma unroll
     for (int c = 0; c < NV; ++c) {
       float v[8];
       raw[c].get(v);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) ss = fmaf(v[i], v[i], ss);
+      for (int i = 0; i < 8; ++i) ss4[i & 3] = fmaf(v[i], v[i], ss4[i & 3]);
     }
-    ss = warp_sum(ss);
+    const float ss = warp_sum((ss4[0] + ss4[1]) + (ss4[2] + ss4[3]));
     const float rstd = 1.0f / sqrtf(ss / static_cast<float>(d) + f.eps);
     const bool in_sets = b == set_b[0] || b == set_b[1];  // false only when L < 8 (a group spans 3+ batch elements)
     const float* A = nm_smem + (b == set_b[0] ? 0 : 2 * d);
