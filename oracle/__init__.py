@@ -5,7 +5,8 @@ and by the benchmark's CPU-baseline leg, never by the library. It shares no code
 with the CUDA path. Parity pins: every function here is pinned by the CPU tests
 (textbook library routines, closed forms, invariants, brute force on tiny
 inputs); none is "parity unpinned". ``oracle.gemm8`` adds the block with 8-bit
-(e4m3, scaled) GEMM operands, pinned in ``tests/test_oracle_gemm8.py``.
+(e4m3, scaled) GEMM operands, pinned in ``tests/test_oracle_gemm8.py``; ``oracle.backward``
+the analytic gradients of the block, pinned in ``tests/test_oracle_backward.py``.
 """
 from __future__ import annotations
 
