@@ -42,6 +42,7 @@ EXPORTS = [
     "krea_dit_block_enable_host_io", "krea_dit_block_forward_host", "krea_dit_block_host_sync",
     "krea_dit_block_forward_joint", "krea_dit_stack_forward", "krea_dit_stack_graph_create", "krea_dit_graph_launch",
     "krea_dit_graph_destroy", "krea_dit_weights8_quantize", "krea_dit_block_forward8",
+    "krea_dit_block_enable_backward", "krea_dit_block_backward",
 ]
 
 
@@ -66,6 +67,12 @@ class krea_dit_weights(ctypes.Structure):
 class krea_dit_weights8(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in (
         "w_qkvg", "w_o", "w_gate", "w_up", "w_down", "dq_qkvg", "dq_o", "dq_gate", "dq_up", "dq_down")]
+
+
+class krea_dit_grads(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in (
+        "d_x_txt", "d_x_img", "d_w_qkvg", "d_w_o", "d_w_gate", "d_w_up", "d_w_down", "d_norm1_w", "d_norm2_w",
+        "d_q_norm_w", "d_k_norm_w", "d_mod_bias", "d_mod_shared")]
 
 
 class krea_dit_temb_weights(ctypes.Structure):
@@ -109,6 +116,9 @@ def lib() -> ctypes.CDLL:
         L.krea_dit_graph_destroy.argtypes = [vp]
         L.krea_dit_weights8_quantize.argtypes = [vp, ctypes.POINTER(krea_dit_weights), ctypes.POINTER(krea_dit_weights8),
                                                  vp]
+        L.krea_dit_block_enable_backward.argtypes = [vp]
+        L.krea_dit_block_backward.argtypes = [vp, vp, vp, ci, ci, ci, ci, vp, ctypes.POINTER(krea_dit_weights), vp,
+                                              ctypes.POINTER(krea_dit_grads), vp]
         L.krea_dit_block_forward8.argtypes = [vp, vp, vp, ci, ci, ci, ci, vp, ctypes.POINTER(krea_dit_weights),
                                               ctypes.POINTER(krea_dit_weights8), vp, vp]
         for name in EXPORTS:
@@ -182,6 +192,23 @@ def krea_dit_block_forward8(handle: int, x_img, x_txt, B: int, img_h: int, img_w
     _check(lib().krea_dit_block_forward8(handle, _ptr(x_img), _ptr(x_txt), B, img_h, img_w, n_txt, _ptr(t_emb),
                                          ctypes.byref(w), ctypes.byref(q), _ptr(out), _stream(stream)),
            "krea_dit_block_forward8")
+
+
+def krea_dit_block_enable_backward(handle: int) -> None:
+    _check(lib().krea_dit_block_enable_backward(handle), "krea_dit_block_enable_backward")
+
+
+def krea_dit_block_backward(handle: int, x_img, x_txt, B: int, img_h: int, img_w: int, n_txt: int, t_emb,
+                            w: krea_dit_weights, d_out, g: krea_dit_grads, stream=None) -> None:
+    _check(lib().krea_dit_block_backward(handle, _ptr(x_img), _ptr(x_txt), B, img_h, img_w, n_txt, _ptr(t_emb),
+                                         ctypes.byref(w), _ptr(d_out), ctypes.byref(g), _stream(stream)),
+           "krea_dit_block_backward")
+
+
+def make_grads(t: Dict[str, object]) -> krea_dit_grads:
+    """Gradient struct from a dict of device tensors keyed by the struct's field names
+    (a missing key is passed as NULL)."""
+    return krea_dit_grads(*[_ptr(t.get(n)) for n, _ in krea_dit_grads._fields_])
 
 
 def krea_dit_block_enable_host_io(handle: int) -> None:

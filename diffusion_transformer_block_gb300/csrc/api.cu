@@ -46,6 +46,10 @@ enum Slot {
   S_QUANT_HMID,
   S_W8_AMAX,
   S_W8_QUANT,
+  S_BWD_GEMM,
+  S_BWD_TRANSPOSE,
+  S_BWD_POINTWISE,
+  S_BWD_SOFTMAX,
   S_COUNT
 };
 const char* const kSlotNames[S_COUNT] = {
@@ -55,7 +59,8 @@ const char* const kSlotNames[S_COUNT] = {
     "up_gemm_f32",          "swiglu_f32",            "down_gemm_f32",   "residual_mlp_f32",
     "temb_sinusoid",        "temb_mlp1",             "temb_mlp2",       "norm1_amax",
     "quant_og_e4m3",        "norm2_amax",            "quant_hmid_e4m3", "weights8_row_amax",
-    "weights8_quant_e4m3"};
+    "weights8_quant_e4m3",  "bwd_gemm",              "bwd_transpose",   "bwd_pointwise",
+    "bwd_attn_softmax"};
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
@@ -151,6 +156,18 @@ struct krea_dit_block_s {
   void *xn8 = nullptr, *og8 = nullptr, *hn8 = nullptr, *hmid8 = nullptr;
   float *dq_xn = nullptr, *dq_og = nullptr, *dq_hn = nullptr, *dq_hmid = nullptr;
   float *am_xn = nullptr, *am_og = nullptr, *am_hn = nullptr, *am_hmid = nullptr, *am_w = nullptr;
+  // backward workspace (krea_dit_block_enable_backward): one allocation, carved below
+  char* bw = nullptr;
+  size_t bw_Tp = 0, bw_Lp = 0;
+  void *bw_out = nullptr, *wT_down = nullptr, *wT_gu = nullptr, *wT_o = nullptr, *wT_qkvg = nullptr;
+  float *f_td = nullptr, *f_hmid = nullptr, *f_a = nullptr, *f_u = nullptr, *f_dn = nullptr, *f_dh1 = nullptr,
+        *f_dog = nullptr, *f_o = nullptr, *f_raw = nullptr, *f_dq = nullptr, *f_dk = nullptr, *f_dv = nullptr,
+        *f_S = nullptr, *f_rstd = nullptr;
+  void *b_dfm = nullptr, *b_dau = nullptr, *b_dfa = nullptr, *b_do = nullptr, *b_dP = nullptr, *b_P = nullptr,
+       *b_dS = nullptr, *b_PT = nullptr, *b_dST = nullptr, *b_vrow = nullptr, *b_kT = nullptr, *b_qT = nullptr,
+       *b_doT = nullptr;
+  void *t_dfm = nullptr, *t_hmid = nullptr, *t_dau = nullptr, *t_hn = nullptr, *t_dfa = nullptr, *t_og = nullptr,
+       *t_dP = nullptr, *t_xn = nullptr;
   float2* rope = nullptr;
   int* err = nullptr;
   Fwd last{};
@@ -395,6 +412,7 @@ int krea_dit_block_destroy(krea_dit_block_t h) {
     cudaStreamDestroy(h->down);
     cudaFree(h->stage);
   }
+  if (h->bw) cudaFree(h->bw);
   cudaError_t r = cudaFree(h->ws);
   delete h;
   return r == cudaSuccess ? KREA_DIT_OK : KREA_DIT_ERR_CUDA;
@@ -730,6 +748,245 @@ int krea_dit_graph_destroy(krea_dit_graph_t g) {
   cudaGraphDestroy(g->graph);
   delete g;
   return KREA_DIT_OK;
+}
+
+int krea_dit_block_enable_backward(krea_dit_block_t h) {
+  if (!h) return KREA_DIT_ERR_INVALID_ARG;
+  if (!h->bf16 || h->mode8) return KREA_DIT_ERR_INVALID_ARG;  // bf16 mode only
+  if (h->bw) return KREA_DIT_OK;
+  const krea_dit_config& c = h->cfg;
+  const size_t T = h->max_T, d = c.d_model, F = c.ffn, hd = c.head_dim;
+  const size_t nq = static_cast<size_t>(c.n_q) * hd, nkv = static_cast<size_t>(c.n_kv) * hd, nqkvg = h->n_qkvg;
+  const size_t Tp = round_up(T, 64), Lp = round_up(static_cast<size_t>(c.max_seq), 64);
+  struct Item {
+    void** p;
+    size_t bytes;
+  };
+  std::vector<Item> items = {
+      {&h->bw_out, T * d * 2},
+      {&h->wT_down, F * d * 2},
+      {&h->wT_gu, d * 2 * F * 2},
+      {&h->wT_o, nq * d * 2},
+      {&h->wT_qkvg, d * nqkvg * 2},
+      {reinterpret_cast<void**>(&h->f_td), T * d * 4},
+      {reinterpret_cast<void**>(&h->f_hmid), T * F * 4},
+      {reinterpret_cast<void**>(&h->f_a), T * F * 4},
+      {reinterpret_cast<void**>(&h->f_u), T * F * 4},
+      {reinterpret_cast<void**>(&h->f_dn), T * d * 4},
+      {reinterpret_cast<void**>(&h->f_dh1), T * d * 4},
+      {reinterpret_cast<void**>(&h->f_dog), T * nq * 4},
+      {reinterpret_cast<void**>(&h->f_o), T * nq * 4},
+      {reinterpret_cast<void**>(&h->f_raw), T * nqkvg * 4},
+      {reinterpret_cast<void**>(&h->f_dq), T * nq * 4},
+      {reinterpret_cast<void**>(&h->f_dk), T * nkv * 4},
+      {reinterpret_cast<void**>(&h->f_dv), T * nkv * 4},
+      {reinterpret_cast<void**>(&h->f_S), Lp * Lp * 4},
+      {reinterpret_cast<void**>(&h->f_rstd), T * 4},
+      {&h->b_dfm, T * d * 2},
+      {&h->b_dau, T * 2 * F * 2},
+      {&h->b_dfa, T * d * 2},
+      {&h->b_do, T * nq * 2},
+      {&h->b_dP, T * nqkvg * 2},
+      {&h->b_P, Lp * Lp * 2},
+      {&h->b_dS, Lp * Lp * 2},
+      {&h->b_PT, Lp * Lp * 2},
+      {&h->b_dST, Lp * Lp * 2},
+      {&h->b_vrow, static_cast<size_t>(c.max_batch) * c.n_kv * Lp * hd * 2},
+      {&h->b_kT, static_cast<size_t>(c.max_batch) * c.n_kv * hd * Lp * 2},
+      {&h->b_qT, hd * Lp * 2},
+      {&h->b_doT, hd * Lp * 2},
+      {&h->t_dfm, d * Tp * 2},
+      {&h->t_hmid, F * Tp * 2},
+      {&h->t_dau, 2 * F * Tp * 2},
+      {&h->t_hn, d * Tp * 2},
+      {&h->t_dfa, d * Tp * 2},
+      {&h->t_og, nq * Tp * 2},
+      {&h->t_dP, nqkvg * Tp * 2},
+      {&h->t_xn, d * Tp * 2},
+  };
+  size_t total = 0;
+  for (auto& it : items) total += round_up(it.bytes, 256);
+  char* base = nullptr;
+  if (cudaMalloc(&base, total) != cudaSuccess) return KREA_DIT_ERR_CUDA;
+  if (cudaMemset(base, 0, total) != cudaSuccess) {
+    cudaFree(base);
+    return KREA_DIT_ERR_CUDA;
+  }
+  size_t off = 0;
+  for (auto& it : items) {
+    *it.p = base + off;
+    off += round_up(it.bytes, 256);
+  }
+  h->bw = base;
+  h->bw_Tp = Tp;
+  h->bw_Lp = Lp;
+  return KREA_DIT_OK;
+}
+
+int krea_dit_block_backward(krea_dit_block_t h, const void* x_img, const void* x_txt, int B, int img_h, int img_w,
+                            int n_txt, const float* t_emb, const krea_dit_weights* w, const void* d_out,
+                            const krea_dit_grads* g, krea_dit_stream_t stream) {
+  if (!h || !w || !g || !d_out || !t_emb) return KREA_DIT_ERR_INVALID_ARG;
+  if (!h->bw) return KREA_DIT_ERR_INVALID_ARG;  // krea_dit_block_enable_backward first
+  const float* gp[] = {g->d_w_qkvg, g->d_w_o, g->d_w_gate, g->d_w_up, g->d_w_down, g->d_norm1_w, g->d_norm2_w,
+                       g->d_q_norm_w, g->d_k_norm_w, g->d_mod_bias, g->d_mod_shared};
+  for (const float* p : gp) {
+    if (!p) return KREA_DIT_ERR_INVALID_ARG;
+    if (!aligned16(p)) return KREA_DIT_ERR_MISALIGNED;
+  }
+  const int n_img = img_h * img_w;
+  if ((n_img > 0 && !g->d_x_img) || (n_txt > 0 && !g->d_x_txt)) return KREA_DIT_ERR_INVALID_ARG;
+  if (!aligned16(d_out) || (g->d_x_img && !aligned16(g->d_x_img)) || (g->d_x_txt && !aligned16(g->d_x_txt)))
+    return KREA_DIT_ERR_MISALIGNED;
+  // the forward, recomputed: fills the workspace (xn, Q, K, V^T, G, O_g, h1, hn, hmid)
+  int r = forward_impl(h, x_img, x_txt, nullptr, B, img_h, img_w, n_txt, t_emb, w, nullptr, h->bw_out, stream);
+  if (r != KREA_DIT_OK) return r;
+  const Fwd f = h->last;
+  if (f.T == 0) return KREA_DIT_OK;
+  const krea_dit_config& c = h->cfg;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const int sms = h->num_sms;
+  const int T = f.T, d = c.d_model, F = c.ffn, hd = c.head_dim, L = f.L;
+  const int nq = c.n_q * hd, nkv = c.n_kv * hd, nqkvg = h->n_qkvg, G = c.n_q / c.n_kv;
+  const int Tp = static_cast<int>(round_up(static_cast<size_t>(T), 64));
+  const int Lp = static_cast<int>(round_up(static_cast<size_t>(L), 64));
+  const float scale = 1.0f / sqrtf(static_cast<float>(hd));
+  float* d_mod = g->d_mod_shared;
+  float* d_bias = g->d_mod_bias;
+  cudaError_t e = cudaSuccess;
+  auto run = [&](int slot, auto&& fn) {
+    if (e == cudaSuccess) e = timed(h, slot, st, fn);
+  };
+  // C[M,N] (+)= alpha * A[M,K] B[N,K]^T, A / B bf16 row-major with pitches (elements)
+  auto gemm = [&](const void* A, int a_rows, long long a_pitch, const void* Bm, int b_rows, long long b_pitch, int K,
+                  float* C, long long ldc, int M, int N, float alpha, int acc) {
+    run(S_BWD_GEMM, [&]() -> cudaError_t {
+      CUtensorMap ta, tb;
+      if (!encode_2d(&ta, A, K, a_rows, a_pitch, 64, 128) || !encode_2d(&tb, Bm, K, b_rows, b_pitch, 64, 128))
+        return cudaErrorInvalidValue;
+      return kd::launch_gemm_plain(&ta, &tb, M, N, K, C, ldc, alpha, acc, sms, h->err, st);
+    });
+  };
+  auto transpose = [&](const void* src, int R, int C, long long lds, long long sbs, void* dst, int Rp, long long ldd,
+                       long long dbs, int batch) {
+    run(S_BWD_TRANSPOSE, [&] { return kd::launch_transpose_bf16(src, R, C, lds, sbs, dst, Rp, ldd, dbs, batch, st); });
+  };
+  // element offsets into bf16 buffers (2 bytes per element)
+  auto bf = [](const void* p, long long off) { return static_cast<const void*>(static_cast<const char*>(p) + 2 * off); };
+  auto bfw = [](void* p, long long off) { return static_cast<void*>(static_cast<char*>(p) + 2 * off); };
+
+  // accumulators
+  if (e == cudaSuccess) e = cudaMemsetAsync(d_mod, 0, static_cast<size_t>(B) * 6 * d * 4, st);
+  if (e == cudaSuccess) e = cudaMemsetAsync(d_bias, 0, static_cast<size_t>(6) * d * 4, st);
+  if (e == cudaSuccess) e = cudaMemsetAsync(g->d_norm1_w, 0, static_cast<size_t>(d) * 4, st);
+  if (e == cudaSuccess) e = cudaMemsetAsync(g->d_norm2_w, 0, static_cast<size_t>(d) * 4, st);
+  if (e == cudaSuccess) e = cudaMemsetAsync(g->d_q_norm_w, 0, static_cast<size_t>(hd) * 4, st);
+  if (e == cudaSuccess) e = cudaMemsetAsync(g->d_k_norm_w, 0, static_cast<size_t>(hd) * 4, st);
+  if (e == cudaSuccess) e = cudaMemsetAsync(h->f_dk, 0, static_cast<size_t>(T) * nkv * 4, st);
+  if (e == cudaSuccess) e = cudaMemsetAsync(h->f_dv, 0, static_cast<size_t>(T) * nkv * 4, st);
+  // weights as K-major operands of the data-gradient products
+  transpose(w->w_down, d, F, F, 0, h->wT_down, d, d, 0, 1);                    // [F, d]
+  transpose(w->w_gate, F, d, d, 0, h->wT_gu, F, 2LL * F, 0, 1);                // [d, 0:F]
+  transpose(w->w_up, F, d, d, 0, bfw(h->wT_gu, F), F, 2LL * F, 0, 1);          // [d, F:2F]
+  transpose(w->w_o, d, nq, nq, 0, h->wT_o, d, d, 0, 1);                        // [nq, d]
+  transpose(w->w_qkvg, nqkvg, d, d, 0, h->wT_qkvg, nqkvg, nqkvg, 0, 1);        // [d, nqkvg]
+
+  // ---- MLP residual: out = h1 + gate_m * fm,  fm = hmid W_down^T
+  gemm(h->hmid, T, F, w->w_down, d, F, F, h->f_td, d, T, d, 1.0f, 0);
+  run(S_BWD_POINTWISE, [&] {
+    return kd::launch_gated_bwd(f, d_out, 0, h->f_td, t_emb, w->mod_bias, 5, h->b_dfm, d_mod, d_bias, st);
+  });
+  gemm(h->b_dfm, T, d, h->wT_down, F, d, d, h->f_hmid, F, T, F, 1.0f, 0);      // d_hmid
+  // ---- SwiGLU (pre-activations recomputed)
+  gemm(h->hn, T, d, w->w_gate, F, d, d, h->f_a, F, T, F, 1.0f, 0);
+  gemm(h->hn, T, d, w->w_up, F, d, d, h->f_u, F, T, F, 1.0f, 0);
+  run(S_BWD_POINTWISE, [&] { return kd::launch_swiglu_bwd(h->f_hmid, h->f_a, h->f_u, T, F, h->b_dau, sms, st); });
+  gemm(h->b_dau, T, 2LL * F, h->wT_gu, d, 2LL * F, 2 * F, h->f_dn, d, T, d, 1.0f, 0);  // d_hn
+  // ---- norm2 + modulation; the residual adds d_out
+  const RowSrc h1src{nullptr, nullptr, h->h1};
+  run(S_BWD_POINTWISE, [&] {
+    return kd::launch_norm_bwd(f, h1src, 1, h->f_dn, w->norm2_w, t_emb, w->mod_bias, 3, 4, d_out, 0, h->f_dh1,
+                               RowSrc{}, h->f_rstd, d_mod, d_bias, g->d_norm2_w, st);
+  });
+  // ---- attention residual: h1 = x + gate_a * fa,  fa = og W_o^T
+  gemm(h->og, T, nq, w->w_o, d, nq, nq, h->f_td, d, T, d, 1.0f, 0);
+  run(S_BWD_POINTWISE, [&] {
+    return kd::launch_gated_bwd(f, h->f_dh1, 1, h->f_td, t_emb, w->mod_bias, 2, h->b_dfa, d_mod, d_bias, st);
+  });
+  gemm(h->b_dfa, T, d, h->wT_o, nq, d, d, h->f_dog, nq, T, nq, 1.0f, 0);       // d_og
+  // ---- attention. Pass 1, per head: S = scale q k^T, P = softmax(S), o = P V (into O)
+  const long long qh = static_cast<long long>(L) * hd;  // one head of Q / K (elements)
+  for (int b = 0; b < B; ++b)
+    for (int hq = 0; hq < c.n_q; ++hq) {
+      const int kv = hq / G;
+      const void* Qh = bf(h->q, (static_cast<long long>(b) * c.n_q + hq) * qh);
+      const void* Kh = bf(h->k, (static_cast<long long>(b) * c.n_kv + kv) * qh);
+      const void* VTh = bf(h->vt, (static_cast<long long>(b) * c.n_kv + kv) * hd * static_cast<long long>(f.Lp));
+      gemm(Qh, L, hd, Kh, L, hd, hd, h->f_S, Lp, L, L, scale, 0);
+      run(S_BWD_SOFTMAX, [&] { return kd::launch_softmax_rows(h->f_S, L, Lp, h->b_P, st); });
+      gemm(h->b_P, L, Lp, VTh, hd, f.Lp, Lp, h->f_o + static_cast<long long>(b) * L * nq + hq * hd, nq, L, hd, 1.0f,
+           0);
+    }
+  // output gate: d_o, and the gate's gradient into d_P
+  run(S_BWD_POINTWISE, [&] {
+    return kd::launch_gate_bwd(h->f_dog, h->f_o, h->g, T, nq, c.gate_on, h->b_do, h->b_dP, nqkvg, nq + 2 * nkv,
+                               sms, st);
+  });
+  // V row-major and K^T (zero-padded keys), per (b, kv head)
+  transpose(h->vt, hd, Lp, f.Lp, static_cast<long long>(hd) * f.Lp, h->b_vrow, hd, hd,
+            static_cast<long long>(Lp) * hd, B * c.n_kv);
+  transpose(h->k, L, hd, hd, qh, h->b_kT, Lp, Lp, static_cast<long long>(hd) * Lp, B * c.n_kv);
+  // Pass 2, per head: P again; dP = d_o V^T; dS = P (dP - D) scale; dQ = dS K; dK += dS^T Q;
+  // dV += P^T d_o
+  for (int b = 0; b < B; ++b)
+    for (int hq = 0; hq < c.n_q; ++hq) {
+      const int kv = hq / G;
+      const long long bkv = static_cast<long long>(b) * c.n_kv + kv;
+      const void* Qh = bf(h->q, (static_cast<long long>(b) * c.n_q + hq) * qh);
+      const void* Kh = bf(h->k, bkv * qh);
+      const void* dOh = bf(h->b_do, static_cast<long long>(b) * L * nq + hq * hd);
+      gemm(Qh, L, hd, Kh, L, hd, hd, h->f_S, Lp, L, L, scale, 0);
+      run(S_BWD_SOFTMAX, [&] { return kd::launch_softmax_rows(h->f_S, L, Lp, h->b_P, st); });
+      gemm(dOh, L, nq, bf(h->b_vrow, bkv * Lp * hd), L, hd, hd, h->f_S, Lp, L, L, 1.0f, 0);  // dP
+      run(S_BWD_SOFTMAX, [&] { return kd::launch_attn_ds(h->b_P, h->f_S, L, Lp, scale, h->b_dS, st); });
+      gemm(h->b_dS, L, Lp, bf(h->b_kT, bkv * hd * Lp), hd, Lp, Lp,
+           h->f_dq + (static_cast<long long>(b) * c.n_q + hq) * qh, hd, L, hd, 1.0f, 0);
+      transpose(h->b_dS, L, L, Lp, 0, h->b_dST, Lp, Lp, 0, 1);
+      transpose(Qh, L, hd, hd, 0, h->b_qT, Lp, Lp, 0, 1);
+      gemm(h->b_dST, L, Lp, h->b_qT, hd, Lp, Lp, h->f_dk + bkv * qh, hd, L, hd, 1.0f, 1);
+      transpose(h->b_P, L, L, Lp, 0, h->b_PT, Lp, Lp, 0, 1);
+      transpose(dOh, L, hd, nq, 0, h->b_doT, Lp, Lp, 0, 1);
+      gemm(h->b_PT, L, Lp, h->b_doT, hd, Lp, Lp, h->f_dv + bkv * qh, hd, L, hd, 1.0f, 1);
+    }
+  // ---- QK-norm + RoPE and V into d_P (raw projections recomputed in fp32)
+  gemm(h->xn, T, d, w->w_qkvg, nqkvg, d, d, h->f_raw, nqkvg, T, nqkvg, 1.0f, 0);
+  run(S_BWD_POINTWISE, [&] {
+    return kd::launch_qkv_bwd(f, h->f_raw, nqkvg, h->f_dq, h->f_dk, h->f_dv, w->q_norm_w, w->k_norm_w, h->rope,
+                              h->b_dP, nqkvg, g->d_q_norm_w, g->d_k_norm_w, st);
+  });
+  gemm(h->b_dP, T, nqkvg, h->wT_qkvg, d, nqkvg, nqkvg, h->f_dn, d, T, d, 1.0f, 0);  // d_xn
+  // ---- norm1 + modulation; the residual adds d_h1; d_x in the storage dtype, split
+  const RowSrc xsrc{x_txt, x_img, nullptr};
+  const RowSrc dxs{g->d_x_txt, g->d_x_img, nullptr};
+  run(S_BWD_POINTWISE, [&] {
+    return kd::launch_norm_bwd(f, xsrc, 0, h->f_dn, w->norm1_w, t_emb, w->mod_bias, 0, 1, h->f_dh1, 1, nullptr, dxs,
+                               h->f_rstd, d_mod, d_bias, g->d_norm1_w, st);
+  });
+  // ---- weight gradients: dW = dY^T X over the T rows (both operands transposed, K = Tp)
+  transpose(h->b_dfm, T, d, d, 0, h->t_dfm, Tp, Tp, 0, 1);
+  transpose(h->hmid, T, F, F, 0, h->t_hmid, Tp, Tp, 0, 1);
+  gemm(h->t_dfm, d, Tp, h->t_hmid, F, Tp, Tp, g->d_w_down, F, d, F, 1.0f, 0);
+  transpose(h->b_dau, T, 2 * F, 2LL * F, 0, h->t_dau, Tp, Tp, 0, 1);
+  transpose(h->hn, T, d, d, 0, h->t_hn, Tp, Tp, 0, 1);
+  gemm(h->t_dau, F, Tp, h->t_hn, d, Tp, Tp, g->d_w_gate, d, F, d, 1.0f, 0);
+  gemm(bf(h->t_dau, static_cast<long long>(F) * Tp), F, Tp, h->t_hn, d, Tp, Tp, g->d_w_up, d, F, d, 1.0f, 0);
+  transpose(h->b_dfa, T, d, d, 0, h->t_dfa, Tp, Tp, 0, 1);
+  transpose(h->og, T, nq, nq, 0, h->t_og, Tp, Tp, 0, 1);
+  gemm(h->t_dfa, d, Tp, h->t_og, nq, Tp, Tp, g->d_w_o, nq, d, nq, 1.0f, 0);
+  transpose(h->b_dP, T, nqkvg, nqkvg, 0, h->t_dP, Tp, Tp, 0, 1);
+  transpose(h->xn, T, d, d, 0, h->t_xn, Tp, Tp, 0, 1);
+  gemm(h->t_dP, nqkvg, Tp, h->t_xn, d, Tp, Tp, g->d_w_qkvg, d, nqkvg, d, 1.0f, 0);
+  return e == cudaSuccess ? KREA_DIT_OK : KREA_DIT_ERR_CUDA;
 }
 
 int krea_dit_block_enable_host_io(krea_dit_block_t h) {

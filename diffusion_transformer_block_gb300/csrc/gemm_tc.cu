@@ -332,6 +332,49 @@ struct EpiSwiGLUT {
   }
 };
 
+// C = alpha * (A B^T) (+ C when accumulating), fp32 row-major with row pitch ldc (a
+// multiple of 4): the plain product the block backward is built from.
+struct EpiPlain {
+  static constexpr bool kS8 = false;
+  float* C;
+  long long ldc;
+  int N;
+  int accumulate;
+  float alpha;
+  __device__ __forceinline__ void apply(int row, int nb, int half, uint32_t taddr, int M) const {
+    const int n0 = nb * BN + half * 128;
+    if (n0 >= N) return;
+    const bool ok = row < M;
+    uint32_t r[32];
+#pragma unroll 1
+    for (int c = 0; c < 4; ++c) {
+      const int col = n0 + c * 32;
+      if (col >= N) break;
+      tmem_ld32(taddr + half * 128 + c * 32, r);
+      if (!ok) continue;
+      float* o = C + static_cast<long long>(row) * ldc + col;
+      if (col + 32 <= N) {
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          float4 v = make_float4(alpha * u2f(r[4 * q]), alpha * u2f(r[4 * q + 1]), alpha * u2f(r[4 * q + 2]),
+                                 alpha * u2f(r[4 * q + 3]));
+          float4* p4 = reinterpret_cast<float4*>(o + 4 * q);
+          if (accumulate) {
+            const float4 w = *p4;
+            v.x += w.x;
+            v.y += w.y;
+            v.z += w.z;
+            v.w += w.w;
+          }
+          *p4 = v;
+        }
+      } else {
+        for (int i = 0; i < N - col; ++i) o[i] = alpha * u2f(r[i]) + (accumulate ? o[i] : 0.0f);
+      }
+    }
+  }
+};
+
 // ------------------------------------------------------------------ the kernel
 template <class Epi, bool DUAL>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
@@ -578,7 +621,16 @@ cudaError_t gemm_tc_init_set(int num_sms) {
 
 cudaError_t gemm_tc_init(int num_sms) {
   cudaError_t e = gemm_tc_init_set<false>(num_sms);
-  return e != cudaSuccess ? e : gemm_tc_init_set<true>(num_sms);
+  if (e == cudaSuccess) e = gemm_tc_init_set<true>(num_sms);
+  return e != cudaSuccess ? e : set_smem_attr<EpiPlain, false>(num_sms);
+}
+
+cudaError_t launch_gemm_plain(const CUtensorMap* tm_a, const CUtensorMap* tm_b, int M, int N, int K, float* C,
+                              long long ldc, float alpha, int accumulate, int num_sms, int* err, cudaStream_t st) {
+  if (M <= 0 || N <= 0) return cudaSuccess;
+  if (ldc % 4 || ldc < N) return cudaErrorInvalidValue;
+  EpiPlain epi{C, ldc, N, accumulate, alpha};
+  return launch<EpiPlain, false>(tm_a, tm_b, tm_b, M, (N + BN - 1) / BN, K, epi, num_sms, err, st);
 }
 
 cudaError_t launch_gemm_qkvg(const Fwd& f, const CUtensorMap* tm_a, const CUtensorMap* tm_b, int N,

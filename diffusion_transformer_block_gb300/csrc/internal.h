@@ -114,6 +114,11 @@ cudaError_t launch_gemm_swiglu(const Fwd& f, const CUtensorMap* tm_a, const CUte
                                const CUtensorMap* tm_up, void* hmid, float* rowamax, const Deq* dq, int num_sms,
                                int* err, cudaStream_t st);
 
+// C[M,N] (fp32, row pitch ldc % 4 == 0) = alpha * A[M,K] B[N,K]^T (+ C if accumulate);
+// A and B bf16 K-major tensor maps (box 64 x 128)
+cudaError_t launch_gemm_plain(const CUtensorMap* tm_a, const CUtensorMap* tm_b, int M, int N, int K, float* C,
+                              long long ldc, float alpha, int accumulate, int num_sms, int* err, cudaStream_t st);
+
 // ---- attn_tc.cu (bf16 mode, tcgen05 + TMA) ----
 cudaError_t attn_tc_init();
 // og = softmax(q k^T / sqrt(hd)) v * sigmoid(g); rowamax (optional, pre-zeroed [T]) gets
@@ -129,5 +134,34 @@ cudaError_t launch_quant_e4m3(const void* src, int R, int K, const float* rowama
                               int num_sms, cudaStream_t st);
 // rowamax[r] = max_k |src[r, k]| of a bf16 matrix [R, K] (K % 8 == 0)
 cudaError_t launch_row_amax(const void* src, int R, int K, float* rowamax, int num_sms, cudaStream_t st);
+
+// ---- backward.cu (block backward: transposes, elementwise and reduction steps) ----
+// dst[z][c, r] = src[z][r, c] (bf16), r < R; columns R .. Rp-1 of dst are zeroed
+cudaError_t launch_transpose_bf16(const void* src, int R, int C, long long lds, long long src_bs, void* dst, int Rp,
+                                  long long ldd, long long dst_bs, int batch, cudaStream_t st);
+// y = res + gate_chunk * f: d_f = dy * gate (bf16 [T, d]); sum_l dy f -> d_mod[b, chunk], d_bias[chunk]
+cudaError_t launch_gated_bwd(const Fwd& f, const void* dy, int dy_f32, const float* fv, const float* mod_shared,
+                             const float* mod_bias, int chunk, void* d_f, float* d_mod, float* d_bias, cudaStream_t st);
+// hmid = silu(a) u: d_au = [d_a | d_u] (bf16 [T, 2F])
+cudaError_t launch_swiglu_bwd(const float* d_hmid, const float* a, const float* u, long long T, int F, void* d_au,
+                              int num_sms, cudaStream_t st);
+// norm + modulation backward: dx (fp32 joint, or bf16 into the split buffers of dx_bf16)
+// = d_res + RMSNorm gradient of dy (1 + w)(1 + scale); column sums into d_mod / d_bias / d_gain
+cudaError_t launch_norm_bwd(const Fwd& f, RowSrc xs, int x_f32, const float* dy, const float* gain_w,
+                            const float* mod_shared, const float* mod_bias, int chunk_shift, int chunk_scale,
+                            const void* d_res, int res_f32, float* dx_f32, RowSrc dx_bf16, float* rstd,
+                            float* d_mod, float* d_bias, float* d_gain, cudaStream_t st);
+// attention backward helpers for one head: row softmax of scaled scores (bf16, zero padded)
+// and dS = P (dP - rowsum(P dP)) * scale
+cudaError_t launch_softmax_rows(const float* S, int L, long long ld, void* P, cudaStream_t st);
+cudaError_t launch_attn_ds(const void* P, const float* dP, int L, long long ld, float scale, void* dS,
+                           cudaStream_t st);
+// output gate backward: d_o (bf16 [T, nq]) and the gate's gradient into d_P columns goff..
+cudaError_t launch_gate_bwd(const float* d_og, const float* o, const void* g, long long T, int nq, int gate_on,
+                            void* d_o, void* d_P, int ldp, int goff, int num_sms, cudaStream_t st);
+// QK-norm + RoPE backward and the V gradient into d_P (bf16); gain gradients into d_qw / d_kw
+cudaError_t launch_qkv_bwd(const Fwd& f, const float* raw, int ldr, const float* dq, const float* dk, const float* dv,
+                           const float* q_norm_w, const float* k_norm_w, const float2* rope, void* d_P, int ldp,
+                           float* d_qw, float* d_kw, cudaStream_t st);
 
 }  // namespace kd

@@ -11,7 +11,8 @@ import torch
 
 from . import (KREA_DIT_BF16, KREA_DIT_FP8_ROW, KREA_DIT_FP8_TENSOR, KREA_DIT_FP32, krea_dit_block_create,
                krea_dit_block_destroy, krea_dit_block_forward, krea_dit_block_forward8, krea_dit_block_forward_joint,
-               krea_dit_block_workspace, krea_dit_weights8_quantize, make_weights8,
+               krea_dit_block_workspace, krea_dit_weights8_quantize, make_weights8, krea_dit_block_backward,
+               krea_dit_block_enable_backward, make_grads,
                krea_dit_graph_destroy, krea_dit_graph_launch, krea_dit_stack_forward, krea_dit_stack_graph_create,
                krea_dit_timestep_embed, make_config, make_temb_weights, make_weights)
 
@@ -95,6 +96,31 @@ class DitBlock:
         else:
             krea_dit_block_forward(self.handle, xi, xt, B, img_h, img_w, n_txt, t_emb, self._wstruct, out, st)
         return out
+
+    def backward(self, x_img: Optional[torch.Tensor], x_txt: Optional[torch.Tensor], B: int, img_h: int, img_w: int,
+                 n_txt: int, t_emb: torch.Tensor, d_out: torch.Tensor, stream=None) -> Dict[str, torch.Tensor]:
+        """Gradients of the block (bf16 mode) for the upstream gradient d_out [B, L, d]:
+        d_x_txt, d_x_img (bf16) and fp32 d_<weight>, d_mod_bias, d_mod_shared."""
+        if not getattr(self, "_bw", False):
+            krea_dit_block_enable_backward(self.handle)
+            self._bw = True
+        dev, d = self.device, self.dims["d"]
+        n_img = img_h * img_w
+        g: Dict[str, torch.Tensor] = {
+            "d_x_txt": torch.empty(B, n_txt, d, device=dev, dtype=self.dtype),
+            "d_x_img": torch.empty(B, n_img, d, device=dev, dtype=self.dtype),
+            "d_mod_bias": torch.empty(6, d, device=dev, dtype=torch.float32),
+            "d_mod_shared": torch.empty(B, 6, d, device=dev, dtype=torch.float32),
+        }
+        for k in WEIGHT_KEYS:
+            if k != "mod_bias":
+                g["d_" + k] = torch.empty(self.w[k].shape, device=dev, dtype=torch.float32)
+        gs = make_grads({k: (v if v.numel() else None) for k, v in g.items()})
+        xi = x_img if (x_img is not None and n_img > 0) else None
+        xt = x_txt if (x_txt is not None and n_txt > 0) else None
+        krea_dit_block_backward(self.handle, xi, xt, B, img_h, img_w, n_txt, t_emb, self._wstruct, d_out.contiguous(),
+                                gs, stream or torch.cuda.current_stream(self.device))
+        return g
 
     def forward_joint(self, x: torch.Tensor, B: int, img_h: int, img_w: int, n_txt: int, t_emb: torch.Tensor,
                       out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:

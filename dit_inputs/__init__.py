@@ -188,6 +188,15 @@ def make_stack(cfg: Config, n_blocks: int, **kw) -> List[Case]:
     return [make_case(cfg if i == 0 else cfg.replace(seed=cfg.seed + 7919 * i), **kw) for i in range(n_blocks)]
 
 
+def make_dout(cfg: Config, seed: int = 4321):
+    """Upstream gradient [B, L, d] for a backward: standard normal, rounded to the storage
+    dtype. Returns (float64 array of the rounded values, torch CPU tensor in the dtype)."""
+    g = torch.Generator().manual_seed(seed)
+    x = torch.randn(cfg.B, cfg.L, cfg.d, generator=g, dtype=torch.float64)
+    dev = _round(x, cfg.dtype)
+    return dev.to(torch.float64).numpy(), dev
+
+
 def sample_rows(cfg: Config, n_per_batch: int, seed: int = 1234) -> List[np.ndarray]:
     """Stratified row sample per batch element (joint-sequence indices, text rows
     first): first/last text rows, the four image corners, image-edge rows, then

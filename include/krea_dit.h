@@ -221,6 +221,50 @@ int krea_dit_block_forward8(krea_dit_block_t h, const void* x_img, const void* x
                             int n_txt, const float* t_emb, const krea_dit_weights* w, const krea_dit_weights8* q,
                             void* out, krea_dit_stream_t stream);
 
+/* ---- block backward (KREA_DIT_BF16 mode) -------------------------------------------- */
+
+/* Gradients of one block forward (Krea 2 Technical Report, "Training": the block is
+ * trained, so its forward has a backward). Device memory, caller-owned; every buffer is
+ * overwritten by krea_dit_block_backward.
+ *  d_x_txt, d_x_img  bf16 [B, n_txt, d], [B, img_h*img_w, d]: gradient of the block input
+ *  d_w_*             fp32, the shapes of the matching weights of krea_dit_weights
+ *  d_norm1_w, d_norm2_w fp32 [d]; d_q_norm_w, d_k_norm_w fp32 [hd]
+ *  d_mod_bias        fp32 [6, d]: gradient of the block's modulation bias
+ *  d_mod_shared      fp32 [B, 6, d]: gradient of the shared modulation (chain it through
+ *                    the timestep MLP outside the block) */
+typedef struct {
+  void* d_x_txt;
+  void* d_x_img;
+  float* d_w_qkvg;
+  float* d_w_o;
+  float* d_w_gate;
+  float* d_w_up;
+  float* d_w_down;
+  float* d_norm1_w;
+  float* d_norm2_w;
+  float* d_q_norm_w;
+  float* d_k_norm_w;
+  float* d_mod_bias;
+  float* d_mod_shared;
+} krea_dit_grads;
+
+/* Allocate the backward workspace of a KREA_DIT_BF16 handle (transposed operands and the
+ * recomputed activations for max_batch x max_seq tokens; about 3.5 GB at d = 3072,
+ * F = 8192, 9216 tokens). Synchronous; INVALID_ARG for another mode. Idempotent. */
+int krea_dit_block_enable_backward(krea_dit_block_t h);
+
+/* Gradients of krea_dit_block_forward for the upstream gradient d_out (bf16 [B, L, d],
+ * joint order, text rows first) at inputs x_img, x_txt, t_emb and weights w (the same
+ * arguments as the forward). Recomputes the forward into the handle's workspace, then
+ * runs the chain rule in reverse: the data gradients of the four projections and the
+ * attention products on the tensor cores (bf16 operands, fp32 accumulation), the
+ * attention's probabilities recomputed per head, the weight gradients as products over
+ * the token rows. Needs krea_dit_block_enable_backward (INVALID_ARG otherwise). Errors as
+ * krea_dit_block_forward, plus INVALID_ARG / MISALIGNED for the gradient buffers. */
+int krea_dit_block_backward(krea_dit_block_t h, const void* x_img, const void* x_txt, int B, int img_h, int img_w,
+                            int n_txt, const float* t_emb, const krea_dit_weights* w, const void* d_out,
+                            const krea_dit_grads* g, krea_dit_stream_t stream);
+
 /* ---- joint-layout forward and stacks of blocks ------------------------------------ */
 
 /* One block forward whose input is the joint sequence itself (Krea 2 Technical Report,

@@ -1,0 +1,93 @@
+"""Block backward through the C ABI against the fp64 gradient oracle (``oracle.backward``).
+
+The oracle recomputes the forward with the path's storage rounding (bf16 intermediates,
+fp32 residual stream) and takes exact gradients of it. Criterion per gradient tensor:
+max |gpu - ref| <= TOL_BWD * RMS(ref) (see the module constant for its derivation).
+"""
+import numpy as np
+import pytest
+import torch
+
+import dit_inputs as di
+from gpu_helpers import make_block, path_storage, upload
+from oracle import backward as ob
+
+pytestmark = pytest.mark.gpu
+
+GRADS = ("d_x_txt", "d_x_img", "d_w_qkvg", "d_w_o", "d_w_gate", "d_w_up", "d_w_down", "d_norm1_w", "d_norm2_w",
+         "d_q_norm_w", "d_k_norm_w", "d_mod_bias", "d_mod_shared")
+# The path rounds the gradients it hands from one product to the next to bf16 (d_fm,
+# d_a, d_u, d_fa, d_o, d_P) and the attention probabilities and their gradients (P, dS)
+# too, each a relative error of up to 2^-9 per element; a product over K terms averages
+# these, so a gradient's elementwise error stays a small multiple of 2^-9 of the typical
+# term, and its largest element error within a few percent of its RMS.
+TOL_BWD = 5e-2
+
+
+def run_backward(case, seed=4321):
+    cfg = case.cfg
+    blk = make_block(cfg)
+    try:
+        t, x_img, x_txt = upload(blk, case)
+        ms = blk.timestep_embed(t)
+        dout_np, dout = di.make_dout(cfg, seed)
+        g = blk.backward(x_img, x_txt, cfg.B, cfg.img_h, cfg.img_w, cfg.n_txt, ms, dout.to(blk.device))
+        torch.cuda.synchronize()
+        return {k: v.double().cpu().numpy() for k, v in g.items()}, ms.double().cpu().numpy(), dout_np
+    finally:
+        blk.close()
+
+
+def report(case, got, ms, dout):
+    ref = ob.run_case_backward(case, dout, mod_shared=ms, store=path_storage(case.cfg.dtype))
+    rep = {}
+    for k in GRADS:
+        r, gv = np.asarray(ref[k]), got[k]
+        assert gv.shape == r.shape, (k, gv.shape, r.shape)
+        if r.size == 0:
+            continue
+        rms = float(np.sqrt(np.mean(r * r)))
+        rep[k] = float(np.max(np.abs(gv - r)) / max(rms, 1e-300))
+    return rep
+
+
+@pytest.mark.parametrize("name", ["small_a", "small_b", "small_c", "small_imgonly", "small_txtonly"])
+def test_backward_small(name):
+    case = di.make_case(di.CONFIGS[name])
+    got, ms, dout = run_backward(case)
+    rep = report(case, got, ms, dout)
+    print(name, {k: round(v, 4) for k, v in rep.items()})
+    bad = {k: v for k, v in rep.items() if not v <= TOL_BWD}
+    assert not bad, f"{name}: gradient errors {bad}; full report {rep}"
+
+
+def test_backward_without_gate():
+    case = di.make_case(di.CONFIGS["small_a"].replace(gate_on=False))
+    got, ms, dout = run_backward(case)
+    rep = report(case, got, ms, dout)
+    bad = {k: v for k, v in rep.items() if not v <= TOL_BWD}
+    assert not bad, f"gradient errors {bad}; full report {rep}"
+
+
+def test_backward_is_deterministic():
+    case = di.make_case(di.CONFIGS["small_b"])
+    a, _, _ = run_backward(case)
+    b, _, _ = run_backward(case)
+    # atomics add the modulation / gain column sums in a run-dependent order; the rest is fixed
+    for k in GRADS:
+        if k in ("d_mod_bias", "d_mod_shared", "d_norm1_w", "d_norm2_w", "d_q_norm_w", "d_k_norm_w"):
+            np.testing.assert_allclose(a[k], b[k], rtol=1e-5, atol=1e-6, err_msg=k)
+        else:
+            np.testing.assert_array_equal(a[k], b[k], err_msg=k)
+
+
+@pytest.mark.slow
+def test_backward_medium_width():
+    """The 512px block (d = 3072, F = 8192, 24/8 heads) at batch 1: full-width products,
+    five K/V tiles per head."""
+    case = di.make_case(di.CONFIGS["512px"].replace(B=1))
+    got, ms, dout = run_backward(case)
+    rep = report(case, got, ms, dout)
+    print("512px B=1", {k: round(v, 4) for k, v in rep.items()})
+    bad = {k: v for k, v in rep.items() if not v <= TOL_BWD}
+    assert not bad, f"gradient errors {bad}; full report {rep}"
