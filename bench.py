@@ -176,6 +176,53 @@ def time_gemm8(args, cfg, case, dev, flush, bf16_ms):
     return res
 
 
+def time_backward(args, cfg, blk, case, dev, flush, x_img, x_txt, ms):
+    """The block backward (gradients of input, weights and modulation; the forward is
+    recomputed inside the call), same workload and timing protocol as the headline."""
+    import torch
+
+    import dit_inputs as di
+    import diffusion_transformer_block_gb300 as kd
+
+    world, _, _ = dist_env()
+    peaks = load_peaks()
+    _, dout = di.make_dout(cfg)
+    dout = dout.to(dev)
+    stream = torch.cuda.current_stream(dev)
+    step = lambda: blk.backward(x_img, x_txt, cfg.B, cfg.img_h, cfg.img_w, cfg.n_txt, ms, dout,  # noqa: E731
+                                stream=stream)
+    for _ in range(2):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    kd.krea_dit_block_set_timing(blk.handle, True)
+    kd.krea_dit_block_timing_reset(blk.handle)
+    steps = max(3, min(args.steps, 10))
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for a, b in evs:
+        flush.zero_()
+        a.record(stream)
+        step()
+        b.record(stream)
+    torch.cuda.synchronize()
+    ktimes = kd.krea_dit_block_kernel_times(blk.handle)
+    kd.krea_dit_block_set_timing(blk.handle, False)
+    st, site = kd.krea_dit_block_device_status(blk.handle)
+    if st != kd.KREA_DIT_OK:
+        raise RuntimeError(f"backward device status: {kd.krea_dit_status_string(st)} (site {site})")
+    ms_step = reduce_max(sum(a.elapsed_time(b) for a, b in evs), world) / steps
+    flops = di.config_backward_flops(cfg)
+    return {"ms_per_step": ms_step, "tokens_per_s": world * cfg.T / (ms_step / 1000.0),
+            "tflops": flops / (ms_step / 1000.0) / 1e12,
+            "frac_of_peak": flops / (ms_step / 1000.0) / 1e12 / peaks["bf16_tflops"],
+            "flops_per_step": flops,
+            "kernels_ms_per_step": {k: tot / steps for k, (tot, n) in ktimes.items()},
+            "launches_per_step": sum(n for tot, n in ktimes.values()) / steps,
+            "how": "krea_dit_block_backward (forward recomputed inside), CUDA events per step, L2 flushed before "
+                   "each step outside the events; TFLOP/s counts the backward's algorithmic FLOPs only "
+                   "(2x the projections, 2.5x the attention contractions), not the recomputation"}
+
+
 class ClockSampler:
     """Samples nvidia-smi clocks and throttle reasons while the timed region runs."""
 
@@ -448,6 +495,10 @@ def run_ours(args, cfg):
                         "in place on the joint sequence; CUDA events around each stack"}
         del sw
 
+    backward = None
+    if not args.no_backward:
+        backward = time_backward(args, cfg, blk, case, dev, flush, x_img, x_txt, ms)
+
     gemm8 = None
     if not args.no_gemm8:
         gemm8 = time_gemm8(args, cfg, case, dev, flush, total_ms_max / args.steps)
@@ -510,6 +561,7 @@ def run_ours(args, cfg):
                        "with device and copy streams synchronised on both sides"},
         "stack": stack,
         "gemm8": gemm8,
+        "backward": backward,
         "clocks": clk,
         "gpu_launches": sum(pk["launches"] for pk in per_kernel.values()),
         "wall_s_timed_region": wall,
@@ -535,6 +587,7 @@ def main(argv=None):
     ap.add_argument("--ref-rows", type=int, default=1024, help="query rows per reference-arm step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-gemm8", action="store_true", help="skip the 8-bit GEMM measurement")
+    ap.add_argument("--no-backward", action="store_true", help="skip the block-backward measurement")
     ap.add_argument("--stack-blocks", type=int, default=8, help="blocks of the stack / CUDA-graph measurement (0: skip)")
     args = ap.parse_args(argv)
     if args.warmup < 3:

@@ -49,7 +49,7 @@ enum Slot {
   S_BWD_GEMM,
   S_BWD_TRANSPOSE,
   S_BWD_POINTWISE,
-  S_BWD_SOFTMAX,
+  S_BWD_SCORES,
   S_COUNT
 };
 const char* const kSlotNames[S_COUNT] = {
@@ -60,7 +60,7 @@ const char* const kSlotNames[S_COUNT] = {
     "temb_sinusoid",        "temb_mlp1",             "temb_mlp2",       "norm1_amax",
     "quant_og_e4m3",        "norm2_amax",            "quant_hmid_e4m3", "weights8_row_amax",
     "weights8_quant_e4m3",  "bwd_gemm",              "bwd_transpose",   "bwd_pointwise",
-    "bwd_attn_softmax"};
+    "bwd_attn_scores"};
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
@@ -159,10 +159,13 @@ struct krea_dit_block_s {
   // backward workspace (krea_dit_block_enable_backward): one allocation, carved below
   char* bw = nullptr;
   size_t bw_Tp = 0, bw_Lp = 0;
+  bool bw_stats = false;  // the next forward also writes the attention's lse and ungated output
+  float* f_lse = nullptr;
+  float* f_D = nullptr;
   void *bw_out = nullptr, *wT_down = nullptr, *wT_gu = nullptr, *wT_o = nullptr, *wT_qkvg = nullptr;
   float *f_td = nullptr, *f_hmid = nullptr, *f_a = nullptr, *f_u = nullptr, *f_dn = nullptr, *f_dh1 = nullptr,
         *f_dog = nullptr, *f_o = nullptr, *f_raw = nullptr, *f_dq = nullptr, *f_dk = nullptr, *f_dv = nullptr,
-        *f_S = nullptr, *f_rstd = nullptr;
+        *f_rstd = nullptr;
   void *b_dfm = nullptr, *b_dau = nullptr, *b_dfa = nullptr, *b_do = nullptr, *b_dP = nullptr, *b_P = nullptr,
        *b_dS = nullptr, *b_PT = nullptr, *b_dST = nullptr, *b_vrow = nullptr, *b_kT = nullptr, *b_qT = nullptr,
        *b_doT = nullptr;
@@ -553,7 +556,7 @@ int forward_impl(krea_dit_block_t h, const void* x_img, const void* x_txt, const
     KD_RUN(S_NORM1, kd::launch_norm_modulate(kd::NormIO::BF16_BF16, f, xsrc, w->norm1_w, t_emb, w->mod_bias, 0, 1,
                                              nullptr, sms, st, &q_xn));
     KD_RUN(S_QKVG_TC, kd::launch_gemm_qkvg(f, &tm_xn8, &tm_wqkvg, h->n_qkvg, dst, &dq_qkvg, sms, h->err, st));
-    KD_RUN(S_ATTN, kd::launch_attn_tc(f, &tm_q, &tm_k, &tm_vt, h->g, h->og, h->am_og, sms, h->err, st));
+    KD_RUN(S_ATTN, kd::launch_attn_tc(f, &tm_q, &tm_k, &tm_vt, h->g, h->og, h->am_og, nullptr, nullptr, sms, h->err, st));
     KD_RUN(S_QUANT_OG, kd::launch_quant_e4m3(h->og, f.T, nqhd, h->am_og, per_row, h->og8, h->dq_og, sms, st));
     KD_RUN(S_OPROJ_TC, kd::launch_gemm_resid_attn(f, &tm_og8, &tm_wo, nqhd, xsrc, t_emb, w->mod_bias,
                                                   static_cast<float*>(h->h1), &dq_o, sms, h->err, st));
@@ -587,7 +590,8 @@ int forward_impl(krea_dit_block_t h, const void* x_img, const void* x_txt, const
     KD_RUN(S_NORM1, kd::launch_norm_modulate(kd::NormIO::BF16_BF16, f, xsrc, w->norm1_w, t_emb, w->mod_bias, 0, 1,
                                              h->xn, sms, st));
     KD_RUN(S_QKVG_TC, kd::launch_gemm_qkvg(f, &tm_xn, &tm_wqkvg, h->n_qkvg, dst, nullptr, sms, h->err, st));
-    KD_RUN(S_ATTN, kd::launch_attn_tc(f, &tm_q, &tm_k, &tm_vt, h->g, h->og, nullptr, sms, h->err, st));
+    KD_RUN(S_ATTN, kd::launch_attn_tc(f, &tm_q, &tm_k, &tm_vt, h->g, h->og, nullptr, h->bw_stats ? h->f_lse : nullptr,
+                                        h->bw_stats ? h->f_o : nullptr, sms, h->err, st));
     KD_RUN(S_OPROJ_TC, kd::launch_gemm_resid_attn(f, &tm_og, &tm_wo, nqhd, xsrc, t_emb, w->mod_bias,
                                                   static_cast<float*>(h->h1), nullptr, sms, h->err, st));
     KD_RUN(S_NORM2, kd::launch_norm_modulate(kd::NormIO::F32_BF16, f, h1src, w->norm2_w, t_emb, w->mod_bias, 3, 4,
@@ -758,6 +762,7 @@ int krea_dit_block_enable_backward(krea_dit_block_t h) {
   const size_t T = h->max_T, d = c.d_model, F = c.ffn, hd = c.head_dim;
   const size_t nq = static_cast<size_t>(c.n_q) * hd, nkv = static_cast<size_t>(c.n_kv) * hd, nqkvg = h->n_qkvg;
   const size_t Tp = round_up(T, 64), Lp = round_up(static_cast<size_t>(c.max_seq), 64);
+  const size_t Gq = static_cast<size_t>(c.n_q / c.n_kv);  // query heads per KV head
   struct Item {
     void** p;
     size_t bytes;
@@ -780,21 +785,22 @@ int krea_dit_block_enable_backward(krea_dit_block_t h) {
       {reinterpret_cast<void**>(&h->f_dq), T * nq * 4},
       {reinterpret_cast<void**>(&h->f_dk), T * nkv * 4},
       {reinterpret_cast<void**>(&h->f_dv), T * nkv * 4},
-      {reinterpret_cast<void**>(&h->f_S), Lp * Lp * 4},
       {reinterpret_cast<void**>(&h->f_rstd), T * 4},
+      {reinterpret_cast<void**>(&h->f_lse), T * c.n_q * 4},
+      {reinterpret_cast<void**>(&h->f_D), T * c.n_q * 4},
       {&h->b_dfm, T * d * 2},
       {&h->b_dau, T * 2 * F * 2},
       {&h->b_dfa, T * d * 2},
       {&h->b_do, T * nq * 2},
       {&h->b_dP, T * nqkvg * 2},
-      {&h->b_P, Lp * Lp * 2},
-      {&h->b_dS, Lp * Lp * 2},
-      {&h->b_PT, Lp * Lp * 2},
-      {&h->b_dST, Lp * Lp * 2},
+      {&h->b_P, Gq * Lp * Lp * 2},
+      {&h->b_dS, Gq * Lp * Lp * 2},
+      {&h->b_PT, Lp * Gq * Lp * 2},
+      {&h->b_dST, Lp * Gq * Lp * 2},
       {&h->b_vrow, static_cast<size_t>(c.max_batch) * c.n_kv * Lp * hd * 2},
       {&h->b_kT, static_cast<size_t>(c.max_batch) * c.n_kv * hd * Lp * 2},
-      {&h->b_qT, hd * Lp * 2},
-      {&h->b_doT, hd * Lp * 2},
+      {&h->b_qT, hd * Gq * Lp * 2},
+      {&h->b_doT, hd * Gq * Lp * 2},
       {&h->t_dfm, d * Tp * 2},
       {&h->t_hmid, F * Tp * 2},
       {&h->t_dau, 2 * F * Tp * 2},
@@ -839,7 +845,9 @@ int krea_dit_block_backward(krea_dit_block_t h, const void* x_img, const void* x
   if (!aligned16(d_out) || (g->d_x_img && !aligned16(g->d_x_img)) || (g->d_x_txt && !aligned16(g->d_x_txt)))
     return KREA_DIT_ERR_MISALIGNED;
   // the forward, recomputed: fills the workspace (xn, Q, K, V^T, G, O_g, h1, hn, hmid)
+  h->bw_stats = true;  // the attention also leaves lse and the ungated output
   int r = forward_impl(h, x_img, x_txt, nullptr, B, img_h, img_w, n_txt, t_emb, w, nullptr, h->bw_out, stream);
+  h->bw_stats = false;
   if (r != KREA_DIT_OK) return r;
   const Fwd f = h->last;
   if (f.T == 0) return KREA_DIT_OK;
@@ -882,8 +890,6 @@ int krea_dit_block_backward(krea_dit_block_t h, const void* x_img, const void* x
   if (e == cudaSuccess) e = cudaMemsetAsync(g->d_norm2_w, 0, static_cast<size_t>(d) * 4, st);
   if (e == cudaSuccess) e = cudaMemsetAsync(g->d_q_norm_w, 0, static_cast<size_t>(hd) * 4, st);
   if (e == cudaSuccess) e = cudaMemsetAsync(g->d_k_norm_w, 0, static_cast<size_t>(hd) * 4, st);
-  if (e == cudaSuccess) e = cudaMemsetAsync(h->f_dk, 0, static_cast<size_t>(T) * nkv * 4, st);
-  if (e == cudaSuccess) e = cudaMemsetAsync(h->f_dv, 0, static_cast<size_t>(T) * nkv * 4, st);
   // weights as K-major operands of the data-gradient products
   transpose(w->w_down, d, F, F, 0, h->wT_down, d, d, 0, 1);                    // [F, d]
   transpose(w->w_gate, F, d, d, 0, h->wT_gu, F, 2LL * F, 0, 1);                // [d, 0:F]
@@ -914,49 +920,55 @@ int krea_dit_block_backward(krea_dit_block_t h, const void* x_img, const void* x
     return kd::launch_gated_bwd(f, h->f_dh1, 1, h->f_td, t_emb, w->mod_bias, 2, h->b_dfa, d_mod, d_bias, st);
   });
   gemm(h->b_dfa, T, d, h->wT_o, nq, d, d, h->f_dog, nq, T, nq, 1.0f, 0);       // d_og
-  // ---- attention. Pass 1, per head: S = scale q k^T, P = softmax(S), o = P V (into O)
+  // ---- attention: the forward left each row's log2 normaliser (lse) and the ungated
+  // output o; P and dP are recomputed per head in both orientations by products whose
+  // epilogues finish them (P = exp2(c s - lse), dS = P (dP - D) / sqrt(hd)).
   const long long qh = static_cast<long long>(L) * hd;  // one head of Q / K (elements)
-  for (int b = 0; b < B; ++b)
-    for (int hq = 0; hq < c.n_q; ++hq) {
-      const int kv = hq / G;
-      const void* Qh = bf(h->q, (static_cast<long long>(b) * c.n_q + hq) * qh);
-      const void* Kh = bf(h->k, (static_cast<long long>(b) * c.n_kv + kv) * qh);
-      const void* VTh = bf(h->vt, (static_cast<long long>(b) * c.n_kv + kv) * hd * static_cast<long long>(f.Lp));
-      gemm(Qh, L, hd, Kh, L, hd, hd, h->f_S, Lp, L, L, scale, 0);
-      run(S_BWD_SOFTMAX, [&] { return kd::launch_softmax_rows(h->f_S, L, Lp, h->b_P, st); });
-      gemm(h->b_P, L, Lp, VTh, hd, f.Lp, Lp, h->f_o + static_cast<long long>(b) * L * nq + hq * hd, nq, L, hd, 1.0f,
-           0);
-    }
-  // output gate: d_o, and the gate's gradient into d_P
+  const float c_log2 = scale * 1.4426950408889634f;
   run(S_BWD_POINTWISE, [&] {
-    return kd::launch_gate_bwd(h->f_dog, h->f_o, h->g, T, nq, c.gate_on, h->b_do, h->b_dP, nqkvg, nq + 2 * nkv,
-                               sms, st);
+    return kd::launch_gate_bwd(h->f_dog, h->f_o, h->g, T, L, c.n_q, c.gate_on, h->b_do, h->b_dP, nqkvg,
+                               nq + 2 * nkv, sms, st);
   });
+  run(S_BWD_POINTWISE, [&] { return kd::launch_attn_rowdot(h->b_do, h->f_o, T, L, c.n_q, h->f_D, st); });
   // V row-major and K^T (zero-padded keys), per (b, kv head)
   transpose(h->vt, hd, Lp, f.Lp, static_cast<long long>(hd) * f.Lp, h->b_vrow, hd, hd,
             static_cast<long long>(Lp) * hd, B * c.n_kv);
   transpose(h->k, L, hd, hd, qh, h->b_kT, Lp, Lp, static_cast<long long>(hd) * Lp, B * c.n_kv);
-  // Pass 2, per head: P again; dP = d_o V^T; dS = P (dP - D) scale; dQ = dS K; dK += dS^T Q;
-  // dV += P^T d_o
+  // Per (b, kv head), the group's G query heads stacked (G L rows: Q, d_o, lse and D are
+  // head-major, so the group is one block): P and dS [G L, Lp], P^T and dS^T [L, Lgp]
+  // (Lgp = G L rounded up to 64), then dQ of the whole group, dK and dV each one product
+  // over all G L queries.
+  const int GL = G * L;
+  const int Lgp = static_cast<int>(round_up(static_cast<size_t>(GL), 64));
+  auto attn_gemm = [&](int mode, const void* A, int a_rows, long long a_pitch, const void* Bm, int b_rows,
+                       long long b_pitch, void* out, long long ldo, float cc, const float* v, const void* pin,
+                       long long ldp) {
+    run(S_BWD_SCORES, [&]() -> cudaError_t {
+      CUtensorMap ta, tb;
+      if (!encode_2d(&ta, A, hd, a_rows, a_pitch, 64, 128) || !encode_2d(&tb, Bm, hd, b_rows, b_pitch, 64, 128))
+        return cudaErrorInvalidValue;
+      return kd::launch_gemm_attn_bwd(mode, &ta, &tb, a_rows, b_rows, hd, out, ldo, cc, v, pin, ldp, sms, h->err, st);
+    });
+  };
   for (int b = 0; b < B; ++b)
-    for (int hq = 0; hq < c.n_q; ++hq) {
-      const int kv = hq / G;
+    for (int kv = 0; kv < c.n_kv; ++kv) {
       const long long bkv = static_cast<long long>(b) * c.n_kv + kv;
-      const void* Qh = bf(h->q, (static_cast<long long>(b) * c.n_q + hq) * qh);
+      const long long bh0 = static_cast<long long>(b) * c.n_q + static_cast<long long>(kv) * G;  // first head
+      const void* Qg = bf(h->q, bh0 * qh);
+      const void* dOg = bf(h->b_do, bh0 * qh);
       const void* Kh = bf(h->k, bkv * qh);
-      const void* dOh = bf(h->b_do, static_cast<long long>(b) * L * nq + hq * hd);
-      gemm(Qh, L, hd, Kh, L, hd, hd, h->f_S, Lp, L, L, scale, 0);
-      run(S_BWD_SOFTMAX, [&] { return kd::launch_softmax_rows(h->f_S, L, Lp, h->b_P, st); });
-      gemm(dOh, L, nq, bf(h->b_vrow, bkv * Lp * hd), L, hd, hd, h->f_S, Lp, L, L, 1.0f, 0);  // dP
-      run(S_BWD_SOFTMAX, [&] { return kd::launch_attn_ds(h->b_P, h->f_S, L, Lp, scale, h->b_dS, st); });
-      gemm(h->b_dS, L, Lp, bf(h->b_kT, bkv * hd * Lp), hd, Lp, Lp,
-           h->f_dq + (static_cast<long long>(b) * c.n_q + hq) * qh, hd, L, hd, 1.0f, 0);
-      transpose(h->b_dS, L, L, Lp, 0, h->b_dST, Lp, Lp, 0, 1);
-      transpose(Qh, L, hd, hd, 0, h->b_qT, Lp, Lp, 0, 1);
-      gemm(h->b_dST, L, Lp, h->b_qT, hd, Lp, Lp, h->f_dk + bkv * qh, hd, L, hd, 1.0f, 1);
-      transpose(h->b_P, L, L, Lp, 0, h->b_PT, Lp, Lp, 0, 1);
-      transpose(dOh, L, hd, nq, 0, h->b_doT, Lp, Lp, 0, 1);
-      gemm(h->b_PT, L, Lp, h->b_doT, hd, Lp, Lp, h->f_dv + bkv * qh, hd, L, hd, 1.0f, 1);
+      const void* Vh = bf(h->b_vrow, bkv * Lp * hd);
+      const float* lse = h->f_lse + bh0 * L;
+      const float* Dg = h->f_D + bh0 * L;
+      attn_gemm(1, Qg, GL, hd, Kh, L, hd, h->b_P, Lp, c_log2, lse, nullptr, 0);        // P [G L, Lp]
+      attn_gemm(2, Kh, L, hd, Qg, GL, hd, h->b_PT, Lgp, c_log2, lse, nullptr, 0);      // P^T [L, Lgp]
+      attn_gemm(3, dOg, GL, hd, Vh, L, hd, h->b_dS, Lp, scale, Dg, h->b_P, Lp);        // dS
+      attn_gemm(4, Vh, L, hd, dOg, GL, hd, h->b_dST, Lgp, scale, Dg, h->b_PT, Lgp);    // dS^T
+      gemm(h->b_dS, GL, Lp, bf(h->b_kT, bkv * hd * Lp), hd, Lp, Lp, h->f_dq + bh0 * qh, hd, GL, hd, 1.0f, 0);
+      transpose(Qg, GL, hd, hd, 0, h->b_qT, Lgp, Lgp, 0, 1);
+      gemm(h->b_dST, L, Lgp, h->b_qT, hd, Lgp, Lgp, h->f_dk + bkv * qh, hd, L, hd, 1.0f, 0);
+      transpose(dOg, GL, hd, hd, 0, h->b_doT, Lgp, Lgp, 0, 1);
+      gemm(h->b_PT, L, Lgp, h->b_doT, hd, Lgp, Lgp, h->f_dv + bkv * qh, hd, L, hd, 1.0f, 0);
     }
   // ---- QK-norm + RoPE and V into d_P (raw projections recomputed in fp32)
   gemm(h->xn, T, d, w->w_qkvg, nqkvg, d, d, h->f_raw, nqkvg, T, nqkvg, 1.0f, 0);

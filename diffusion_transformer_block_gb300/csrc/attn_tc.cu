@@ -53,6 +53,9 @@ struct AttnArgs {
   const bf16* g;     // [T, n_q*hd] gate pre-activation
   bf16* og;          // [T, n_q*hd]
   float* rowamax;    // optional [T]: largest |og| of each row, as stored (for an 8-bit o_proj)
+  float* lse;        // optional [B, n_q, L]: log2 of each row's softmax normaliser, in the
+                     // scaled-log2 units of the scores (for the backward)
+  float* o_raw;      // optional [T, n_q*hd] fp32: the attention output before the gate (backward)
   int* err;
 };
 
@@ -343,6 +346,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             float o[32];
 #pragma unroll
             for (int i = 0; i < 32; ++i) o[i] = __uint_as_float(r[i]) * inv_l;
+            if (a.o_raw) {
+              float4* w4 = reinterpret_cast<float4*>(a.o_raw + off + c * 32);
+#pragma unroll
+              for (int q = 0; q < 8; ++q) w4[q] = make_float4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+            }
             if (a.gate_on) {
               const uint4* g4 = reinterpret_cast<const uint4*>(a.g + off + c * 32);
 #pragma unroll
@@ -369,6 +377,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
         }
         // bf16 rounding is monotone, so the largest stored magnitude is the rounded largest
+        if (a.lse && valid)
+          a.lse[(static_cast<size_t>(b) * a.n_q + tile_head(t)) * a.L + ql] = m_run + log2f(l_run);
         if (a.rowamax && valid)
           atomic_max_nonneg(a.rowamax + static_cast<size_t>(b) * a.L + ql, round_bf16(amax));
       }
@@ -390,7 +400,8 @@ cudaError_t attn_tc_init() {
 }
 
 cudaError_t launch_attn_tc(const Fwd& f, const CUtensorMap* tm_q, const CUtensorMap* tm_k, const CUtensorMap* tm_vt,
-                           const void* g, void* og, float* rowamax, int num_sms, int* err, cudaStream_t st) {
+                           const void* g, void* og, float* rowamax, float* lse, float* o_raw, int num_sms, int* err,
+                           cudaStream_t st) {
   (void)num_sms;
   AttnArgs a;
   a.B = f.B;
@@ -406,6 +417,8 @@ cudaError_t launch_attn_tc(const Fwd& f, const CUtensorMap* tm_q, const CUtensor
   a.g = reinterpret_cast<const bf16*>(g);
   a.og = reinterpret_cast<bf16*>(og);
   a.rowamax = rowamax;
+  a.lse = lse;
+  a.o_raw = o_raw;
   a.err = err;
   const long long units = static_cast<long long>(f.B) * f.n_kv * a.npairs;
   if (units == 0) return cudaSuccess;

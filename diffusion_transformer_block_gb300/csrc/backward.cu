@@ -159,61 +159,27 @@ __global__ void norm_bwd_cols_kernel(Fwd f, RowSrc xs, int x_f32, const float* _
   atomicAdd(&d_gain[c], s_dyn * (1.0f + scale));
 }
 
-// Attention, backward, one head: P = softmax of the scaled scores S (fp32 [L, ld]) row by
-// row, as bf16 [L, ld] with columns L .. ld-1 zero. One block per row.
-__global__ void softmax_rows_kernel(const float* __restrict__ S, int L, long long ld, bf16* __restrict__ P) {
-  __shared__ float red[32];
-  const float* s = S + blockIdx.x * ld;
-  bf16* p = P + blockIdx.x * ld;
-  float m = -INFINITY;
-  for (int j = threadIdx.x; j < L; j += blockDim.x) m = fmaxf(m, s[j]);
-  m = warp_max(m);
-  {
-    const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    __syncthreads();
-    if (lane == 0) red[w] = m;
-    __syncthreads();
-    m = -INFINITY;
-    for (int i = 0; i < (blockDim.x >> 5); ++i) m = fmaxf(m, red[i]);
-  }
-  float l = 0.0f;
-  for (int j = threadIdx.x; j < L; j += blockDim.x) l += __expf(s[j] - m);
-  l = block_sum(l, red);
-  const float inv = 1.0f / l;
-  for (int j = threadIdx.x; j < ld; j += blockDim.x)
-    p[j] = __float2bfloat16_rn(j < L ? __expf(s[j] - m) * inv : 0.0f);
-}
-
-// dS = P (dP - D) * scale, D = sum_j P dP (row), bf16 [L, ld] with zero padding.
-__global__ void attn_ds_kernel(const bf16* __restrict__ P, const float* __restrict__ dP, int L, long long ld,
-                               float scale, bf16* __restrict__ dS) {
-  __shared__ float red[32];
-  const bf16* p = P + blockIdx.x * ld;
-  const float* dp = dP + blockIdx.x * ld;
-  bf16* ds = dS + blockIdx.x * ld;
-  float D = 0.0f;
-  for (int j = threadIdx.x; j < L; j += blockDim.x) D = fmaf(__bfloat162float(p[j]), dp[j], D);
-  D = block_sum(D, red);
-  for (int j = threadIdx.x; j < ld; j += blockDim.x)
-    ds[j] = __float2bfloat16_rn(j < L ? __bfloat162float(p[j]) * (dp[j] - D) * scale : 0.0f);
-}
-
-// Output gate, backward: og = o sigmoid(g). d_o = d_og sigmoid(g) (bf16 [T, nq]); the
+// Output gate, backward: og = o sigmoid(g). d_o = d_og sigmoid(g), stored head-major (bf16
+// [B, n_q, L, 128], so that a KV group's heads are one contiguous block of rows); the
 // gate's gradient d_og o sigmoid(g)(1 - sigmoid(g)) goes to d_P's g columns (bf16).
 __global__ void gate_bwd_kernel(const float* __restrict__ d_og, const float* __restrict__ o,
-                                const bf16* __restrict__ g, long long T, int nq, int gate_on, bf16* __restrict__ d_o,
-                                bf16* __restrict__ d_P, int ldp, int goff) {
+                                const bf16* __restrict__ g, long long T, int L, int n_q, int gate_on,
+                                bf16* __restrict__ d_o, bf16* __restrict__ d_P, int ldp, int goff) {
+  const int nq = n_q * 128;
   const long long n = T * nq;
   for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n;
        i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const long long t = i / nq;
+    const int col = static_cast<int>(i - t * nq);
+    const long long b = t / L, l = t - b * L;
+    const long long hm = ((b * n_q + (col >> 7)) * L + l) * 128 + (col & 127);
     const float dv = d_og[i];
     if (gate_on) {
       const float sg = 1.0f / (1.0f + __expf(-__bfloat162float(g[i])));
-      d_o[i] = __float2bfloat16_rn(dv * sg);
-      const long long t = i / nq;
-      d_P[t * ldp + goff + (i - t * nq)] = __float2bfloat16_rn(dv * o[i] * sg * (1.0f - sg));
+      d_o[hm] = __float2bfloat16_rn(dv * sg);
+      d_P[t * ldp + goff + col] = __float2bfloat16_rn(dv * o[i] * sg * (1.0f - sg));
     } else {
-      d_o[i] = __float2bfloat16_rn(dv);
+      d_o[hm] = __float2bfloat16_rn(dv);
     }
   }
 }
@@ -267,9 +233,36 @@ __global__ void qkv_bwd_kernel(Fwd f, const float* __restrict__ raw, int ldr, co
   if (kind < 2) atomicAdd(kind == 0 ? &d_qw[j] : &d_kw[j], gacc);
 }
 
+// D[b, h, l] = sum_j d_o[b, h, l, j] o[t, h hd + j] (t = b L + l, hd = 128; d_o head-major):
+// the row term of the softmax gradient, rowsum(P dP) = rowsum(dO O). One warp per (row, head).
+__global__ void attn_rowdot_kernel(const bf16* __restrict__ d_o, const float* __restrict__ o, int T, int L, int n_q,
+                                   float* __restrict__ D) {
+  const long long wid = (blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (wid >= static_cast<long long>(T) * n_q) return;
+  const int t = static_cast<int>(wid / n_q), h = static_cast<int>(wid - static_cast<long long>(t) * n_q);
+  const int b = t / L, l = t - b * L;
+  const long long base = static_cast<long long>(t) * n_q * 128 + h * 128 + lane * 4;
+  const long long hm = ((static_cast<long long>(b) * n_q + h) * L + l) * 128 + lane * 4;
+  const uint2 u = *reinterpret_cast<const uint2*>(d_o + hm);
+  const float4 ov = *reinterpret_cast<const float4*>(o + base);
+  const float2 a = unpack_bf16x2(u.x), b2 = unpack_bf16x2(u.y);
+  float s = a.x * ov.x + a.y * ov.y + b2.x * ov.z + b2.y * ov.w;
+  s = warp_sum(s);
+  if (lane == 0) D[(static_cast<long long>(b) * n_q + h) * L + l] = s;
+}
+
 }  // namespace
 
 // ------------------------------------------------------------------ launchers
+cudaError_t launch_attn_rowdot(const void* d_o, const float* o, int T, int L, int n_q, float* D, cudaStream_t st) {
+  const long long warps = static_cast<long long>(T) * n_q;
+  if (warps == 0) return cudaSuccess;
+  const long long blocks = (warps * 32 + 255) / 256;
+  attn_rowdot_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(reinterpret_cast<const bf16*>(d_o), o, T, L, n_q,
+                                                                   D);
+  return cudaGetLastError();
+}
 cudaError_t launch_transpose_bf16(const void* src, int R, int C, long long lds, long long src_bs, void* dst, int Rp,
                                   long long ldd, long long dst_bs, int batch, cudaStream_t st) {
   if (R <= 0 || C <= 0 || batch <= 0) return cudaSuccess;
@@ -309,22 +302,9 @@ cudaError_t launch_norm_bwd(const Fwd& f, RowSrc xs, int x_f32, const float* dy,
   return cudaGetLastError();
 }
 
-cudaError_t launch_softmax_rows(const float* S, int L, long long ld, void* P, cudaStream_t st) {
-  if (L <= 0) return cudaSuccess;
-  softmax_rows_kernel<<<L, 256, 0, st>>>(S, L, ld, reinterpret_cast<bf16*>(P));
-  return cudaGetLastError();
-}
-
-cudaError_t launch_attn_ds(const void* P, const float* dP, int L, long long ld, float scale, void* dS,
-                           cudaStream_t st) {
-  if (L <= 0) return cudaSuccess;
-  attn_ds_kernel<<<L, 256, 0, st>>>(reinterpret_cast<const bf16*>(P), dP, L, ld, scale, reinterpret_cast<bf16*>(dS));
-  return cudaGetLastError();
-}
-
-cudaError_t launch_gate_bwd(const float* d_og, const float* o, const void* g, long long T, int nq, int gate_on,
+cudaError_t launch_gate_bwd(const float* d_og, const float* o, const void* g, long long T, int L, int n_q, int gate_on,
                             void* d_o, void* d_P, int ldp, int goff, int num_sms, cudaStream_t st) {
-  gate_bwd_kernel<<<num_sms * 8, 256, 0, st>>>(d_og, o, reinterpret_cast<const bf16*>(g), T, nq, gate_on,
+  gate_bwd_kernel<<<num_sms * 8, 256, 0, st>>>(d_og, o, reinterpret_cast<const bf16*>(g), T, L, n_q, gate_on,
                                                reinterpret_cast<bf16*>(d_o), reinterpret_cast<bf16*>(d_P), ldp, goff);
   return cudaGetLastError();
 }

@@ -231,3 +231,11 @@ def config_flops(cfg: Config) -> float:
     lin = 2.0 * T * d * qkvg_rows + 2.0 * T * cfg.n_q * hd * d + 2.0 * T * d * 2 * F + 2.0 * T * F * d
     attn = 4.0 * cfg.B * cfg.L * cfg.L * cfg.n_q * hd
     return lin + attn
+
+
+def config_backward_flops(cfg: Config) -> float:
+    """Algorithmic FLOPs of one block backward: a data and a weight gradient product per
+    projection (2x the forward's), and the attention's dV, dP, dQ, dK products plus the
+    score product it recomputes (2.5x the forward's two contractions)."""
+    attn = 4.0 * cfg.B * cfg.L * cfg.L * cfg.n_q * cfg.hd
+    return 2.0 * (config_flops(cfg) - attn) + 2.5 * attn

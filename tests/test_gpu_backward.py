@@ -1,8 +1,17 @@
 """Block backward through the C ABI against the fp64 gradient oracle (``oracle.backward``).
 
 The oracle recomputes the forward with the path's storage rounding (bf16 intermediates,
-fp32 residual stream) and takes exact gradients of it. Criterion per gradient tensor:
-max |gpu - ref| <= TOL_BWD * RMS(ref) (see the module constant for its derivation).
+fp32 residual stream) and takes exact gradients of it (``ref``); ``exact`` is the same
+without storage rounding. Criteria per gradient tensor g:
+  * relative RMS error ||g - ref|| / ||ref|| <= TOL_RMS;
+  * max |g - ref| <= TOL_BWD * RMS(ref) + 2 max |ref - exact|.
+A weight gradient sums products over all token rows, so a few entries collect the
+rounding of many large terms: the oracle's own storage rounding moves the largest entry
+of dW_o by 7% of its RMS at the 512px width (measured), while the RMS moves by a tenth of
+a percent. The path rounds in the same places as the oracle and additionally rounds the
+gradients it hands between products to bf16 (d_fm, d_a, d_u, d_fa, d_o, d_P, P, dS); the
+max criterion therefore allows twice the oracle's own rounding sensitivity on top of
+TOL_BWD, and the RMS criterion keeps the bulk tight.
 """
 import numpy as np
 import pytest
@@ -16,12 +25,8 @@ pytestmark = pytest.mark.gpu
 
 GRADS = ("d_x_txt", "d_x_img", "d_w_qkvg", "d_w_o", "d_w_gate", "d_w_up", "d_w_down", "d_norm1_w", "d_norm2_w",
          "d_q_norm_w", "d_k_norm_w", "d_mod_bias", "d_mod_shared")
-# The path rounds the gradients it hands from one product to the next to bf16 (d_fm,
-# d_a, d_u, d_fa, d_o, d_P) and the attention probabilities and their gradients (P, dS)
-# too, each a relative error of up to 2^-9 per element; a product over K terms averages
-# these, so a gradient's elementwise error stays a small multiple of 2^-9 of the typical
-# term, and its largest element error within a few percent of its RMS.
-TOL_BWD = 5e-2
+TOL_BWD = 5e-2  # the forward block's max-abs tolerance, 2.5x (bf16 gradients between products)
+TOL_RMS = 2e-2  # relative RMS error of every gradient tensor
 
 
 def run_backward(case, seed=4321):
@@ -40,33 +45,34 @@ def run_backward(case, seed=4321):
 
 def report(case, got, ms, dout):
     ref = ob.run_case_backward(case, dout, mod_shared=ms, store=path_storage(case.cfg.dtype))
+    exact = ob.run_case_backward(case, dout, mod_shared=ms)
     rep = {}
     for k in GRADS:
-        r, gv = np.asarray(ref[k]), got[k]
+        r, gv, e = np.asarray(ref[k]), got[k], np.asarray(exact[k])
         assert gv.shape == r.shape, (k, gv.shape, r.shape)
         if r.size == 0:
             continue
-        rms = float(np.sqrt(np.mean(r * r)))
-        rep[k] = float(np.max(np.abs(gv - r)) / max(rms, 1e-300))
+        rms = max(float(np.sqrt(np.mean(r * r))), 1e-300)
+        rep[k + ":rms"] = float(np.sqrt(np.mean((gv - r) ** 2))) / rms / TOL_RMS
+        rep[k + ":max"] = float(np.max(np.abs(gv - r))) / (TOL_BWD * rms + 2 * float(np.max(np.abs(r - e))))
     return rep
+
+
+def check(name, case):
+    got, ms, dout = run_backward(case)
+    rep = report(case, got, ms, dout)
+    print(name, {k: round(v, 3) for k, v in rep.items()})
+    bad = {k: v for k, v in rep.items() if not v <= 1.0}
+    assert not bad, f"{name}: gradient errors (ratio to bound) {bad}; full report {rep}"
 
 
 @pytest.mark.parametrize("name", ["small_a", "small_b", "small_c", "small_imgonly", "small_txtonly"])
 def test_backward_small(name):
-    case = di.make_case(di.CONFIGS[name])
-    got, ms, dout = run_backward(case)
-    rep = report(case, got, ms, dout)
-    print(name, {k: round(v, 4) for k, v in rep.items()})
-    bad = {k: v for k, v in rep.items() if not v <= TOL_BWD}
-    assert not bad, f"{name}: gradient errors {bad}; full report {rep}"
+    check(name, di.make_case(di.CONFIGS[name]))
 
 
 def test_backward_without_gate():
-    case = di.make_case(di.CONFIGS["small_a"].replace(gate_on=False))
-    got, ms, dout = run_backward(case)
-    rep = report(case, got, ms, dout)
-    bad = {k: v for k, v in rep.items() if not v <= TOL_BWD}
-    assert not bad, f"gradient errors {bad}; full report {rep}"
+    check("small_a no gate", di.make_case(di.CONFIGS["small_a"].replace(gate_on=False)))
 
 
 def test_backward_is_deterministic():
@@ -85,9 +91,4 @@ def test_backward_is_deterministic():
 def test_backward_medium_width():
     """The 512px block (d = 3072, F = 8192, 24/8 heads) at batch 1: full-width products,
     five K/V tiles per head."""
-    case = di.make_case(di.CONFIGS["512px"].replace(B=1))
-    got, ms, dout = run_backward(case)
-    rep = report(case, got, ms, dout)
-    print("512px B=1", {k: round(v, 4) for k, v in rep.items()})
-    bad = {k: v for k, v in rep.items() if not v <= TOL_BWD}
-    assert not bad, f"gradient errors {bad}; full report {rep}"
+    check("512px B=1", di.make_case(di.CONFIGS["512px"].replace(B=1)))
