@@ -48,12 +48,12 @@ constexpr int SMEM_BYTES = SMEM_BAR + 256 + 1024;
 constexpr float RESCALE_THRESHOLD = 8.0f;  // log2 units: rescale O only if the max grows by > 2^8
 
 struct AttnArgs {
-  int B, L, n_q, n_kv, G, nqt, nkt, npairs, gate_on;
+  int B, L, Lp, n_q, n_kv, G, nqt, nkt, npairs, gate_on;
   float scale_log2;  // log2(e) / sqrt(hd)
   const bf16* g;     // [T, n_q*hd] gate pre-activation
   bf16* og;          // [T, n_q*hd]
   float* rowamax;    // optional [T]: largest |og| of each row, as stored (for an 8-bit o_proj)
-  float* lse;        // optional [B, n_q, L]: log2 of each row's softmax normaliser, in the
+  float* lse;        // optional [B, n_q, Lp]: log2 of each row's softmax normaliser, in the
                      // scaled-log2 units of the scores (for the backward)
   float* o_raw;      // optional [T, n_q*hd] fp32: the attention output before the gate (backward)
   int* err;
@@ -378,7 +378,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         // bf16 rounding is monotone, so the largest stored magnitude is the rounded largest
         if (a.lse && valid)
-          a.lse[(static_cast<size_t>(b) * a.n_q + tile_head(t)) * a.L + ql] = m_run + log2f(l_run);
+          a.lse[(static_cast<size_t>(b) * a.n_q + tile_head(t)) * a.Lp + ql] = m_run + log2f(l_run);
         if (a.rowamax && valid)
           atomic_max_nonneg(a.rowamax + static_cast<size_t>(b) * a.L + ql, round_bf16(amax));
       }
@@ -406,6 +406,7 @@ cudaError_t launch_attn_tc(const Fwd& f, const CUtensorMap* tm_q, const CUtensor
   AttnArgs a;
   a.B = f.B;
   a.L = f.L;
+  a.Lp = f.Lp;
   a.n_q = f.n_q;
   a.n_kv = f.n_kv;
   a.G = f.n_q / f.n_kv;

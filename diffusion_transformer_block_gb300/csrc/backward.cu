@@ -235,8 +235,8 @@ __global__ void qkv_bwd_kernel(Fwd f, const float* __restrict__ raw, int ldr, co
 
 // D[b, h, l] = sum_j d_o[b, h, l, j] o[t, h hd + j] (t = b L + l, hd = 128; d_o head-major):
 // the row term of the softmax gradient, rowsum(P dP) = rowsum(dO O). One warp per (row, head).
-__global__ void attn_rowdot_kernel(const bf16* __restrict__ d_o, const float* __restrict__ o, int T, int L, int n_q,
-                                   float* __restrict__ D) {
+__global__ void attn_rowdot_kernel(const bf16* __restrict__ d_o, const float* __restrict__ o, int T, int L, int Lp,
+                                   int n_q, float* __restrict__ D) {
   const long long wid = (blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (wid >= static_cast<long long>(T) * n_q) return;
@@ -249,18 +249,19 @@ __global__ void attn_rowdot_kernel(const bf16* __restrict__ d_o, const float* __
   const float2 a = unpack_bf16x2(u.x), b2 = unpack_bf16x2(u.y);
   float s = a.x * ov.x + a.y * ov.y + b2.x * ov.z + b2.y * ov.w;
   s = warp_sum(s);
-  if (lane == 0) D[(static_cast<long long>(b) * n_q + h) * L + l] = s;
+  if (lane == 0) D[(static_cast<long long>(b) * n_q + h) * Lp + l] = s;
 }
 
 }  // namespace
 
 // ------------------------------------------------------------------ launchers
-cudaError_t launch_attn_rowdot(const void* d_o, const float* o, int T, int L, int n_q, float* D, cudaStream_t st) {
+cudaError_t launch_attn_rowdot(const void* d_o, const float* o, int T, int L, int Lp, int n_q, float* D,
+                               cudaStream_t st) {
   const long long warps = static_cast<long long>(T) * n_q;
   if (warps == 0) return cudaSuccess;
   const long long blocks = (warps * 32 + 255) / 256;
-  attn_rowdot_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(reinterpret_cast<const bf16*>(d_o), o, T, L, n_q,
-                                                                   D);
+  attn_rowdot_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(reinterpret_cast<const bf16*>(d_o), o, T, L, Lp,
+                                                                   n_q, D);
   return cudaGetLastError();
 }
 cudaError_t launch_transpose_bf16(const void* src, int R, int C, long long lds, long long src_bs, void* dst, int Rp,

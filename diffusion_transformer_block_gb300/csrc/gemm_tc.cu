@@ -375,87 +375,6 @@ struct EpiPlain {
   }
 };
 
-// The attention backward's score-sized products, finished in the epilogue and stored as
-// bf16 [M, ldo] (columns N .. ldo-1 zeroed): MODE 1 P = exp2(c acc - v[row]), MODE 2
-// P^T = exp2(c acc - v[col]) (v = the rows' log2 normalisers, c = the scores' log2
-// scale), MODE 3 dS = P (acc - v[row]) c, MODE 4 dS^T = P^T (acc - v[col]) c (acc = dP or
-// dP^T, v = D = rowsum(dO O), c = 1/sqrt(hd), P or P^T read from pin).
-template <int MODE>
-struct EpiAttnBwd {
-  static constexpr bool kS8 = false;
-  bf16* out;
-  long long ldo;
-  int N;
-  float c;
-  const float* v;
-  const bf16* pin;
-  long long ldp;
-  __device__ __forceinline__ static float fex2(float x) {
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-  }
-  __device__ __forceinline__ float value(float acc, float vr, float vc, float p) const {
-    if (MODE == 1) return fex2(c * acc - vr);
-    if (MODE == 2) return fex2(c * acc - vc);
-    if (MODE == 3) return p * (acc - vr) * c;
-    return p * (acc - vc) * c;
-  }
-  __device__ __forceinline__ void apply(int row, int nb, int half, uint32_t taddr, int M) const {
-    const int n0 = nb * BN + half * 128;
-    if (n0 >= ldo) return;
-    const bool ok = row < M;
-    const float vr = (MODE == 1 || MODE == 3) && ok ? v[row] : 0.0f;
-    uint32_t r[32];
-#pragma unroll 1
-    for (int ch = 0; ch < 4; ++ch) {
-      const int col = n0 + ch * 32;
-      if (col >= ldo) break;
-      if (col < N) tmem_ld32(taddr + half * 128 + ch * 32, r);
-      if (!ok) continue;
-      bf16* o = out + static_cast<long long>(row) * ldo + col;
-      const bf16* pi = (MODE >= 3) ? pin + static_cast<long long>(row) * ldp + col : nullptr;
-      if (col + 32 <= N) {  // whole chunk inside: vector loads of P and of the column terms
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          float pv[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f}, vc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-          if (MODE >= 3) {
-            const uint4 u = *reinterpret_cast<const uint4*>(pi + 8 * q);
-            const float2 a0 = unpack_bf16x2(u.x), a1 = unpack_bf16x2(u.y), a2 = unpack_bf16x2(u.z),
-                         a3 = unpack_bf16x2(u.w);
-            pv[0] = a0.x; pv[1] = a0.y; pv[2] = a1.x; pv[3] = a1.y; pv[4] = a2.x; pv[5] = a2.y; pv[6] = a3.x;
-            pv[7] = a3.y;
-          }
-          if (MODE == 2 || MODE == 4) {  // the same columns for every lane: broadcast loads
-#pragma unroll
-            for (int i = 0; i < 8; ++i) vc[i] = __ldg(v + col + 8 * q + i);
-          }
-          float y[8];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) y[i] = value(u2f(r[8 * q + i]), vr, vc[i], pv[i]);
-          *reinterpret_cast<uint4*>(o + 8 * q) = make_uint4(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]),
-                                                            pack_bf16x2(y[4], y[5]), pack_bf16x2(y[6], y[7]));
-        }
-      } else {  // the chunk holding column N: element by element, zeros past N
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          float y[8];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const int cc = col + 8 * q + i;
-            y[i] = cc < N ? value(u2f(r[8 * q + i]), vr, (MODE == 2 || MODE == 4) ? v[cc] : 0.0f,
-                                  MODE >= 3 ? __bfloat162float(pi[8 * q + i]) : 0.0f)
-                          : 0.0f;
-          }
-          if (col + 8 * q < ldo)
-            *reinterpret_cast<uint4*>(o + 8 * q) = make_uint4(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]),
-                                                              pack_bf16x2(y[4], y[5]), pack_bf16x2(y[6], y[7]));
-        }
-      }
-    }
-  }
-};
-
 // ------------------------------------------------------------------ the kernel
 template <class Epi, bool DUAL>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
@@ -703,32 +622,7 @@ cudaError_t gemm_tc_init_set(int num_sms) {
 cudaError_t gemm_tc_init(int num_sms) {
   cudaError_t e = gemm_tc_init_set<false>(num_sms);
   if (e == cudaSuccess) e = gemm_tc_init_set<true>(num_sms);
-  if (e == cudaSuccess) e = set_smem_attr<EpiPlain, false>(num_sms);
-  if (e == cudaSuccess) e = set_smem_attr<EpiAttnBwd<1>, false>(num_sms);
-  if (e == cudaSuccess) e = set_smem_attr<EpiAttnBwd<2>, false>(num_sms);
-  if (e == cudaSuccess) e = set_smem_attr<EpiAttnBwd<3>, false>(num_sms);
-  return e != cudaSuccess ? e : set_smem_attr<EpiAttnBwd<4>, false>(num_sms);
-}
-
-cudaError_t launch_gemm_attn_bwd(int mode, const CUtensorMap* tm_a, const CUtensorMap* tm_b, int M, int N, int K,
-                                 void* out, long long ldo, float c, const float* v, const void* pin, long long ldp,
-                                 int num_sms, int* err, cudaStream_t st) {
-  if (M <= 0 || N <= 0) return cudaSuccess;
-  if (ldo % 8 || ldo < N || (mode >= 3 && (!pin || ldp % 8))) return cudaErrorInvalidValue;
-  const int num_n = static_cast<int>((ldo + BN - 1) / BN);
-  bf16* o = reinterpret_cast<bf16*>(out);
-  const bf16* p = reinterpret_cast<const bf16*>(pin);
-  switch (mode) {
-    case 1: return launch<EpiAttnBwd<1>, false>(tm_a, tm_b, tm_b, M, num_n, K, EpiAttnBwd<1>{o, ldo, N, c, v, p, ldp},
-                                                num_sms, err, st);
-    case 2: return launch<EpiAttnBwd<2>, false>(tm_a, tm_b, tm_b, M, num_n, K, EpiAttnBwd<2>{o, ldo, N, c, v, p, ldp},
-                                                num_sms, err, st);
-    case 3: return launch<EpiAttnBwd<3>, false>(tm_a, tm_b, tm_b, M, num_n, K, EpiAttnBwd<3>{o, ldo, N, c, v, p, ldp},
-                                                num_sms, err, st);
-    case 4: return launch<EpiAttnBwd<4>, false>(tm_a, tm_b, tm_b, M, num_n, K, EpiAttnBwd<4>{o, ldo, N, c, v, p, ldp},
-                                                num_sms, err, st);
-    default: return cudaErrorInvalidValue;
-  }
+  return e != cudaSuccess ? e : set_smem_attr<EpiPlain, false>(num_sms);
 }
 
 cudaError_t launch_gemm_plain(const CUtensorMap* tm_a, const CUtensorMap* tm_b, int M, int N, int K, float* C,

@@ -119,22 +119,28 @@ cudaError_t launch_gemm_swiglu(const Fwd& f, const CUtensorMap* tm_a, const CUte
 cudaError_t launch_gemm_plain(const CUtensorMap* tm_a, const CUtensorMap* tm_b, int M, int N, int K, float* C,
                               long long ldc, float alpha, int accumulate, int num_sms, int* err, cudaStream_t st);
 
-// attention-backward products finished in the epilogue, bf16 [M, ldo] out (ldo % 8 == 0):
-// mode 1 P = exp2(c acc - v[row]), 2 P^T = exp2(c acc - v[col]), 3 dS = P (acc - v[row]) c,
-// 4 dS^T = P^T (acc - v[col]) c with P / P^T read from pin [M, ldp]
-cudaError_t launch_gemm_attn_bwd(int mode, const CUtensorMap* tm_a, const CUtensorMap* tm_b, int M, int N, int K,
-                                 void* out, long long ldo, float c, const float* v, const void* pin, long long ldp,
-                                 int num_sms, int* err, cudaStream_t st);
-
 // ---- attn_tc.cu (bf16 mode, tcgen05 + TMA) ----
 cudaError_t attn_tc_init();
 // og = softmax(q k^T / sqrt(hd)) v * sigmoid(g); rowamax (optional, pre-zeroed [T]) gets
 // each row's largest |og| as stored (bf16)
-// lse (optional, [B, n_q, L]) gets m + log2(l) per row in the scores' scaled-log2 units, o_raw
-// (optional, fp32 [T, n_q*hd]) the output before the gate; both for the backward
+// lse (optional, [B, n_q, Lp]: row pitch Lp) gets m + log2(l) per row in the scores'
+// scaled-log2 units, o_raw (optional, fp32 [T, n_q*hd]) the output before the gate; both
+// for the backward
 cudaError_t launch_attn_tc(const Fwd& f, const CUtensorMap* tm_q, const CUtensorMap* tm_k, const CUtensorMap* tm_vt,
                            const void* g, void* og, float* rowamax, float* lse, float* o_raw, int num_sms, int* err,
                            cudaStream_t st);
+
+// ---- attn_bwd.cu (flash-style attention backward, tcgen05 + TMA) ----
+cudaError_t attn_bwd_init();
+// dq [B n_q, L, hd], dk and dv [B n_kv, L, hd] (fp32) from d_o (head-major bf16, the
+// gradient of the ungated output), the forward's lse and D = rowsum(d_o o) (both
+// [B n_q, Lp]). Maps (bf16, 128 x 64 boxes, 128-byte swizzle): tm_q / tm_do over
+// [B n_q, L, hd], tm_k / tm_v over [B n_kv, L, hd] (row-major V), tm_qt / tm_dot over
+// [B n_q, hd, L] (pitch Lp), tm_kt over [B n_kv, hd, L] (pitch Lp). Two launches.
+cudaError_t launch_attn_bwd(const Fwd& f, const CUtensorMap* tm_q, const CUtensorMap* tm_do, const CUtensorMap* tm_k,
+                            const CUtensorMap* tm_v, const CUtensorMap* tm_qt, const CUtensorMap* tm_dot,
+                            const CUtensorMap* tm_kt, const float* lse, const float* D, float* dq, float* dk,
+                            float* dv, int* err, cudaStream_t st);
 
 // ---- quant8.cu (e4m3 casts of GEMM operands) ----
 // Scaled e4m3 cast of a bf16 matrix src [R, K] (K % 16 == 0) into codes q [R, K]:
@@ -161,8 +167,10 @@ cudaError_t launch_norm_bwd(const Fwd& f, RowSrc xs, int x_f32, const float* dy,
                             const float* mod_shared, const float* mod_bias, int chunk_shift, int chunk_scale,
                             const void* d_res, int res_f32, float* dx_f32, RowSrc dx_bf16, float* rstd,
                             float* d_mod, float* d_bias, float* d_gain, cudaStream_t st);
-// D[b, h, l] = sum over the head's 128 columns of d_o (bf16, head-major) times o (fp32 [T, n_q*128])
-cudaError_t launch_attn_rowdot(const void* d_o, const float* o, int T, int L, int n_q, float* D, cudaStream_t st);
+// D[b, h, l] (row pitch Lp) = sum over the head's 128 columns of d_o (bf16, head-major)
+// times o (fp32 [T, n_q*128])
+cudaError_t launch_attn_rowdot(const void* d_o, const float* o, int T, int L, int Lp, int n_q, float* D,
+                               cudaStream_t st);
 // output gate backward: d_o (bf16, head-major [B, n_q, L, 128]) and the gate's gradient
 // into d_P columns goff..
 cudaError_t launch_gate_bwd(const float* d_og, const float* o, const void* g, long long T, int L, int n_q, int gate_on,
