@@ -163,8 +163,8 @@ struct krea_dit_block_s {
   float* f_lse = nullptr;
   float* f_D = nullptr;
   void *bw_out = nullptr, *wT_down = nullptr, *wT_gu = nullptr, *wT_o = nullptr, *wT_qkvg = nullptr;
-  float *f_td = nullptr, *f_hmid = nullptr, *f_a = nullptr, *f_u = nullptr, *f_dn = nullptr, *f_dh1 = nullptr,
-        *f_dog = nullptr, *f_o = nullptr, *f_raw = nullptr, *f_dq = nullptr, *f_dk = nullptr, *f_dv = nullptr,
+  float *f_td = nullptr, *f_fa = nullptr, *f_a = nullptr, *f_u = nullptr, *f_dn = nullptr, *f_dh1 = nullptr,
+        *f_o = nullptr, *f_raw = nullptr, *f_dq = nullptr, *f_dk = nullptr, *f_dv = nullptr,
         *f_rstd = nullptr;
   void *b_dfm = nullptr, *b_dau = nullptr, *b_dfa = nullptr, *b_do = nullptr, *b_dP = nullptr, *b_vrow = nullptr,
        *b_kT = nullptr, *b_qT = nullptr, *b_doT = nullptr;
@@ -516,7 +516,11 @@ int forward_impl(krea_dit_block_t h, const void* x_img, const void* x_txt, const
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const RowSrc xsrc{x_txt, x_img, x_joint};
   const RowSrc h1src{nullptr, nullptr, h->h1};
-  const QkvgDst dst{h->q, h->k, h->vt, h->g, w->q_norm_w, w->k_norm_w, h->rope};
+  QkvgDst dst{h->q, h->k, h->vt, h->g, w->q_norm_w, w->k_norm_w, h->rope};
+  if (h->bw_stats) {  // the backward's recomputed forward keeps its pre-activations
+    dst.raw = h->f_raw;
+    dst.ldr = h->n_qkvg;
+  }
   const int nqhd = c.n_q * c.head_dim;
   cudaError_t e = cudaSuccess;
 #define KD_RUN(slot, expr)                                 \
@@ -559,18 +563,18 @@ int forward_impl(krea_dit_block_t h, const void* x_img, const void* x_txt, const
     KD_RUN(S_ATTN, kd::launch_attn_tc(f, &tm_q, &tm_k, &tm_vt, h->g, h->og, h->am_og, nullptr, nullptr, sms, h->err, st));
     KD_RUN(S_QUANT_OG, kd::launch_quant_e4m3(h->og, f.T, nqhd, h->am_og, per_row, h->og8, h->dq_og, sms, st));
     KD_RUN(S_OPROJ_TC, kd::launch_gemm_resid_attn(f, &tm_og8, &tm_wo, nqhd, xsrc, t_emb, w->mod_bias,
-                                                  static_cast<float*>(h->h1), &dq_o, sms, h->err, st));
+                                                  static_cast<float*>(h->h1), &dq_o, nullptr, sms, h->err, st));
     if (!per_row)
       KD_RUN(S_NORM2_AMAX, kd::launch_norm_modulate(kd::NormIO::F32_BF16, f, h1src, w->norm2_w, t_emb, w->mod_bias, 3,
                                                     4, nullptr, sms, st, &q_amax2));
     KD_RUN(S_NORM2, kd::launch_norm_modulate(kd::NormIO::F32_BF16, f, h1src, w->norm2_w, t_emb, w->mod_bias, 3, 4,
                                              nullptr, sms, st, &q_hn));
-    KD_RUN(S_UPGATE_TC, kd::launch_gemm_swiglu(f, &tm_hn8, &tm_wgate, &tm_wup, h->hmid, h->am_hmid, &dq_ff, sms,
-                                               h->err, st));
+    KD_RUN(S_UPGATE_TC, kd::launch_gemm_swiglu(f, &tm_hn8, &tm_wgate, &tm_wup, h->hmid, h->am_hmid, &dq_ff, nullptr,
+                                               nullptr, sms, h->err, st));
     KD_RUN(S_QUANT_HMID,
            kd::launch_quant_e4m3(h->hmid, f.T, c.ffn, h->am_hmid, per_row, h->hmid8, h->dq_hmid, sms, st));
     KD_RUN(S_DOWN_TC, kd::launch_gemm_resid_mlp(f, &tm_hmid8, &tm_wdown, c.ffn, static_cast<const float*>(h->h1),
-                                                t_emb, w->mod_bias, out, &dq_down, sms, h->err, st));
+                                                t_emb, w->mod_bias, out, &dq_down, nullptr, sms, h->err, st));
   } else if (h->bf16) {
     CUtensorMap tm_xn, tm_wqkvg, tm_og, tm_wo, tm_hn, tm_wgate, tm_wup, tm_hmid, tm_wdown, tm_q, tm_k, tm_vt;
     const uint64_t T = static_cast<uint64_t>(f.T);
@@ -593,13 +597,16 @@ int forward_impl(krea_dit_block_t h, const void* x_img, const void* x_txt, const
     KD_RUN(S_ATTN, kd::launch_attn_tc(f, &tm_q, &tm_k, &tm_vt, h->g, h->og, nullptr, h->bw_stats ? h->f_lse : nullptr,
                                         h->bw_stats ? h->f_o : nullptr, sms, h->err, st));
     KD_RUN(S_OPROJ_TC, kd::launch_gemm_resid_attn(f, &tm_og, &tm_wo, nqhd, xsrc, t_emb, w->mod_bias,
-                                                  static_cast<float*>(h->h1), nullptr, sms, h->err, st));
+                                                  static_cast<float*>(h->h1), nullptr,
+                                                  h->bw_stats ? h->f_fa : nullptr, sms, h->err, st));
     KD_RUN(S_NORM2, kd::launch_norm_modulate(kd::NormIO::F32_BF16, f, h1src, w->norm2_w, t_emb, w->mod_bias, 3, 4,
                                              h->hn, sms, st));
-    KD_RUN(S_UPGATE_TC, kd::launch_gemm_swiglu(f, &tm_hn, &tm_wgate, &tm_wup, h->hmid, nullptr, nullptr, sms,
-                                               h->err, st));
+    KD_RUN(S_UPGATE_TC, kd::launch_gemm_swiglu(f, &tm_hn, &tm_wgate, &tm_wup, h->hmid, nullptr, nullptr,
+                                               h->bw_stats ? h->f_a : nullptr, h->bw_stats ? h->f_u : nullptr,
+                                               sms, h->err, st));
     KD_RUN(S_DOWN_TC, kd::launch_gemm_resid_mlp(f, &tm_hmid, &tm_wdown, c.ffn, static_cast<const float*>(h->h1),
-                                                t_emb, w->mod_bias, out, nullptr, sms, h->err, st));
+                                                t_emb, w->mod_bias, out, nullptr, h->bw_stats ? h->f_td : nullptr, sms,
+                                                h->err, st));
   } else {
     const int T = f.T;
     const float* wq = static_cast<const float*>(w->w_qkvg);
@@ -773,12 +780,11 @@ int krea_dit_block_enable_backward(krea_dit_block_t h) {
       {&h->wT_o, nq * d * 2},
       {&h->wT_qkvg, d * nqkvg * 2},
       {reinterpret_cast<void**>(&h->f_td), T * d * 4},
-      {reinterpret_cast<void**>(&h->f_hmid), T * F * 4},
+      {reinterpret_cast<void**>(&h->f_fa), T * d * 4},
       {reinterpret_cast<void**>(&h->f_a), T * F * 4},
       {reinterpret_cast<void**>(&h->f_u), T * F * 4},
       {reinterpret_cast<void**>(&h->f_dn), T * d * 4},
       {reinterpret_cast<void**>(&h->f_dh1), T * d * 4},
-      {reinterpret_cast<void**>(&h->f_dog), T * nq * 4},
       {reinterpret_cast<void**>(&h->f_o), T * nq * 4},
       {reinterpret_cast<void**>(&h->f_raw), T * nqkvg * 4},
       {reinterpret_cast<void**>(&h->f_dq), T * nq * 4},
@@ -892,16 +898,17 @@ int krea_dit_block_backward(krea_dit_block_t h, const void* x_img, const void* x
   transpose(w->w_o, d, nq, nq, 0, h->wT_o, d, d, 0, 1);                        // [nq, d]
   transpose(w->w_qkvg, nqkvg, d, d, 0, h->wT_qkvg, nqkvg, nqkvg, 0, 1);        // [d, nqkvg]
 
-  // ---- MLP residual: out = h1 + gate_m * fm,  fm = hmid W_down^T
-  gemm(h->hmid, T, F, w->w_down, d, F, F, h->f_td, d, T, d, 1.0f, 0);
+  // ---- MLP residual: out = h1 + gate_m * fm,  fm = hmid W_down^T (kept by the forward in f_td)
   run(S_BWD_POINTWISE, [&] {
     return kd::launch_gated_bwd(f, d_out, 0, h->f_td, t_emb, w->mod_bias, 5, h->b_dfm, d_mod, d_bias, st);
   });
-  gemm(h->b_dfm, T, d, h->wT_down, F, d, d, h->f_hmid, F, T, F, 1.0f, 0);      // d_hmid
-  // ---- SwiGLU (pre-activations recomputed)
-  gemm(h->hn, T, d, w->w_gate, F, d, d, h->f_a, F, T, F, 1.0f, 0);
-  gemm(h->hn, T, d, w->w_up, F, d, d, h->f_u, F, T, F, 1.0f, 0);
-  run(S_BWD_POINTWISE, [&] { return kd::launch_swiglu_bwd(h->f_hmid, h->f_a, h->f_u, T, F, h->b_dau, sms, st); });
+  // ---- d_hmid = d_fm W_down and the SwiGLU backward in its epilogue (a, u kept by the forward)
+  run(S_BWD_GEMM, [&]() -> cudaError_t {
+    CUtensorMap ta, tb;
+    if (!encode_2d(&ta, h->b_dfm, d, T, d, 64, 128) || !encode_2d(&tb, h->wT_down, d, F, d, 64, 128))
+      return cudaErrorInvalidValue;
+    return kd::launch_gemm_swiglu_bwd(&ta, &tb, T, F, d, h->f_a, h->f_u, h->b_dau, sms, h->err, st);
+  });
   gemm(h->b_dau, T, 2LL * F, h->wT_gu, d, 2LL * F, 2 * F, h->f_dn, d, T, d, 1.0f, 0);  // d_hn
   // ---- norm2 + modulation; the residual adds d_out
   const RowSrc h1src{nullptr, nullptr, h->h1};
@@ -909,21 +916,22 @@ int krea_dit_block_backward(krea_dit_block_t h, const void* x_img, const void* x
     return kd::launch_norm_bwd(f, h1src, 1, h->f_dn, w->norm2_w, t_emb, w->mod_bias, 3, 4, d_out, 0, h->f_dh1,
                                RowSrc{}, h->f_rstd, d_mod, d_bias, g->d_norm2_w, st);
   });
-  // ---- attention residual: h1 = x + gate_a * fa,  fa = og W_o^T
-  gemm(h->og, T, nq, w->w_o, d, nq, nq, h->f_td, d, T, d, 1.0f, 0);
+  // ---- attention residual: h1 = x + gate_a * fa,  fa = og W_o^T (kept by the forward)
   run(S_BWD_POINTWISE, [&] {
-    return kd::launch_gated_bwd(f, h->f_dh1, 1, h->f_td, t_emb, w->mod_bias, 2, h->b_dfa, d_mod, d_bias, st);
+    return kd::launch_gated_bwd(f, h->f_dh1, 1, h->f_fa, t_emb, w->mod_bias, 2, h->b_dfa, d_mod, d_bias, st);
   });
-  gemm(h->b_dfa, T, d, h->wT_o, nq, d, d, h->f_dog, nq, T, nq, 1.0f, 0);       // d_og
+  // d_og = d_fa W_o, with the gate backward and D = rowsum(d_o o) in its epilogue
+  run(S_BWD_GEMM, [&]() -> cudaError_t {
+    CUtensorMap ta, tb;
+    if (!encode_2d(&ta, h->b_dfa, d, T, d, 64, 128) || !encode_2d(&tb, h->wT_o, d, nq, d, 64, 128))
+      return cudaErrorInvalidValue;
+    return kd::launch_gemm_gate_bwd(f, &ta, &tb, d, h->f_o, h->g, h->b_do, h->b_dP, nqkvg, nq + 2 * nkv, h->f_D, sms,
+                                    h->err, st);
+  });
   // ---- attention: the forward left each row's log2 normaliser (lse) and the ungated
   // output o; two flash-style kernels recompute P and dP tile by tile in TMEM (no L x L
   // array in memory) and give dQ, dK, dV in fp32.
   const long long qh = static_cast<long long>(L) * hd;  // one head of Q / K (elements)
-  run(S_BWD_POINTWISE, [&] {
-    return kd::launch_gate_bwd(h->f_dog, h->f_o, h->g, T, L, c.n_q, c.gate_on, h->b_do, h->b_dP, nqkvg,
-                               nq + 2 * nkv, sms, st);
-  });
-  run(S_BWD_POINTWISE, [&] { return kd::launch_attn_rowdot(h->b_do, h->f_o, T, L, f.Lp, c.n_q, h->f_D, st); });
   // head-dim-major copies (B operands of dQ, dK, dV) and row-major V [B n_kv, L, hd]
   transpose(h->vt, hd, L, f.Lp, static_cast<long long>(hd) * f.Lp, h->b_vrow, hd, hd, qh, B * c.n_kv);
   transpose(h->k, L, hd, hd, qh, h->b_kT, Lp, Lp, static_cast<long long>(hd) * Lp, B * c.n_kv);
@@ -940,8 +948,7 @@ int krea_dit_block_backward(krea_dit_block_t h, const void* x_img, const void* x
     return kd::launch_attn_bwd(f, &tm_q, &tm_do, &tm_k, &tm_v, &tm_qt, &tm_dot, &tm_kt, h->f_lse, h->f_D, h->f_dq,
                                h->f_dk, h->f_dv, h->err, st);
   });
-  // ---- QK-norm + RoPE and V into d_P (raw projections recomputed in fp32)
-  gemm(h->xn, T, d, w->w_qkvg, nqkvg, d, d, h->f_raw, nqkvg, T, nqkvg, 1.0f, 0);
+  // ---- QK-norm + RoPE and V into d_P (the Q, K projections before the norm kept by the forward)
   run(S_BWD_POINTWISE, [&] {
     return kd::launch_qkv_bwd(f, h->f_raw, nqkvg, h->f_dq, h->f_dk, h->f_dv, w->q_norm_w, w->k_norm_w, h->rope,
                               h->b_dP, nqkvg, g->d_q_norm_w, g->d_k_norm_w, st);

@@ -11,24 +11,60 @@
 namespace kd {
 namespace {
 
-constexpr int TB = 32;  // transpose tile
+constexpr int TB = 64;  // transpose tile (64 x 64 bf16), 256 threads
 
-// dst[z][c, r] = src[z][r, c] for r < R, 0 for R <= r < Rp (bf16).
-__global__ void transpose_kernel(const bf16* __restrict__ src, int R, int C, long long lds, long long src_bs,
-                                 bf16* __restrict__ dst, int Rp, long long ldd, long long dst_bs) {
-  __shared__ bf16 tile[TB][TB + 2];
-  const bf16* s = src + blockIdx.z * src_bs;
-  bf16* d = dst + blockIdx.z * dst_bs;
+// dst[z][c, r] = src[z][r, c] for r < R, 0 for R <= r < Rp (bf16). Loads and stores move
+// 8 elements (16 bytes) per thread where the row lies inside the matrix and the address is
+// 16-byte aligned, else element by element.
+__global__ void __launch_bounds__(256) transpose_kernel(const bf16* __restrict__ src, int R, int C, long long lds,
+                                                        long long src_bs, bf16* __restrict__ dst, int Rp,
+                                                        long long ldd, long long dst_bs) {
+  __shared__ uint16_t tile[TB][TB + 2];  // +2: a column read walks the banks
+  const uint16_t* s = reinterpret_cast<const uint16_t*>(src) + blockIdx.z * src_bs;
+  uint16_t* d = reinterpret_cast<uint16_t*>(dst) + blockIdx.z * dst_bs;
   const int r0 = blockIdx.y * TB, c0 = blockIdx.x * TB;
-  const int tx = threadIdx.x, ty = threadIdx.y;  // 32 x 8
-  for (int k = ty; k < TB; k += 8) {
-    const int r = r0 + k, c = c0 + tx;
-    tile[k][tx] = (r < R && c < C) ? s[r * lds + c] : __float2bfloat16_rn(0.0f);
+  const int t = threadIdx.x, chunk = t & 7;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int k = (t >> 3) + 32 * h;  // tile row
+    const int r = r0 + k, c = c0 + 8 * chunk;
+    uint16_t v[8];
+    const uint16_t* p = s + static_cast<long long>(r) * lds + c;
+    if (r < R && c + 8 <= C && (reinterpret_cast<uintptr_t>(p) & 15) == 0) {
+      const uint4 u = *reinterpret_cast<const uint4*>(p);
+      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        v[2 * i] = static_cast<uint16_t>(w[i] & 0xFFFFu);
+        v[2 * i + 1] = static_cast<uint16_t>(w[i] >> 16);
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v[i] = (r < R && c + i < C) ? p[i] : static_cast<uint16_t>(0);
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) tile[k][8 * chunk + i] = v[i];
   }
   __syncthreads();
-  for (int k = ty; k < TB; k += 8) {
-    const int c = c0 + k, r = r0 + tx;
-    if (c < C && r < Rp) d[c * ldd + r] = tile[tx][k];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int k = (t >> 3) + 32 * h;  // tile column = destination row
+    const int c = c0 + k, r = r0 + 8 * chunk;
+    if (c >= C) continue;
+    uint16_t v[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = tile[8 * chunk + i][k];
+    uint16_t* q = d + static_cast<long long>(c) * ldd + r;
+    if (r + 8 <= Rp && (reinterpret_cast<uintptr_t>(q) & 15) == 0) {
+      *reinterpret_cast<uint4*>(q) = make_uint4(v[0] | (static_cast<uint32_t>(v[1]) << 16),
+                                                v[2] | (static_cast<uint32_t>(v[3]) << 16),
+                                                v[4] | (static_cast<uint32_t>(v[5]) << 16),
+                                                v[6] | (static_cast<uint32_t>(v[7]) << 16));
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        if (r + i < Rp) q[i] = v[i];
+    }
   }
 }
 
@@ -59,22 +95,6 @@ __global__ void gated_bwd_kernel(Fwd f, const void* __restrict__ dy, int dy_f32,
   atomicAdd(&d_bias[chunk * f.d + c], acc);
 }
 
-// SwiGLU, backward: hmid = silu(a) u. d_au[t, 0:F] = d_hmid u silu'(a), d_au[t, F:2F] =
-// d_hmid silu(a), silu'(a) = sigma(a) (1 + a (1 - sigma(a))).
-__global__ void swiglu_bwd_kernel(const float* __restrict__ d_hmid, const float* __restrict__ a,
-                                  const float* __restrict__ u, long long T, int F, bf16* __restrict__ d_au) {
-  const long long n = T * F;
-  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n;
-       i += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const long long t = i / F;
-    const int j = static_cast<int>(i - t * F);
-    const float av = a[i], sg = 1.0f / (1.0f + __expf(-av));
-    const float dh = d_hmid[i];
-    d_au[t * 2 * F + j] = __float2bfloat16_rn(dh * u[i] * sg * (1.0f + av * (1.0f - sg)));
-    d_au[t * 2 * F + F + j] = __float2bfloat16_rn(dh * av * sg);
-  }
-}
-
 // block-wide sum (blockDim.x multiple of 32, <= 1024)
 __device__ __forceinline__ float block_sum(float v, float* red) {
   v = warp_sum(v);
@@ -91,42 +111,60 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
 // r = (mean(x^2) + eps)^(-1/2). dx = r dn - r^3 x mean(dn x) + d_res, dn = dy (1 + w)(1 + scale).
 // One block per row; writes r to rstd[t] for the column pass. dx goes to a joint fp32 buffer
 // (dx_f32) or, as the storage dtype, to split text / image buffers (dx_src).
-__global__ void norm_bwd_rows_kernel(Fwd f, RowSrc xs, int x_f32, const float* __restrict__ dy,
-                                     const float* __restrict__ gain_w, const float* __restrict__ mod_shared,
-                                     const float* __restrict__ mod_bias, int chunk_scale, const void* __restrict__ d_res,
-                                     int res_f32, float* __restrict__ dx_f32, RowSrc dx_bf16,
-                                     float* __restrict__ rstd) {
+__device__ __forceinline__ float4 ld4_any(const void* p, long long i, int f32) {
+  if (f32) return *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(p) + i);
+  const uint2 u = *reinterpret_cast<const uint2*>(reinterpret_cast<const bf16*>(p) + i);
+  const float2 a = unpack_bf16x2(u.x), b = unpack_bf16x2(u.y);
+  return make_float4(a.x, a.y, b.x, b.y);
+}
+
+__global__ void __launch_bounds__(256) norm_bwd_rows_kernel(Fwd f, RowSrc xs, int x_f32, const float* __restrict__ dy,
+                                                            const float* __restrict__ gain_w,
+                                                            const float* __restrict__ mod_shared,
+                                                            const float* __restrict__ mod_bias, int chunk_scale,
+                                                            const void* __restrict__ d_res, int res_f32,
+                                                            float* __restrict__ dx_f32, RowSrc dx_bf16,
+                                                            float* __restrict__ rstd) {
   __shared__ float red[32];
   const int t = blockIdx.x;
   const int b = t / f.L;
-  const int d = f.d;
+  const int d = f.d;  // a multiple of 64: four columns per access
   const void* x = x_f32 ? static_cast<const void*>(row_src_ptr<float>(xs, t, f.L, f.n_txt, f.n_img, d))
                         : static_cast<const void*>(row_src_ptr<bf16>(xs, t, f.L, f.n_txt, f.n_img, d));
+  const float* ms = mod_shared + (static_cast<size_t>(b) * 6 + chunk_scale) * d;
+  const float* mb = mod_bias + static_cast<size_t>(chunk_scale) * d;
+  const float* dyr = dy + static_cast<long long>(t) * d;
+  auto coef = [&](int c) {  // (1 + w)(1 + scale) for columns c .. c+3
+    const float4 w = *reinterpret_cast<const float4*>(gain_w + c);
+    const float4 s0 = *reinterpret_cast<const float4*>(ms + c);
+    const float4 s1 = *reinterpret_cast<const float4*>(mb + c);
+    return make_float4((1.0f + w.x) * (1.0f + s0.x + s1.x), (1.0f + w.y) * (1.0f + s0.y + s1.y),
+                       (1.0f + w.z) * (1.0f + s0.z + s1.z), (1.0f + w.w) * (1.0f + s0.w + s1.w));
+  };
   float ss = 0.0f, sdx = 0.0f;
-  for (int c = threadIdx.x; c < d; c += blockDim.x) {
-    const float xv = ld_any(x, c, x_f32);
-    const float A = (1.0f + gain_w[c]) * (1.0f + mod_shared[(b * 6 + chunk_scale) * d + c] +
-                                          mod_bias[chunk_scale * d + c]);
-    ss = fmaf(xv, xv, ss);
-    sdx = fmaf(dy[static_cast<long long>(t) * d + c] * A, xv, sdx);
+  for (int c = 4 * threadIdx.x; c < d; c += 4 * blockDim.x) {
+    const float4 xv = ld4_any(x, c, x_f32);
+    const float4 A = coef(c);
+    const float4 g = *reinterpret_cast<const float4*>(dyr + c);
+    ss += xv.x * xv.x + xv.y * xv.y + xv.z * xv.z + xv.w * xv.w;
+    sdx += g.x * A.x * xv.x + g.y * A.y * xv.y + g.z * A.z * xv.z + g.w * A.w * xv.w;
   }
   ss = block_sum(ss, red);
   sdx = block_sum(sdx, red);
   const float r = rsqrtf(ss / d + f.eps);
   const float k = r * r * r * (sdx / d);
   if (threadIdx.x == 0) rstd[t] = r;
-  for (int c = threadIdx.x; c < d; c += blockDim.x) {
+  bf16* ob = dx_f32 ? nullptr : const_cast<bf16*>(row_src_ptr<bf16>(dx_bf16, t, f.L, f.n_txt, f.n_img, d));
+  for (int c = 4 * threadIdx.x; c < d; c += 4 * blockDim.x) {
     const long long i = static_cast<long long>(t) * d + c;
-    const float xv = ld_any(x, c, x_f32);
-    const float A = (1.0f + gain_w[c]) * (1.0f + mod_shared[(b * 6 + chunk_scale) * d + c] +
-                                          mod_bias[chunk_scale * d + c]);
-    const float g = r * dy[i] * A - k * xv + ld_any(d_res, i, res_f32);
-    if (dx_f32) {
-      dx_f32[i] = g;
-    } else {
-      bf16* o = const_cast<bf16*>(row_src_ptr<bf16>(dx_bf16, t, f.L, f.n_txt, f.n_img, d));
-      o[c] = __float2bfloat16_rn(g);
-    }
+    const float4 xv = ld4_any(x, c, x_f32);
+    const float4 A = coef(c);
+    const float4 g = *reinterpret_cast<const float4*>(dyr + c);
+    const float4 rs = ld4_any(d_res, i, res_f32);
+    const float4 o = make_float4(r * g.x * A.x - k * xv.x + rs.x, r * g.y * A.y - k * xv.y + rs.y,
+                                 r * g.z * A.z - k * xv.z + rs.z, r * g.w * A.w - k * xv.w + rs.w);
+    if (dx_f32) *reinterpret_cast<float4*>(dx_f32 + i) = o;
+    else *reinterpret_cast<uint2*>(ob + c) = make_uint2(pack_bf16x2(o.x, o.y), pack_bf16x2(o.z, o.w));
   }
 }
 
@@ -159,115 +197,96 @@ __global__ void norm_bwd_cols_kernel(Fwd f, RowSrc xs, int x_f32, const float* _
   atomicAdd(&d_gain[c], s_dyn * (1.0f + scale));
 }
 
-// Output gate, backward: og = o sigmoid(g). d_o = d_og sigmoid(g), stored head-major (bf16
-// [B, n_q, L, 128], so that a KV group's heads are one contiguous block of rows); the
-// gate's gradient d_og o sigmoid(g)(1 - sigmoid(g)) goes to d_P's g columns (bf16).
-__global__ void gate_bwd_kernel(const float* __restrict__ d_og, const float* __restrict__ o,
-                                const bf16* __restrict__ g, long long T, int L, int n_q, int gate_on,
-                                bf16* __restrict__ d_o, bf16* __restrict__ d_P, int ldp, int goff) {
-  const int nq = n_q * 128;
-  const long long n = T * nq;
-  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n;
-       i += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const long long t = i / nq;
-    const int col = static_cast<int>(i - t * nq);
-    const long long b = t / L, l = t - b * L;
-    const long long hm = ((b * n_q + (col >> 7)) * L + l) * 128 + (col & 127);
-    const float dv = d_og[i];
-    if (gate_on) {
-      const float sg = 1.0f / (1.0f + __expf(-__bfloat162float(g[i])));
-      d_o[hm] = __float2bfloat16_rn(dv * sg);
-      d_P[t * ldp + goff + col] = __float2bfloat16_rn(dv * o[i] * sg * (1.0f - sg));
-    } else {
-      d_o[hm] = __float2bfloat16_rn(dv);
-    }
-  }
-}
-
-// QK-RMSNorm + RoPE, backward, and the V gradient, into d_P (bf16 [T, ldp]). Block = one
-// head slot (blockIdx.y: q heads, then k heads, then v heads) over a chunk of rows;
-// thread j = head-dim element. For q / k: d_n = rotation by -angle of d (fp32 gradient
-// of the rotated, normalised head), dx = r dn (1 + w) - r^3 x mean(dn (1 + w) x) with x the
-// raw projection (fp32 [T, ldr]) and r its rstd over hd; the gain's gradient
-// sum d_n x r is added to d_gain. For v: d_P takes d_v.
-__global__ void qkv_bwd_kernel(Fwd f, const float* __restrict__ raw, int ldr, const float* __restrict__ dq,
-                               const float* __restrict__ dk, const float* __restrict__ dv,
-                               const float* __restrict__ q_norm_w, const float* __restrict__ k_norm_w,
-                               const float2* __restrict__ rope, int rows_per, bf16* __restrict__ d_P, int ldp,
-                               float* __restrict__ d_qw, float* __restrict__ d_kw) {
-  __shared__ float red[32];
-  const int HD = 128;
-  const int j = threadIdx.x;  // 0..127
+// QK-RMSNorm + RoPE, backward, and the V gradient, into d_P (bf16 [T, ldp]). Block = 8
+// warps over a chunk of rows of one head slot (blockIdx.y: q heads, then k heads, then v
+// heads); a warp takes one row at a time, lane i the head-dim elements 4i .. 4i+3 (two
+// rotation pairs). For q / k: d_n = rotation by -angle of d (fp32 gradient of the
+// rotated, normalised head), dx = r dn (1 + w) - r^3 x mean(dn (1 + w) x) with x the raw
+// projection (fp32 [T, ldr]) and r its rstd over hd; the gain's gradient sum d_n x r is
+// added to d_gain. For v: d_P takes d_v.
+__global__ void __launch_bounds__(256) qkv_bwd_kernel(Fwd f, const float* __restrict__ raw, int ldr,
+                                                      const float* __restrict__ dq, const float* __restrict__ dk,
+                                                      const float* __restrict__ dv,
+                                                      const float* __restrict__ q_norm_w,
+                                                      const float* __restrict__ k_norm_w,
+                                                      const float2* __restrict__ rope, int rows_per,
+                                                      bf16* __restrict__ d_P, int ldp, float* __restrict__ d_qw,
+                                                      float* __restrict__ d_kw) {
+  constexpr int HD = 128;
+  __shared__ float red[8][HD];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int slot = blockIdx.y;
   const int kind = slot < f.n_q ? 0 : (slot < f.n_q + f.n_kv ? 1 : 2);
   const int head = kind == 0 ? slot : (kind == 1 ? slot - f.n_q : slot - f.n_q - f.n_kv);
   const int nh = kind == 0 ? f.n_q : f.n_kv;
   const float* dsrc = kind == 0 ? dq : (kind == 1 ? dk : dv);
-  const int col = (kind == 0 ? 0 : (kind == 1 ? f.n_q * HD : (f.n_q + f.n_kv) * HD)) + head * HD + j;
-  const float wj = kind == 0 ? q_norm_w[j] : (kind == 1 ? k_norm_w[j] : 0.0f);
+  const int j0 = 4 * lane;
+  const int col = (kind == 0 ? 0 : (kind == 1 ? f.n_q * HD : (f.n_q + f.n_kv) * HD)) + head * HD + j0;
+  float w1[4] = {1.f, 1.f, 1.f, 1.f};
+  if (kind < 2) {
+    const float4 w4 = *reinterpret_cast<const float4*>((kind == 0 ? q_norm_w : k_norm_w) + j0);
+    w1[0] = 1.0f + w4.x; w1[1] = 1.0f + w4.y; w1[2] = 1.0f + w4.z; w1[3] = 1.0f + w4.w;
+  }
   const int t0 = blockIdx.x * rows_per, t1 = min(t0 + rows_per, f.T);
-  float gacc = 0.0f;
-  for (int t = t0; t < t1; ++t) {
+  float gacc[4] = {0.f, 0.f, 0.f, 0.f};
+  for (int t = t0 + warp; t < t1; t += 8) {
     const int b = t / f.L, l = t - b * f.L;
-    const float g = dsrc[((static_cast<long long>(b) * nh + head) * f.L + l) * HD + j];
+    const float4 g4 = *reinterpret_cast<const float4*>(dsrc + ((static_cast<long long>(b) * nh + head) * f.L + l) * HD + j0);
+    bf16* out = d_P + static_cast<long long>(t) * ldp + col;
     if (kind == 2) {
-      d_P[static_cast<long long>(t) * ldp + col] = __float2bfloat16_rn(g);
+      *reinterpret_cast<uint2*>(out) = make_uint2(pack_bf16x2(g4.x, g4.y), pack_bf16x2(g4.z, g4.w));
       continue;
     }
-    // rotation by the negative angle: pair (2p, 2p+1) of this element
-    float dn = g;
-    if (l >= f.n_txt) {
+    float dn[4] = {g4.x, g4.y, g4.z, g4.w};
+    if (l >= f.n_txt) {  // rotation by the negative angle, pairs (j0, j0+1) and (j0+2, j0+3)
       const int n = l - f.n_txt, pr = n / f.img_w, pc = n - pr * f.img_w;
-      const float2 cs = rope[(j < 64 ? pr : pc) * (HD / 4) + ((j & 63) >> 1)];
-      const float other = __shfl_xor_sync(0xffffffffu, g, 1);
-      dn = (j & 1) == 0 ? g * cs.x + other * cs.y : -other * cs.y + g * cs.x;
+      const float2* tab = rope + (j0 < 64 ? pr : pc) * (HD / 4) + ((j0 & 63) >> 1);
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const float2 cs = tab[e];
+        const float a = dn[2 * e], bb = dn[2 * e + 1];
+        dn[2 * e] = a * cs.x + bb * cs.y;
+        dn[2 * e + 1] = -a * cs.y + bb * cs.x;
+      }
     }
-    const float x = raw[static_cast<long long>(t) * ldr + col];
-    const float ss = block_sum(x * x, red);
+    const float4 x4 = *reinterpret_cast<const float4*>(raw + static_cast<long long>(t) * ldr + col);
+    const float x[4] = {x4.x, x4.y, x4.z, x4.w};
+    const float ss = warp_sum(x[0] * x[0] + x[1] * x[1] + x[2] * x[2] + x[3] * x[3]);
     const float r = rsqrtf(ss / HD + f.eps);
-    const float dnw = dn * (1.0f + wj);
-    const float m = block_sum(dnw * x, red) / HD;
-    gacc = fmaf(dn, x * r, gacc);
-    d_P[static_cast<long long>(t) * ldp + col] = __float2bfloat16_rn(r * dnw - r * r * r * x * m);
+    float dnw[4], md = 0.0f;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      dnw[e] = dn[e] * w1[e];
+      md = fmaf(dnw[e], x[e], md);
+      gacc[e] = fmaf(dn[e], x[e] * r, gacc[e]);
+    }
+    const float m = warp_sum(md) / HD;
+    const float r3m = r * r * r * m;
+    float o[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) o[e] = r * dnw[e] - r3m * x[e];
+    *reinterpret_cast<uint2*>(out) = make_uint2(pack_bf16x2(o[0], o[1]), pack_bf16x2(o[2], o[3]));
   }
-  if (kind < 2) atomicAdd(kind == 0 ? &d_qw[j] : &d_kw[j], gacc);
-}
-
-// D[b, h, l] = sum_j d_o[b, h, l, j] o[t, h hd + j] (t = b L + l, hd = 128; d_o head-major):
-// the row term of the softmax gradient, rowsum(P dP) = rowsum(dO O). One warp per (row, head).
-__global__ void attn_rowdot_kernel(const bf16* __restrict__ d_o, const float* __restrict__ o, int T, int L, int Lp,
-                                   int n_q, float* __restrict__ D) {
-  const long long wid = (blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  if (wid >= static_cast<long long>(T) * n_q) return;
-  const int t = static_cast<int>(wid / n_q), h = static_cast<int>(wid - static_cast<long long>(t) * n_q);
-  const int b = t / L, l = t - b * L;
-  const long long base = static_cast<long long>(t) * n_q * 128 + h * 128 + lane * 4;
-  const long long hm = ((static_cast<long long>(b) * n_q + h) * L + l) * 128 + lane * 4;
-  const uint2 u = *reinterpret_cast<const uint2*>(d_o + hm);
-  const float4 ov = *reinterpret_cast<const float4*>(o + base);
-  const float2 a = unpack_bf16x2(u.x), b2 = unpack_bf16x2(u.y);
-  float s = a.x * ov.x + a.y * ov.y + b2.x * ov.z + b2.y * ov.w;
-  s = warp_sum(s);
-  if (lane == 0) D[(static_cast<long long>(b) * n_q + h) * Lp + l] = s;
+  if (kind < 2) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) red[warp][j0 + e] = gacc[e];
+    __syncthreads();
+    if (threadIdx.x < HD) {
+      float s = 0.0f;
+#pragma unroll
+      for (int w = 0; w < 8; ++w) s += red[w][threadIdx.x];
+      atomicAdd(kind == 0 ? &d_qw[threadIdx.x] : &d_kw[threadIdx.x], s);
+    }
+  }
 }
 
 }  // namespace
 
 // ------------------------------------------------------------------ launchers
-cudaError_t launch_attn_rowdot(const void* d_o, const float* o, int T, int L, int Lp, int n_q, float* D,
-                               cudaStream_t st) {
-  const long long warps = static_cast<long long>(T) * n_q;
-  if (warps == 0) return cudaSuccess;
-  const long long blocks = (warps * 32 + 255) / 256;
-  attn_rowdot_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(reinterpret_cast<const bf16*>(d_o), o, T, L, Lp,
-                                                                   n_q, D);
-  return cudaGetLastError();
-}
 cudaError_t launch_transpose_bf16(const void* src, int R, int C, long long lds, long long src_bs, void* dst, int Rp,
                                   long long ldd, long long dst_bs, int batch, cudaStream_t st) {
   if (R <= 0 || C <= 0 || batch <= 0) return cudaSuccess;
-  dim3 grid((C + TB - 1) / TB, (Rp + TB - 1) / TB, batch), block(TB, 8);
+  dim3 grid((C + TB - 1) / TB, (Rp + TB - 1) / TB, batch), block(256);
   transpose_kernel<<<grid, block, 0, st>>>(reinterpret_cast<const bf16*>(src), R, C, lds, src_bs,
                                            reinterpret_cast<bf16*>(dst), Rp, ldd, dst_bs);
   return cudaGetLastError();
@@ -280,12 +299,6 @@ cudaError_t launch_gated_bwd(const Fwd& f, const void* dy, int dy_f32, const flo
   dim3 grid((f.d + 255) / 256, (f.L + rows_per - 1) / rows_per, f.B);
   gated_bwd_kernel<<<grid, 256, 0, st>>>(f, dy, dy_f32, fv, mod_shared, mod_bias, chunk, rows_per,
                                          reinterpret_cast<bf16*>(d_f), d_mod, d_bias);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_swiglu_bwd(const float* d_hmid, const float* a, const float* u, long long T, int F, void* d_au,
-                              int num_sms, cudaStream_t st) {
-  swiglu_bwd_kernel<<<num_sms * 8, 256, 0, st>>>(d_hmid, a, u, T, F, reinterpret_cast<bf16*>(d_au));
   return cudaGetLastError();
 }
 
@@ -303,20 +316,13 @@ cudaError_t launch_norm_bwd(const Fwd& f, RowSrc xs, int x_f32, const float* dy,
   return cudaGetLastError();
 }
 
-cudaError_t launch_gate_bwd(const float* d_og, const float* o, const void* g, long long T, int L, int n_q, int gate_on,
-                            void* d_o, void* d_P, int ldp, int goff, int num_sms, cudaStream_t st) {
-  gate_bwd_kernel<<<num_sms * 8, 256, 0, st>>>(d_og, o, reinterpret_cast<const bf16*>(g), T, L, n_q, gate_on,
-                                               reinterpret_cast<bf16*>(d_o), reinterpret_cast<bf16*>(d_P), ldp, goff);
-  return cudaGetLastError();
-}
-
 cudaError_t launch_qkv_bwd(const Fwd& f, const float* raw, int ldr, const float* dq, const float* dk, const float* dv,
                            const float* q_norm_w, const float* k_norm_w, const float2* rope, void* d_P, int ldp,
                            float* d_qw, float* d_kw, cudaStream_t st) {
   if (f.T == 0) return cudaSuccess;
   const int rows_per = 64;
   dim3 grid((f.T + rows_per - 1) / rows_per, f.n_q + 2 * f.n_kv);
-  qkv_bwd_kernel<<<grid, 128, 0, st>>>(f, raw, ldr, dq, dk, dv, q_norm_w, k_norm_w, rope, rows_per,
+  qkv_bwd_kernel<<<grid, 256, 0, st>>>(f, raw, ldr, dq, dk, dv, q_norm_w, k_norm_w, rope, rows_per,
                                        reinterpret_cast<bf16*>(d_P), ldp, d_qw, d_kw);
   return cudaGetLastError();
 }

@@ -160,6 +160,11 @@ struct EpiQKVGT {
       for (int c = 0; c < 4; ++c) {
         tmem_ld32(t0 + c * 32, r);
         deq32<S8>(r, dq, fa, dq.b, n0 + c * 32);
+        if (dst.raw && ok) {  // the projection before the norm, for the backward
+          float4* o4 = reinterpret_cast<float4*>(dst.raw + static_cast<size_t>(row) * dst.ldr + n0 + c * 32);
+#pragma unroll
+          for (int q = 0; q < 8; ++q) o4[q] = make_float4(u2f(r[4 * q]), u2f(r[4 * q + 1]), u2f(r[4 * q + 2]), u2f(r[4 * q + 3]));
+        }
         float v[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) v[i] = u2f(r[i]) * rstd * (1.0f + __ldg(w + c * 32 + i));
@@ -247,6 +252,7 @@ struct EpiResid {
   int chunk;   // modulation chunk of the gate (2 = gate_a, 5 = gate_m)
   TOut* out;   // [T, d]
   Deq dq;
+  float* pre = nullptr;  // optional [T, d] fp32: the product before the gate (for the backward)
   __device__ __forceinline__ void apply(int row, int nb, int half, uint32_t taddr, int M) const {
     const int N = f.d;
     const int n0 = nb * BN + half * 128;
@@ -264,6 +270,11 @@ struct EpiResid {
       if (col >= N) break;
       tmem_ld32(taddr + half * 128 + c * 32, r);
       deq32<S8>(r, dq, fa, dq.b, col);
+      if (ok && pre) {
+        float4* p4 = reinterpret_cast<float4*>(pre + static_cast<size_t>(row) * N + col);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) p4[q] = make_float4(u2f(r[4 * q]), u2f(r[4 * q + 1]), u2f(r[4 * q + 2]), u2f(r[4 * q + 3]));
+      }
       if (ok) {
         const float4* gs4 = reinterpret_cast<const float4*>(gs + col);
         const float4* gb4 = reinterpret_cast<const float4*>(gb + col);
@@ -297,6 +308,8 @@ struct EpiSwiGLUT {
   bf16* hmid;      // [T, F]
   float* rowamax;  // optional [T] (8-bit GEMMs only): largest |hmid| of each row, as stored
   Deq dq;
+  float* pre_a = nullptr;  // optional [T, F] fp32: hn W_gate^T and hn W_up^T (for the backward)
+  float* pre_u = nullptr;
   // accumulator columns [0,128) = hn W_gate^T, [128,256) = hn W_up^T for F-columns nb*128 ..
   __device__ __forceinline__ void apply(int row, int nb, int half, uint32_t taddr, int M) const {
     const int f0 = nb * 128 + half * 64;
@@ -310,6 +323,15 @@ struct EpiSwiGLUT {
       tmem_ld32x2(taddr + half * 64 + c * 32, taddr + 128 + half * 64 + c * 32, rg, ru);
       deq32<S8>(rg, dq, fa, dq.b, f0 + c * 32);
       deq32<S8>(ru, dq, fa, dq.b2, f0 + c * 32);
+      if (ok && pre_a) {
+        float4* a4 = reinterpret_cast<float4*>(pre_a + static_cast<size_t>(row) * F + f0 + c * 32);
+        float4* u4 = reinterpret_cast<float4*>(pre_u + static_cast<size_t>(row) * F + f0 + c * 32);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          a4[q] = make_float4(u2f(rg[4 * q]), u2f(rg[4 * q + 1]), u2f(rg[4 * q + 2]), u2f(rg[4 * q + 3]));
+          u4[q] = make_float4(u2f(ru[4 * q]), u2f(ru[4 * q + 1]), u2f(ru[4 * q + 2]), u2f(ru[4 * q + 3]));
+        }
+      }
       if (ok) {
         uint4* o4 = reinterpret_cast<uint4*>(hmid + static_cast<size_t>(row) * F + f0 + c * 32);
 #pragma unroll
@@ -329,6 +351,134 @@ struct EpiSwiGLUT {
     if constexpr (S8) {
       if (rowamax && ok) atomic_max_nonneg(rowamax + row, round_bf16(amax));
     }
+  }
+};
+
+// SwiGLU backward finished in the epilogue of d_hmid = d_fm W_down: with hmid = silu(a) u,
+// d_a = d_hmid u silu'(a) and d_u = d_hmid silu(a) go as bf16 into d_au [T, 2F] (columns
+// [0, F) and [F, 2F)); a and u are the forward's fp32 pre-activations [T, F].
+struct EpiSwiGLUBwd {
+  static constexpr bool kS8 = false;
+  const float* a;
+  const float* u;
+  bf16* d_au;
+  int F;
+  __device__ __forceinline__ void apply(int row, int nb, int half, uint32_t taddr, int M) const {
+    const int n0 = nb * BN + half * 128;
+    if (n0 >= F) return;
+    const bool ok = row < M;
+    uint32_t r[32];
+#pragma unroll 1
+    for (int c = 0; c < 4; ++c) {
+      const int col = n0 + c * 32;
+      if (col >= F) break;
+      tmem_ld32(taddr + half * 128 + c * 32, r);
+      if (!ok) continue;
+      const size_t off = static_cast<size_t>(row) * F + col;
+      bf16* da = d_au + static_cast<size_t>(row) * 2 * F + col;
+      if (col + 32 <= F) {
+        const float4* a4 = reinterpret_cast<const float4*>(a + off);
+        const float4* u4 = reinterpret_cast<const float4*>(u + off);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {  // 8 columns per step
+          const float4 a0 = __ldg(a4 + 2 * q), a1 = __ldg(a4 + 2 * q + 1);
+          const float4 u0 = __ldg(u4 + 2 * q), u1 = __ldg(u4 + 2 * q + 1);
+          const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+          const float uv[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+          float ga[8], gu[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const float dh = u2f(r[8 * q + i]);
+            const float sg = 1.0f / (1.0f + __expf(-av[i]));
+            ga[i] = dh * uv[i] * sg * (1.0f + av[i] * (1.0f - sg));
+            gu[i] = dh * av[i] * sg;
+          }
+          reinterpret_cast<uint4*>(da)[q] = make_uint4(pack_bf16x2(ga[0], ga[1]), pack_bf16x2(ga[2], ga[3]),
+                                                       pack_bf16x2(ga[4], ga[5]), pack_bf16x2(ga[6], ga[7]));
+          reinterpret_cast<uint4*>(da + F)[q] = make_uint4(pack_bf16x2(gu[0], gu[1]), pack_bf16x2(gu[2], gu[3]),
+                                                           pack_bf16x2(gu[4], gu[5]), pack_bf16x2(gu[6], gu[7]));
+        }
+      } else {
+        for (int i = 0; i < F - col; ++i) {
+          const float dh = u2f(r[i]), av = a[off + i], sg = 1.0f / (1.0f + __expf(-av));
+          da[i] = __float2bfloat16_rn(dh * u[off + i] * sg * (1.0f + av * (1.0f - sg)));
+          da[F + i] = __float2bfloat16_rn(dh * av * sg);
+        }
+      }
+    }
+  }
+};
+
+// Output-gate backward finished in the epilogue of d_og = d_fa W_o (one 128-column half of
+// a tile is one head): with og = o sigmoid(g), d_o = d_og sigmoid(g) goes as bf16 to the
+// head-major [B, n_q, L, 128] buffer the attention backward reads, the gate's gradient
+// d_og o sigmoid(g) (1 - sigmoid(g)) to d_P's g columns (bf16, from column goff), and the
+// softmax row term D = sum over the head of d_o (as stored) times o to D[b, head, l] (row
+// pitch Lp). Without the gate, d_o = d_og.
+struct EpiGateBwd {
+  static constexpr bool kS8 = false;
+  Fwd f;
+  const float* o;    // [T, n_q*128] fp32, the ungated attention output
+  const bf16* g;     // [T, n_q*128] gate pre-activation
+  bf16* d_o;         // [B, n_q, L, 128]
+  bf16* d_P;         // [T, ldp]
+  int ldp, goff;
+  float* D;          // [B, n_q, Lp]
+  __device__ __forceinline__ void apply(int row, int nb, int half, uint32_t taddr, int M) const {
+    constexpr int HD = 128;
+    const int nq = f.n_q * HD;
+    const int n0 = nb * BN + half * HD;
+    if (n0 >= nq) return;
+    const bool ok = row < M;
+    const int head = n0 / HD;
+    const int b = ok ? row / f.L : 0, l = ok ? row - b * f.L : 0;
+    bf16* dst = d_o + ((static_cast<size_t>(b) * f.n_q + head) * f.L + l) * HD;
+    const size_t off = static_cast<size_t>(row) * nq + n0;
+    float dsum = 0.0f;
+    uint32_t r[32];
+#pragma unroll 1
+    for (int c = 0; c < 4; ++c) {
+      tmem_ld32(taddr + half * HD + c * 32, r);
+      if (!ok) continue;
+      const float4* o4 = reinterpret_cast<const float4*>(o + off + c * 32);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {  // 8 columns per step
+        const float4 oa = __ldg(o4 + 2 * q), ob = __ldg(o4 + 2 * q + 1);
+        const float ov[8] = {oa.x, oa.y, oa.z, oa.w, ob.x, ob.y, ob.z, ob.w};
+        float dov[8], dg[8];
+        if (f.gate_on) {
+          const uint4 gu = __ldg(reinterpret_cast<const uint4*>(g + off + c * 32) + q);
+          const uint32_t gw[4] = {gu.x, gu.y, gu.z, gu.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float2 gg = unpack_bf16x2(gw[e]);
+            const float s0 = sigmoidf_(gg.x), s1 = sigmoidf_(gg.y);
+            const float a0 = u2f(r[8 * q + 2 * e]), a1 = u2f(r[8 * q + 2 * e + 1]);
+            dov[2 * e] = a0 * s0;
+            dov[2 * e + 1] = a1 * s1;
+            dg[2 * e] = a0 * ov[2 * e] * s0 * (1.0f - s0);
+            dg[2 * e + 1] = a1 * ov[2 * e + 1] * s1 * (1.0f - s1);
+          }
+          reinterpret_cast<uint4*>(d_P + static_cast<size_t>(row) * ldp + goff + n0 + c * 32)[q] =
+              make_uint4(pack_bf16x2(dg[0], dg[1]), pack_bf16x2(dg[2], dg[3]), pack_bf16x2(dg[4], dg[5]),
+                         pack_bf16x2(dg[6], dg[7]));
+        } else {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) dov[e] = u2f(r[8 * q + e]);
+        }
+        const uint4 pk = make_uint4(pack_bf16x2(dov[0], dov[1]), pack_bf16x2(dov[2], dov[3]),
+                                    pack_bf16x2(dov[4], dov[5]), pack_bf16x2(dov[6], dov[7]));
+        reinterpret_cast<uint4*>(dst + c * 32)[q] = pk;
+        const uint32_t pw[4] = {pk.x, pk.y, pk.z, pk.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 dd = unpack_bf16x2(pw[e]);
+          dsum = fmaf(dd.x, ov[2 * e], dsum);
+          dsum = fmaf(dd.y, ov[2 * e + 1], dsum);
+        }
+      }
+    }
+    if (ok) D[(static_cast<size_t>(b) * f.n_q + head) * f.Lp + l] = dsum;
   }
 };
 
@@ -622,7 +772,29 @@ cudaError_t gemm_tc_init_set(int num_sms) {
 cudaError_t gemm_tc_init(int num_sms) {
   cudaError_t e = gemm_tc_init_set<false>(num_sms);
   if (e == cudaSuccess) e = gemm_tc_init_set<true>(num_sms);
+  if (e == cudaSuccess) e = set_smem_attr<EpiSwiGLUBwd, false>(num_sms);
+  if (e == cudaSuccess) e = set_smem_attr<EpiGateBwd, false>(num_sms);
   return e != cudaSuccess ? e : set_smem_attr<EpiPlain, false>(num_sms);
+}
+
+cudaError_t launch_gemm_gate_bwd(const Fwd& f, const CUtensorMap* tm_a, const CUtensorMap* tm_b, int K, const float* o,
+                                 const void* g, void* d_o, void* d_P, int ldp, int goff, float* D, int num_sms,
+                                 int* err, cudaStream_t st) {
+  const int nq = f.n_q * 128;
+  if (f.T <= 0) return cudaSuccess;
+  if (ldp % 8 || goff % 8) return cudaErrorInvalidValue;
+  EpiGateBwd epi{f, o, reinterpret_cast<const bf16*>(g), reinterpret_cast<bf16*>(d_o), reinterpret_cast<bf16*>(d_P),
+                 ldp, goff, D};
+  return launch<EpiGateBwd, false>(tm_a, tm_b, tm_b, f.T, (nq + BN - 1) / BN, K, epi, num_sms, err, st);
+}
+
+cudaError_t launch_gemm_swiglu_bwd(const CUtensorMap* tm_a, const CUtensorMap* tm_b, int M, int F, int K,
+                                   const float* a, const float* u, void* d_au, int num_sms, int* err,
+                                   cudaStream_t st) {
+  if (M <= 0 || F <= 0) return cudaSuccess;
+  if (F % 8) return cudaErrorInvalidValue;
+  EpiSwiGLUBwd epi{a, u, reinterpret_cast<bf16*>(d_au), F};
+  return launch<EpiSwiGLUBwd, false>(tm_a, tm_b, tm_b, M, (F + BN - 1) / BN, K, epi, num_sms, err, st);
 }
 
 cudaError_t launch_gemm_plain(const CUtensorMap* tm_a, const CUtensorMap* tm_b, int M, int N, int K, float* C,
@@ -646,38 +818,38 @@ cudaError_t launch_gemm_qkvg(const Fwd& f, const CUtensorMap* tm_a, const CUtens
 
 cudaError_t launch_gemm_resid_attn(const Fwd& f, const CUtensorMap* tm_a, const CUtensorMap* tm_b, int K, RowSrc x,
                                    const float* mod_shared, const float* mod_bias, float* h1, const Deq* dq,
-                                   int num_sms, int* err, cudaStream_t st) {
+                                   float* pre, int num_sms, int* err, cudaStream_t st) {
   const int num_n = (f.d + BN - 1) / BN;
   if (dq) {
     EpiResidAttnT<true> epi{f, x, mod_shared, mod_bias, 2, h1, *dq};
     return launch<EpiResidAttnT<true>, false>(tm_a, tm_b, tm_b, f.T, num_n, K, epi, num_sms, err, st);
   }
-  EpiResidAttnT<false> epi{f, x, mod_shared, mod_bias, 2, h1, Deq{}};
+  EpiResidAttnT<false> epi{f, x, mod_shared, mod_bias, 2, h1, Deq{}, pre};
   return launch<EpiResidAttnT<false>, false>(tm_a, tm_b, tm_b, f.T, num_n, K, epi, num_sms, err, st);
 }
 
 cudaError_t launch_gemm_resid_mlp(const Fwd& f, const CUtensorMap* tm_a, const CUtensorMap* tm_b, int K,
                                   const float* h1, const float* mod_shared, const float* mod_bias, void* out,
-                                  const Deq* dq, int num_sms, int* err, cudaStream_t st) {
+                                  const Deq* dq, float* pre, int num_sms, int* err, cudaStream_t st) {
   const int num_n = (f.d + BN - 1) / BN;
   const RowSrc res{nullptr, nullptr, h1};
   if (dq) {
     EpiResidMlpT<true> epi{f, res, mod_shared, mod_bias, 5, reinterpret_cast<bf16*>(out), *dq};
     return launch<EpiResidMlpT<true>, false>(tm_a, tm_b, tm_b, f.T, num_n, K, epi, num_sms, err, st);
   }
-  EpiResidMlpT<false> epi{f, res, mod_shared, mod_bias, 5, reinterpret_cast<bf16*>(out), Deq{}};
+  EpiResidMlpT<false> epi{f, res, mod_shared, mod_bias, 5, reinterpret_cast<bf16*>(out), Deq{}, pre};
   return launch<EpiResidMlpT<false>, false>(tm_a, tm_b, tm_b, f.T, num_n, K, epi, num_sms, err, st);
 }
 
 cudaError_t launch_gemm_swiglu(const Fwd& f, const CUtensorMap* tm_a, const CUtensorMap* tm_gate,
-                               const CUtensorMap* tm_up, void* hmid, float* rowamax, const Deq* dq, int num_sms,
-                               int* err, cudaStream_t st) {
+                               const CUtensorMap* tm_up, void* hmid, float* rowamax, const Deq* dq, float* pre_a,
+                               float* pre_u, int num_sms, int* err, cudaStream_t st) {
   const int num_n = (f.F + 127) / 128;
   if (dq) {
     EpiSwiGLUT<true> epi{f.F, reinterpret_cast<bf16*>(hmid), rowamax, *dq};
     return launch<EpiSwiGLUT<true>, true>(tm_a, tm_gate, tm_up, f.T, num_n, f.d, epi, num_sms, err, st);
   }
-  EpiSwiGLUT<false> epi{f.F, reinterpret_cast<bf16*>(hmid), rowamax, Deq{}};
+  EpiSwiGLUT<false> epi{f.F, reinterpret_cast<bf16*>(hmid), rowamax, Deq{}, pre_a, pre_u};
   return launch<EpiSwiGLUT<false>, true>(tm_a, tm_gate, tm_up, f.T, num_n, f.d, epi, num_sms, err, st);
 }
 

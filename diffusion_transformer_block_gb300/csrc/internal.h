@@ -31,6 +31,8 @@ struct QkvgDst {
   const float* q_norm_w;
   const float* k_norm_w;
   const float2* rope;  // [pos][hd/4] (cos, sin)
+  float* raw = nullptr;  // optional [T, ldr] fp32: the Q and K columns of the projection
+  int ldr = 0;           // before the norm (for the backward)
 };
 
 // Dequantisation factors of an 8-bit GEMM (powers of two): row m, column n of the
@@ -100,20 +102,34 @@ cudaError_t gemm_tc_init(int num_sms);
 // xn[T,d] x W_qkvg^T -> QK-norm, RoPE, scatter to Q / K / V^T / G
 cudaError_t launch_gemm_qkvg(const Fwd& f, const CUtensorMap* tm_a, const CUtensorMap* tm_b, int N,
                              const QkvgDst& dst, const Deq* dq, int num_sms, int* err, cudaStream_t st);
-// h1[T,d] (fp32) = x (bf16, split buffers) + gate_a * (A W^T)
+// h1[T,d] (fp32) = x (bf16, split buffers) + gate_a * (A W^T); pre (optional, bf16 mode,
+// fp32 [T,d]) gets A W^T
 cudaError_t launch_gemm_resid_attn(const Fwd& f, const CUtensorMap* tm_a, const CUtensorMap* tm_b, int K, RowSrc x,
                                    const float* mod_shared, const float* mod_bias, float* h1, const Deq* dq,
-                                   int num_sms, int* err, cudaStream_t st);
-// out[T,d] (bf16) = h1 (fp32) + gate_m * (A W^T)
+                                   float* pre, int num_sms, int* err, cudaStream_t st);
+// out[T,d] (bf16) = h1 (fp32) + gate_m * (A W^T); pre as above
 cudaError_t launch_gemm_resid_mlp(const Fwd& f, const CUtensorMap* tm_a, const CUtensorMap* tm_b, int K,
                                   const float* h1, const float* mod_shared, const float* mod_bias, void* out,
-                                  const Deq* dq, int num_sms, int* err, cudaStream_t st);
+                                  const Deq* dq, float* pre, int num_sms, int* err, cudaStream_t st);
 // hmid[T,F] = silu(hn W_gate^T) * (hn W_up^T); rowamax (optional, pre-zeroed [T]) gets
-// each row's largest |hmid| as stored (bf16)
+// each row's largest |hmid| as stored (bf16); pre_a / pre_u (optional, bf16 mode, fp32
+// [T,F]) get the two products
 cudaError_t launch_gemm_swiglu(const Fwd& f, const CUtensorMap* tm_a, const CUtensorMap* tm_gate,
-                               const CUtensorMap* tm_up, void* hmid, float* rowamax, const Deq* dq, int num_sms,
-                               int* err, cudaStream_t st);
+                               const CUtensorMap* tm_up, void* hmid, float* rowamax, const Deq* dq, float* pre_a,
+                               float* pre_u, int num_sms, int* err, cudaStream_t st);
 
+// the output-gate backward and the softmax row term in the epilogue of d_og = A[T,K] W_o^T
+// (B = W_o^T as a K-major [n_q*128, K] map): d_o (bf16, head-major [B, n_q, L, 128]), the
+// gate's gradient into d_P columns goff.. (bf16, row pitch ldp), D = rowsum(d_o o) per head
+// ([B, n_q, Lp]); o fp32 [T, n_q*128], g bf16 [T, n_q*128]
+cudaError_t launch_gemm_gate_bwd(const Fwd& f, const CUtensorMap* tm_a, const CUtensorMap* tm_b, int K, const float* o,
+                                 const void* g, void* d_o, void* d_P, int ldp, int goff, float* D, int num_sms,
+                                 int* err, cudaStream_t st);
+// d_au [M, 2F] (bf16) = SwiGLU backward of d_hmid = A[M,K] B[F,K]^T with the forward's
+// fp32 pre-activations a, u [M, F]: d_a = d_hmid u silu'(a), d_u = d_hmid silu(a) (F % 8 == 0)
+cudaError_t launch_gemm_swiglu_bwd(const CUtensorMap* tm_a, const CUtensorMap* tm_b, int M, int F, int K,
+                                   const float* a, const float* u, void* d_au, int num_sms, int* err,
+                                   cudaStream_t st);
 // C[M,N] (fp32, row pitch ldc % 4 == 0) = alpha * A[M,K] B[N,K]^T (+ C if accumulate);
 // A and B bf16 K-major tensor maps (box 64 x 128)
 cudaError_t launch_gemm_plain(const CUtensorMap* tm_a, const CUtensorMap* tm_b, int M, int N, int K, float* C,
@@ -158,23 +174,12 @@ cudaError_t launch_transpose_bf16(const void* src, int R, int C, long long lds, 
 // y = res + gate_chunk * f: d_f = dy * gate (bf16 [T, d]); sum_l dy f -> d_mod[b, chunk], d_bias[chunk]
 cudaError_t launch_gated_bwd(const Fwd& f, const void* dy, int dy_f32, const float* fv, const float* mod_shared,
                              const float* mod_bias, int chunk, void* d_f, float* d_mod, float* d_bias, cudaStream_t st);
-// hmid = silu(a) u: d_au = [d_a | d_u] (bf16 [T, 2F])
-cudaError_t launch_swiglu_bwd(const float* d_hmid, const float* a, const float* u, long long T, int F, void* d_au,
-                              int num_sms, cudaStream_t st);
 // norm + modulation backward: dx (fp32 joint, or bf16 into the split buffers of dx_bf16)
 // = d_res + RMSNorm gradient of dy (1 + w)(1 + scale); column sums into d_mod / d_bias / d_gain
 cudaError_t launch_norm_bwd(const Fwd& f, RowSrc xs, int x_f32, const float* dy, const float* gain_w,
                             const float* mod_shared, const float* mod_bias, int chunk_shift, int chunk_scale,
                             const void* d_res, int res_f32, float* dx_f32, RowSrc dx_bf16, float* rstd,
                             float* d_mod, float* d_bias, float* d_gain, cudaStream_t st);
-// D[b, h, l] (row pitch Lp) = sum over the head's 128 columns of d_o (bf16, head-major)
-// times o (fp32 [T, n_q*128])
-cudaError_t launch_attn_rowdot(const void* d_o, const float* o, int T, int L, int Lp, int n_q, float* D,
-                               cudaStream_t st);
-// output gate backward: d_o (bf16, head-major [B, n_q, L, 128]) and the gate's gradient
-// into d_P columns goff..
-cudaError_t launch_gate_bwd(const float* d_og, const float* o, const void* g, long long T, int L, int n_q, int gate_on,
-                            void* d_o, void* d_P, int ldp, int goff, int num_sms, cudaStream_t st);
 // QK-norm + RoPE backward and the V gradient into d_P (bf16); gain gradients into d_qw / d_kw
 cudaError_t launch_qkv_bwd(const Fwd& f, const float* raw, int ldr, const float* dq, const float* dk, const float* dv,
                            const float* q_norm_w, const float* k_norm_w, const float2* rope, void* d_P, int ldp,
