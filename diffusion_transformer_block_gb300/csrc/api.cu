@@ -90,6 +90,18 @@ bool encode_2d(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, u
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2D fp32 tensor map over a row-major [rows, cols] matrix (pitch = cols), box = 32 x 32
+// (128-byte rows, matching the 128-byte swizzle): the residual epilogue's store target.
+bool encode_2d_f32(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows) {
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 4};
+  cuuint32_t box[2] = {32, 32};
+  cuuint32_t estr[2] = {1, 1};
+  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // 3D bf16 tensor map over [planes, rows, cols] (cols contiguous, pitch `pitch_elems`).
 bool encode_3d(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint64_t planes,
                uint64_t pitch_elems, uint32_t box_cols, uint32_t box_rows) {
@@ -531,7 +543,8 @@ int forward_impl(krea_dit_block_t h, const void* x_img, const void* x_txt, const
   if (h->mode8) {
     const int per_row = h->mode8 == 2;
     const uint64_t T = static_cast<uint64_t>(f.T);
-    CUtensorMap tm_xn8, tm_wqkvg, tm_og8, tm_wo, tm_hn8, tm_wgate, tm_wup, tm_hmid8, tm_wdown, tm_q, tm_k, tm_vt;
+    CUtensorMap tm_xn8, tm_wqkvg, tm_og8, tm_wo, tm_hn8, tm_wgate, tm_wup, tm_hmid8, tm_wdown, tm_q, tm_k, tm_vt,
+        tm_h1, tm_out;
     bool ok = encode_2d_u8(&tm_xn8, h->xn8, d, T, 128) && encode_2d_u8(&tm_wqkvg, w8->w_qkvg, d, h->n_qkvg, 128) &&
               encode_2d_u8(&tm_og8, h->og8, nqhd, T, 128) && encode_2d_u8(&tm_wo, w8->w_o, nqhd, d, 128) &&
               encode_2d_u8(&tm_hn8, h->hn8, d, T, 128) && encode_2d_u8(&tm_wgate, w8->w_gate, d, c.ffn, 128) &&
@@ -539,7 +552,8 @@ int forward_impl(krea_dit_block_t h, const void* x_img, const void* x_txt, const
               encode_2d_u8(&tm_wdown, w8->w_down, c.ffn, d, 128) &&
               encode_3d(&tm_q, h->q, c.head_dim, L, static_cast<uint64_t>(B) * c.n_q, c.head_dim, 64, 128) &&
               encode_3d(&tm_k, h->k, c.head_dim, L, static_cast<uint64_t>(B) * c.n_kv, c.head_dim, 64, 128) &&
-              encode_3d(&tm_vt, h->vt, L, c.head_dim, static_cast<uint64_t>(B) * c.n_kv, f.Lp, 64, 128);
+              encode_3d(&tm_vt, h->vt, L, c.head_dim, static_cast<uint64_t>(B) * c.n_kv, f.Lp, 64, 128) &&
+              encode_2d_f32(&tm_h1, h->h1, d, T) && encode_2d(&tm_out, out, d, T, d, 64, 32);
     if (!ok) return KREA_DIT_ERR_CUDA;
     const int sms = h->num_sms;
     // row amax accumulators of the attention and SwiGLU outputs (atomic max from zero)
@@ -562,8 +576,8 @@ int forward_impl(krea_dit_block_t h, const void* x_img, const void* x_txt, const
     KD_RUN(S_QKVG_TC, kd::launch_gemm_qkvg(f, &tm_xn8, &tm_wqkvg, h->n_qkvg, dst, &dq_qkvg, sms, h->err, st));
     KD_RUN(S_ATTN, kd::launch_attn_tc(f, &tm_q, &tm_k, &tm_vt, h->g, h->og, h->am_og, nullptr, nullptr, sms, h->err, st));
     KD_RUN(S_QUANT_OG, kd::launch_quant_e4m3(h->og, f.T, nqhd, h->am_og, per_row, h->og8, h->dq_og, sms, st));
-    KD_RUN(S_OPROJ_TC, kd::launch_gemm_resid_attn(f, &tm_og8, &tm_wo, nqhd, xsrc, t_emb, w->mod_bias,
-                                                  static_cast<float*>(h->h1), &dq_o, nullptr, sms, h->err, st));
+    KD_RUN(S_OPROJ_TC, kd::launch_gemm_resid_attn(f, &tm_og8, &tm_wo, nqhd, xsrc, t_emb, w->mod_bias, &tm_h1, &dq_o,
+                                                  nullptr, sms, h->err, st));
     if (!per_row)
       KD_RUN(S_NORM2_AMAX, kd::launch_norm_modulate(kd::NormIO::F32_BF16, f, h1src, w->norm2_w, t_emb, w->mod_bias, 3,
                                                     4, nullptr, sms, st, &q_amax2));
@@ -574,9 +588,10 @@ int forward_impl(krea_dit_block_t h, const void* x_img, const void* x_txt, const
     KD_RUN(S_QUANT_HMID,
            kd::launch_quant_e4m3(h->hmid, f.T, c.ffn, h->am_hmid, per_row, h->hmid8, h->dq_hmid, sms, st));
     KD_RUN(S_DOWN_TC, kd::launch_gemm_resid_mlp(f, &tm_hmid8, &tm_wdown, c.ffn, static_cast<const float*>(h->h1),
-                                                t_emb, w->mod_bias, out, &dq_down, nullptr, sms, h->err, st));
+                                                t_emb, w->mod_bias, &tm_out, &dq_down, nullptr, sms, h->err, st));
   } else if (h->bf16) {
-    CUtensorMap tm_xn, tm_wqkvg, tm_og, tm_wo, tm_hn, tm_wgate, tm_wup, tm_hmid, tm_wdown, tm_q, tm_k, tm_vt;
+    CUtensorMap tm_xn, tm_wqkvg, tm_og, tm_wo, tm_hn, tm_wgate, tm_wup, tm_hmid, tm_wdown, tm_q, tm_k, tm_vt, tm_h1,
+        tm_out;
     const uint64_t T = static_cast<uint64_t>(f.T);
     bool ok = encode_2d(&tm_xn, h->xn, d, T, d, 64, 128) &&
               encode_2d(&tm_wqkvg, w->w_qkvg, d, h->n_qkvg, d, 64, 128) &&
@@ -588,7 +603,8 @@ int forward_impl(krea_dit_block_t h, const void* x_img, const void* x_txt, const
               encode_2d(&tm_wdown, w->w_down, c.ffn, d, c.ffn, 64, 128) &&
               encode_3d(&tm_q, h->q, c.head_dim, L, static_cast<uint64_t>(B) * c.n_q, c.head_dim, 64, 128) &&
               encode_3d(&tm_k, h->k, c.head_dim, L, static_cast<uint64_t>(B) * c.n_kv, c.head_dim, 64, 128) &&
-              encode_3d(&tm_vt, h->vt, L, c.head_dim, static_cast<uint64_t>(B) * c.n_kv, f.Lp, 64, 128);
+              encode_3d(&tm_vt, h->vt, L, c.head_dim, static_cast<uint64_t>(B) * c.n_kv, f.Lp, 64, 128) &&
+              encode_2d_f32(&tm_h1, h->h1, d, T) && encode_2d(&tm_out, out, d, T, d, 64, 32);
     if (!ok) return KREA_DIT_ERR_CUDA;
     const int sms = h->num_sms;
     KD_RUN(S_NORM1, kd::launch_norm_modulate(kd::NormIO::BF16_BF16, f, xsrc, w->norm1_w, t_emb, w->mod_bias, 0, 1,
@@ -596,8 +612,7 @@ int forward_impl(krea_dit_block_t h, const void* x_img, const void* x_txt, const
     KD_RUN(S_QKVG_TC, kd::launch_gemm_qkvg(f, &tm_xn, &tm_wqkvg, h->n_qkvg, dst, nullptr, sms, h->err, st));
     KD_RUN(S_ATTN, kd::launch_attn_tc(f, &tm_q, &tm_k, &tm_vt, h->g, h->og, nullptr, h->bw_stats ? h->f_lse : nullptr,
                                         h->bw_stats ? h->f_o : nullptr, sms, h->err, st));
-    KD_RUN(S_OPROJ_TC, kd::launch_gemm_resid_attn(f, &tm_og, &tm_wo, nqhd, xsrc, t_emb, w->mod_bias,
-                                                  static_cast<float*>(h->h1), nullptr,
+    KD_RUN(S_OPROJ_TC, kd::launch_gemm_resid_attn(f, &tm_og, &tm_wo, nqhd, xsrc, t_emb, w->mod_bias, &tm_h1, nullptr,
                                                   h->bw_stats ? h->f_fa : nullptr, sms, h->err, st));
     KD_RUN(S_NORM2, kd::launch_norm_modulate(kd::NormIO::F32_BF16, f, h1src, w->norm2_w, t_emb, w->mod_bias, 3, 4,
                                              h->hn, sms, st));
@@ -605,8 +620,8 @@ int forward_impl(krea_dit_block_t h, const void* x_img, const void* x_txt, const
                                                h->bw_stats ? h->f_a : nullptr, h->bw_stats ? h->f_u : nullptr,
                                                sms, h->err, st));
     KD_RUN(S_DOWN_TC, kd::launch_gemm_resid_mlp(f, &tm_hmid, &tm_wdown, c.ffn, static_cast<const float*>(h->h1),
-                                                t_emb, w->mod_bias, out, nullptr, h->bw_stats ? h->f_td : nullptr, sms,
-                                                h->err, st));
+                                                t_emb, w->mod_bias, &tm_out, nullptr, h->bw_stats ? h->f_td : nullptr,
+                                                sms, h->err, st));
   } else {
     const int T = f.T;
     const float* wq = static_cast<const float*>(w->w_qkvg);

@@ -30,6 +30,8 @@
 // even CTA's barrier. Against one CTA per tile (the pair sharing B by multicast), a stage
 // takes 32 KB of shared memory instead of 48 KB, so six stages fit instead of four and
 // cover half as much again of the L2 latency.
+#include <type_traits>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -46,7 +48,19 @@ constexpr int STAGE_BYTES = A_BYTES + BH_BYTES;
 constexpr int TMEM_COLS = 2 * BN;
 constexpr int NUM_EPI_WARPS = 8;
 constexpr int NUM_THREADS = 64 + NUM_EPI_WARPS * 32;
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*alignment slack*/ + 256 /*barriers*/;
+// shared-memory staging per epilogue warp (epilogues that store through TMA declare kStgBytes)
+template <class E, class = void>
+struct StgOf {
+  static constexpr int value = 0;
+};
+template <class E>
+struct StgOf<E, std::void_t<decltype(E::kStgBytes)>> {
+  static constexpr int value = E::kStgBytes;
+};
+template <class Epi>
+constexpr int smem_bytes() {
+  return STAGES * STAGE_BYTES + NUM_EPI_WARPS * StgOf<Epi>::value + 1024 /*alignment slack*/ + 256 /*barriers*/;
+}
 #ifndef KD_GEMM_GROUP_M
 #define KD_GEMM_GROUP_M 32
 #endif
@@ -220,40 +234,62 @@ struct EpiQKVGT {
   }
 };
 
-// 8 consecutive residual values as fp32 (bf16 or fp32 storage)
-__device__ __forceinline__ void load_res8(const bf16* p, float (&v)[8]) {
-  const uint4 u = *reinterpret_cast<const uint4*>(p);
-  const float2 a = unpack_bf16x2(u.x), b = unpack_bf16x2(u.y), c = unpack_bf16x2(u.z), e = unpack_bf16x2(u.w);
-  v[0] = a.x; v[1] = a.y; v[2] = b.x; v[3] = b.y; v[4] = c.x; v[5] = c.y; v[6] = e.x; v[7] = e.y;
-}
-__device__ __forceinline__ void load_res8(const float* p, float (&v)[8]) {
-  const float4 a = reinterpret_cast<const float4*>(p)[0], b = reinterpret_cast<const float4*>(p)[1];
-  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
-}
-__device__ __forceinline__ void store_out8(bf16* p, const float (&v)[8]) {
-  *reinterpret_cast<uint4*>(p) = make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]),
-                                            pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7]));
-}
-__device__ __forceinline__ void store_out8(float* p, const float (&v)[8]) {
-  reinterpret_cast<float4*>(p)[0] = make_float4(v[0], v[1], v[2], v[3]);
-  reinterpret_cast<float4*>(p)[1] = make_float4(v[4], v[5], v[6], v[7]);
-}
+// 32 consecutive residual values of one row (one accumulator chunk), loaded one chunk
+// ahead of their use so that the load's DRAM latency overlaps the previous chunk's work
+template <class T>
+struct Res32;
+template <>
+struct Res32<bf16> {
+  uint4 v[4];
+  __device__ __forceinline__ void load(const bf16* p) {
+    const uint4* p4 = reinterpret_cast<const uint4*>(p);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) v[i] = __ldg(p4 + i);
+  }
+  __device__ __forceinline__ void get8(int q4, float (&o)[8]) const {
+    const float2 a = unpack_bf16x2(v[q4].x), b = unpack_bf16x2(v[q4].y), c = unpack_bf16x2(v[q4].z),
+                 e = unpack_bf16x2(v[q4].w);
+    o[0] = a.x; o[1] = a.y; o[2] = b.x; o[3] = b.y; o[4] = c.x; o[5] = c.y; o[6] = e.x; o[7] = e.y;
+  }
+};
+template <>
+struct Res32<float> {
+  float4 v[8];
+  __device__ __forceinline__ void load(const float* p) {
+    const float4* p4 = reinterpret_cast<const float4*>(p);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = __ldg(p4 + i);
+  }
+  __device__ __forceinline__ void get8(int q4, float (&o)[8]) const {
+    const float4 a = v[2 * q4], b = v[2 * q4 + 1];
+    o[0] = a.x; o[1] = a.y; o[2] = a.z; o[3] = a.w; o[4] = b.x; o[5] = b.y; o[6] = b.z; o[7] = b.w;
+  }
+};
 
 // out = res + gate * acc. The attention residual reads the bf16 block input from the
 // caller's split text/image buffers and writes the fp32 residual stream h1; the MLP
-// residual reads h1 and writes the bf16 block output.
+// residual reads h1 and writes the bf16 block output. d is a multiple of 64, so a
+// 128-column half holds 2 or 4 whole 32-column chunks.
+// The result leaves through shared memory: each epilogue warp owns a 4 KB box (32 rows x
+// 128 bytes, laid out in the 128-byte swizzle), every lane writes its row into it and one
+// lane hands the box to a TMA store, so the output reaches L2 as whole lines rather than as
+// 32 scattered 16-byte pieces per store instruction. Rows past M are clipped by the store.
 template <class TRes, class TOut, bool S8>
 struct EpiResid {
   static constexpr bool kS8 = S8;
+  static constexpr int kStgBytes = 4096;  // per epilogue warp
+  static constexpr int kPerBox = sizeof(TOut) == 4 ? 1 : 2;  // 32-column chunks per box
   Fwd f;
   RowSrc res;
   const float* mod_shared;
   const float* mod_bias;
   int chunk;   // modulation chunk of the gate (2 = gate_a, 5 = gate_m)
-  TOut* out;   // [T, d]
   Deq dq;
   float* pre = nullptr;  // optional [T, d] fp32: the product before the gate (for the backward)
-  __device__ __forceinline__ void apply(int row, int nb, int half, uint32_t taddr, int M) const {
+  // stg: this warp's box (1024-byte aligned); tm_out: the output [T, d] with a box of 128
+  // bytes x 32 rows and the 128-byte swizzle
+  __device__ __forceinline__ void apply(int row, int nb, int half, uint32_t taddr, int M, uint8_t* stg, int lane,
+                                        const CUtensorMap* tm_out) const {
     const int N = f.d;
     const int n0 = nb * BN + half * 128;
     if (n0 >= N) return;
@@ -263,11 +299,16 @@ struct EpiResid {
     const float* gs = mod_shared + (static_cast<size_t>(b) * 6 + chunk) * N;
     const float* gb = mod_bias + static_cast<size_t>(chunk) * N;
     const float fa = deq_row<S8>(dq, row, ok);
+    const int nc = min(4, (N - n0) >> 5);
+    uint8_t* srow = stg + lane * 128;
+    const int sw = lane & 7;  // the swizzle of this row: 16-byte unit j sits at j ^ sw
+    Res32<TRes> cur, nxt;
+    if (ok) cur.load(x + n0);
     uint32_t r[32];
 #pragma unroll 1
-    for (int c = 0; c < 4; ++c) {
+    for (int c = 0; c < nc; ++c) {
       const int col = n0 + c * 32;
-      if (col >= N) break;
+      if (ok && c + 1 < nc) nxt.load(x + col + 32);
       tmem_ld32(taddr + half * 128 + c * 32, r);
       deq32<S8>(r, dq, fa, dq.b, col);
       if (ok && pre) {
@@ -275,24 +316,43 @@ struct EpiResid {
 #pragma unroll
         for (int q = 0; q < 8; ++q) p4[q] = make_float4(u2f(r[4 * q]), u2f(r[4 * q + 1]), u2f(r[4 * q + 2]), u2f(r[4 * q + 3]));
       }
-      if (ok) {
-        const float4* gs4 = reinterpret_cast<const float4*>(gs + col);
-        const float4* gb4 = reinterpret_cast<const float4*>(gb + col);
-        TOut* o = out + static_cast<size_t>(row) * N + col;
+      if (c % kPerBox == 0) {  // the previous box has left shared memory before it is rewritten
+        if (lane == 0) bulk_wait_read_all();
+        __syncwarp();
+      }
+      const float4* gs4 = reinterpret_cast<const float4*>(gs + col);
+      const float4* gb4 = reinterpret_cast<const float4*>(gb + col);
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          float xv[8];
-          load_res8(x + col + 8 * q4, xv);
-          const float4 s0 = __ldg(gs4 + 2 * q4), s1 = __ldg(gs4 + 2 * q4 + 1);
-          const float4 b0 = __ldg(gb4 + 2 * q4), b1 = __ldg(gb4 + 2 * q4 + 1);
-          const float gt[8] = {s0.x + b0.x, s0.y + b0.y, s0.z + b0.z, s0.w + b0.w,
-                               s1.x + b1.x, s1.y + b1.y, s1.z + b1.z, s1.w + b1.w};
-          float y[8];
+      for (int q4 = 0; q4 < 4; ++q4) {
+        float xv[8];
+        cur.get8(q4, xv);
+        const float4 s0 = __ldg(gs4 + 2 * q4), s1 = __ldg(gs4 + 2 * q4 + 1);
+        const float4 b0 = __ldg(gb4 + 2 * q4), b1 = __ldg(gb4 + 2 * q4 + 1);
+        const float gt[8] = {s0.x + b0.x, s0.y + b0.y, s0.z + b0.z, s0.w + b0.w,
+                             s1.x + b1.x, s1.y + b1.y, s1.z + b1.z, s1.w + b1.w};
+        float y[8];
 #pragma unroll
-          for (int i = 0; i < 8; ++i) y[i] = fmaf(gt[i], u2f(r[8 * q4 + i]), xv[i]);
-          store_out8(o + 8 * q4, y);
+        for (int i = 0; i < 8; ++i) y[i] = fmaf(gt[i], u2f(r[8 * q4 + i]), xv[i]);
+        if constexpr (sizeof(TOut) == 4) {
+          const int j = 2 * q4;
+          *reinterpret_cast<float4*>(srow + ((j ^ sw) << 4)) = make_float4(y[0], y[1], y[2], y[3]);
+          *reinterpret_cast<float4*>(srow + (((j + 1) ^ sw) << 4)) = make_float4(y[4], y[5], y[6], y[7]);
+        } else {
+          const int j = (c & 1) * 4 + q4;
+          *reinterpret_cast<uint4*>(srow + ((j ^ sw) << 4)) =
+              make_uint4(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]), pack_bf16x2(y[4], y[5]),
+                         pack_bf16x2(y[6], y[7]));
         }
       }
+      if (c % kPerBox == kPerBox - 1) {
+        fence_proxy_async_smem();  // the lanes' writes are visible to the TMA engine
+        __syncwarp();
+        if (lane == 0 && row < M) {  // lane 0's row is the box's first: a box wholly past M is skipped
+          tma_store_2d(tm_out, stg, col - (kPerBox - 1) * 32, row);
+          bulk_commit();
+        }
+      }
+      cur = nxt;
     }
   }
 };
@@ -529,12 +589,15 @@ struct EpiPlain {
 template <class Epi, bool DUAL>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
-                   const __grid_constant__ CUtensorMap tm_b2, int M, int num_n, int K, Epi epi, int* err) {
+                   const __grid_constant__ CUtensorMap tm_b2, const __grid_constant__ CUtensorMap tm_c, int M,
+                   int num_n, int K, Epi epi, int* err) {
   constexpr bool FP8 = Epi::kS8;
   constexpr int BK = FP8 ? 128 : 64;  // K elements per stage (128 bytes of each operand row)
+  constexpr int STG = StgOf<Epi>::value;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  uint8_t* stg_base = smem + STAGES * STAGE_BYTES;  // epilogue staging boxes (1024-byte aligned)
+  uint64_t* full = reinterpret_cast<uint64_t*>(stg_base + NUM_EPI_WARPS * STG);
   uint64_t* empty = full + STAGES;
   uint64_t* tfull = empty + STAGES;
   uint64_t* tempty = tfull + 2;
@@ -682,7 +745,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       tc_fence_after();
       const int row = mb * BM + quad * 32 + lane;
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(acc * BN);
-      epi.apply(row, nb, half, taddr, M);
+      if constexpr (STG > 0)
+        epi.apply(row, nb, half, taddr, M, stg_base + (warp - 2) * STG, lane, &tm_c);
+      else
+        epi.apply(row, nb, half, taddr, M);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(tempty0 + static_cast<uint32_t>(acc * sizeof(uint64_t)));
@@ -690,6 +756,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         acc = 0;
         acc_phase ^= 1;
       }
+    }
+    if constexpr (STG > 0) {  // this warp's TMA stores have completed
+      if (lane == 0) bulk_wait_all();
+      __syncwarp();
     }
   }
   __syncthreads();
@@ -712,7 +782,7 @@ int MaxClusters<Epi, DUAL>::value = 0;
 template <class Epi, bool DUAL>
 cudaError_t set_smem_attr(int num_sms) {
   cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<Epi, DUAL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       SMEM_BYTES);
+                                       smem_bytes<Epi>());
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
@@ -722,7 +792,7 @@ cudaError_t set_smem_attr(int num_sms) {
   attr[0].val.clusterDim.z = 1;
   cfg.gridDim = dim3(2 * (num_sms / 2));
   cfg.blockDim = dim3(NUM_THREADS);
-  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cfg.dynamicSmemBytes = smem_bytes<Epi>();
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
@@ -734,7 +804,9 @@ cudaError_t set_smem_attr(int num_sms) {
 
 template <class Epi, bool DUAL>
 cudaError_t launch(const CUtensorMap* a, const CUtensorMap* b, const CUtensorMap* b2, int M, int num_n, int K,
-                   const Epi& epi, int num_sms, int* err, cudaStream_t st) {
+                   const Epi& epi, int num_sms, int* err, cudaStream_t st, const CUtensorMap* c = nullptr) {
+  static_assert(smem_bytes<Epi>() <= 232448, "shared memory per CTA");
+  if (StgOf<Epi>::value > 0 && !c) return cudaErrorInvalidValue;
   const int num_m = (M + BM - 1) / BM;
   const int tiles = ((num_m + 1) / 2) * num_n;  // pair tiles
   if (tiles == 0) return cudaSuccess;
@@ -745,7 +817,7 @@ cudaError_t launch(const CUtensorMap* a, const CUtensorMap* b, const CUtensorMap
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.blockDim = dim3(NUM_THREADS);
-  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cfg.dynamicSmemBytes = smem_bytes<Epi>();
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
@@ -753,12 +825,12 @@ cudaError_t launch(const CUtensorMap* a, const CUtensorMap* b, const CUtensorMap
   const int max_clusters = MaxClusters<Epi, DUAL>::value > 0 ? MaxClusters<Epi, DUAL>::value : num_sms / 2;
   const int pairs = tiles < max_clusters ? tiles : max_clusters;
   cfg.gridDim = dim3(2 * pairs);
-  return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<Epi, DUAL>, *a, *b, *b2, M, num_n, K, epi, err);
+  return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<Epi, DUAL>, *a, *b, *b2, c ? *c : *a, M, num_n, K, epi, err);
 }
 
 }  // namespace
 
-int gemm_tc_smem_bytes() { return SMEM_BYTES; }
+int gemm_tc_smem_bytes() { return smem_bytes<EpiResidAttnT<false>>(); }
 
 template <bool S8>
 cudaError_t gemm_tc_init_set(int num_sms) {
@@ -817,28 +889,29 @@ cudaError_t launch_gemm_qkvg(const Fwd& f, const CUtensorMap* tm_a, const CUtens
 }
 
 cudaError_t launch_gemm_resid_attn(const Fwd& f, const CUtensorMap* tm_a, const CUtensorMap* tm_b, int K, RowSrc x,
-                                   const float* mod_shared, const float* mod_bias, float* h1, const Deq* dq,
-                                   float* pre, int num_sms, int* err, cudaStream_t st) {
+                                   const float* mod_shared, const float* mod_bias, const CUtensorMap* tm_h1,
+                                   const Deq* dq, float* pre, int num_sms, int* err, cudaStream_t st) {
   const int num_n = (f.d + BN - 1) / BN;
   if (dq) {
-    EpiResidAttnT<true> epi{f, x, mod_shared, mod_bias, 2, h1, *dq};
-    return launch<EpiResidAttnT<true>, false>(tm_a, tm_b, tm_b, f.T, num_n, K, epi, num_sms, err, st);
+    EpiResidAttnT<true> epi{f, x, mod_shared, mod_bias, 2, *dq};
+    return launch<EpiResidAttnT<true>, false>(tm_a, tm_b, tm_b, f.T, num_n, K, epi, num_sms, err, st, tm_h1);
   }
-  EpiResidAttnT<false> epi{f, x, mod_shared, mod_bias, 2, h1, Deq{}, pre};
-  return launch<EpiResidAttnT<false>, false>(tm_a, tm_b, tm_b, f.T, num_n, K, epi, num_sms, err, st);
+  EpiResidAttnT<false> epi{f, x, mod_shared, mod_bias, 2, Deq{}, pre};
+  return launch<EpiResidAttnT<false>, false>(tm_a, tm_b, tm_b, f.T, num_n, K, epi, num_sms, err, st, tm_h1);
 }
 
 cudaError_t launch_gemm_resid_mlp(const Fwd& f, const CUtensorMap* tm_a, const CUtensorMap* tm_b, int K,
-                                  const float* h1, const float* mod_shared, const float* mod_bias, void* out,
-                                  const Deq* dq, float* pre, int num_sms, int* err, cudaStream_t st) {
+                                  const float* h1, const float* mod_shared, const float* mod_bias,
+                                  const CUtensorMap* tm_out, const Deq* dq, float* pre, int num_sms, int* err,
+                                  cudaStream_t st) {
   const int num_n = (f.d + BN - 1) / BN;
   const RowSrc res{nullptr, nullptr, h1};
   if (dq) {
-    EpiResidMlpT<true> epi{f, res, mod_shared, mod_bias, 5, reinterpret_cast<bf16*>(out), *dq};
-    return launch<EpiResidMlpT<true>, false>(tm_a, tm_b, tm_b, f.T, num_n, K, epi, num_sms, err, st);
+    EpiResidMlpT<true> epi{f, res, mod_shared, mod_bias, 5, *dq};
+    return launch<EpiResidMlpT<true>, false>(tm_a, tm_b, tm_b, f.T, num_n, K, epi, num_sms, err, st, tm_out);
   }
-  EpiResidMlpT<false> epi{f, res, mod_shared, mod_bias, 5, reinterpret_cast<bf16*>(out), Deq{}, pre};
-  return launch<EpiResidMlpT<false>, false>(tm_a, tm_b, tm_b, f.T, num_n, K, epi, num_sms, err, st);
+  EpiResidMlpT<false> epi{f, res, mod_shared, mod_bias, 5, Deq{}, pre};
+  return launch<EpiResidMlpT<false>, false>(tm_a, tm_b, tm_b, f.T, num_n, K, epi, num_sms, err, st, tm_out);
 }
 
 cudaError_t launch_gemm_swiglu(const Fwd& f, const CUtensorMap* tm_a, const CUtensorMap* tm_gate,

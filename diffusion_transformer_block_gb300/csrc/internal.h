@@ -102,15 +102,17 @@ cudaError_t gemm_tc_init(int num_sms);
 // xn[T,d] x W_qkvg^T -> QK-norm, RoPE, scatter to Q / K / V^T / G
 cudaError_t launch_gemm_qkvg(const Fwd& f, const CUtensorMap* tm_a, const CUtensorMap* tm_b, int N,
                              const QkvgDst& dst, const Deq* dq, int num_sms, int* err, cudaStream_t st);
-// h1[T,d] (fp32) = x (bf16, split buffers) + gate_a * (A W^T); pre (optional, bf16 mode,
-// fp32 [T,d]) gets A W^T
+// h1[T,d] (fp32) = x (bf16, split buffers) + gate_a * (A W^T), stored through tm_h1 (fp32
+// [T, d], box 32 x 32, 128-byte swizzle); pre (optional, bf16 mode, fp32 [T,d]) gets A W^T
 cudaError_t launch_gemm_resid_attn(const Fwd& f, const CUtensorMap* tm_a, const CUtensorMap* tm_b, int K, RowSrc x,
-                                   const float* mod_shared, const float* mod_bias, float* h1, const Deq* dq,
-                                   float* pre, int num_sms, int* err, cudaStream_t st);
-// out[T,d] (bf16) = h1 (fp32) + gate_m * (A W^T); pre as above
+                                   const float* mod_shared, const float* mod_bias, const CUtensorMap* tm_h1,
+                                   const Deq* dq, float* pre, int num_sms, int* err, cudaStream_t st);
+// out[T,d] (bf16) = h1 (fp32) + gate_m * (A W^T), stored through tm_out (bf16 [T, d], box
+// 64 x 32, 128-byte swizzle); pre as above
 cudaError_t launch_gemm_resid_mlp(const Fwd& f, const CUtensorMap* tm_a, const CUtensorMap* tm_b, int K,
-                                  const float* h1, const float* mod_shared, const float* mod_bias, void* out,
-                                  const Deq* dq, float* pre, int num_sms, int* err, cudaStream_t st);
+                                  const float* h1, const float* mod_shared, const float* mod_bias,
+                                  const CUtensorMap* tm_out, const Deq* dq, float* pre, int num_sms, int* err,
+                                  cudaStream_t st);
 // hmid[T,F] = silu(hn W_gate^T) * (hn W_up^T); rowamax (optional, pre-zeroed [T]) gets
 // each row's largest |hmid| as stored (bf16); pre_a / pre_u (optional, bf16 mode, fp32
 // [T,F]) get the two products
