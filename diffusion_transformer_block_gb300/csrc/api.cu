@@ -460,6 +460,15 @@ int krea_dit_timestep_embed(krea_dit_block_t h, const float* t, int B, const kre
 namespace {
 // Shared body of the split-input and joint-input forwards. `x_joint` non-null selects
 // the joint input [B, L, d] (then x_img / x_txt are ignored) and allows out == x_joint.
+// 3D maps over [B, L, n_q*hd] of the gate pre-activation (box 64 x 128 rows: the attention
+// epilogue loads a query tile's gate with it; only with the gate) and of the attention
+// output (box 64 x 32 rows: the epilogue's stores)
+bool encode_attn_gate_out(CUtensorMap* tm_g, CUtensorMap* tm_og, krea_dit_block_t h, int B, int L) {
+  const uint64_t nq = static_cast<uint64_t>(h->cfg.n_q) * h->cfg.head_dim;
+  if (h->cfg.gate_on && !encode_3d(tm_g, h->g, nq, L, B, nq, 64, 128)) return false;
+  return encode_3d(tm_og, h->og, nq, L, B, nq, 64, 32);
+}
+
 int forward_impl(krea_dit_block_t h, const void* x_img, const void* x_txt, const void* x_joint, int B, int img_h,
                  int img_w, int n_txt, const float* t_emb, const krea_dit_weights* w, const krea_dit_weights8* w8,
                  void* out, krea_dit_stream_t stream) {
@@ -544,7 +553,7 @@ int forward_impl(krea_dit_block_t h, const void* x_img, const void* x_txt, const
     const int per_row = h->mode8 == 2;
     const uint64_t T = static_cast<uint64_t>(f.T);
     CUtensorMap tm_xn8, tm_wqkvg, tm_og8, tm_wo, tm_hn8, tm_wgate, tm_wup, tm_hmid8, tm_wdown, tm_q, tm_k, tm_vt,
-        tm_h1, tm_out;
+        tm_h1, tm_out, tm_g, tm_og;
     bool ok = encode_2d_u8(&tm_xn8, h->xn8, d, T, 128) && encode_2d_u8(&tm_wqkvg, w8->w_qkvg, d, h->n_qkvg, 128) &&
               encode_2d_u8(&tm_og8, h->og8, nqhd, T, 128) && encode_2d_u8(&tm_wo, w8->w_o, nqhd, d, 128) &&
               encode_2d_u8(&tm_hn8, h->hn8, d, T, 128) && encode_2d_u8(&tm_wgate, w8->w_gate, d, c.ffn, 128) &&
@@ -553,7 +562,8 @@ int forward_impl(krea_dit_block_t h, const void* x_img, const void* x_txt, const
               encode_3d(&tm_q, h->q, c.head_dim, L, static_cast<uint64_t>(B) * c.n_q, c.head_dim, 64, 128) &&
               encode_3d(&tm_k, h->k, c.head_dim, L, static_cast<uint64_t>(B) * c.n_kv, c.head_dim, 64, 128) &&
               encode_3d(&tm_vt, h->vt, L, c.head_dim, static_cast<uint64_t>(B) * c.n_kv, f.Lp, 64, 128) &&
-              encode_2d_f32(&tm_h1, h->h1, d, T) && encode_2d(&tm_out, out, d, T, d, 64, 32);
+              encode_2d_f32(&tm_h1, h->h1, d, T) && encode_2d(&tm_out, out, d, T, d, 64, 32) &&
+              encode_attn_gate_out(&tm_g, &tm_og, h, B, L);
     if (!ok) return KREA_DIT_ERR_CUDA;
     const int sms = h->num_sms;
     // row amax accumulators of the attention and SwiGLU outputs (atomic max from zero)
@@ -574,7 +584,8 @@ int forward_impl(krea_dit_block_t h, const void* x_img, const void* x_txt, const
     KD_RUN(S_NORM1, kd::launch_norm_modulate(kd::NormIO::BF16_BF16, f, xsrc, w->norm1_w, t_emb, w->mod_bias, 0, 1,
                                              nullptr, sms, st, &q_xn));
     KD_RUN(S_QKVG_TC, kd::launch_gemm_qkvg(f, &tm_xn8, &tm_wqkvg, h->n_qkvg, dst, &dq_qkvg, sms, h->err, st));
-    KD_RUN(S_ATTN, kd::launch_attn_tc(f, &tm_q, &tm_k, &tm_vt, h->g, h->og, h->am_og, nullptr, nullptr, sms, h->err, st));
+    KD_RUN(S_ATTN, kd::launch_attn_tc(f, &tm_q, &tm_k, &tm_vt, &tm_g, &tm_og, h->am_og, nullptr, nullptr, sms, h->err,
+                                        st));
     KD_RUN(S_QUANT_OG, kd::launch_quant_e4m3(h->og, f.T, nqhd, h->am_og, per_row, h->og8, h->dq_og, sms, st));
     KD_RUN(S_OPROJ_TC, kd::launch_gemm_resid_attn(f, &tm_og8, &tm_wo, nqhd, xsrc, t_emb, w->mod_bias, &tm_h1, &dq_o,
                                                   nullptr, sms, h->err, st));
@@ -591,7 +602,7 @@ int forward_impl(krea_dit_block_t h, const void* x_img, const void* x_txt, const
                                                 t_emb, w->mod_bias, &tm_out, &dq_down, nullptr, sms, h->err, st));
   } else if (h->bf16) {
     CUtensorMap tm_xn, tm_wqkvg, tm_og, tm_wo, tm_hn, tm_wgate, tm_wup, tm_hmid, tm_wdown, tm_q, tm_k, tm_vt, tm_h1,
-        tm_out;
+        tm_out, tm_g, tm_og_st;
     const uint64_t T = static_cast<uint64_t>(f.T);
     bool ok = encode_2d(&tm_xn, h->xn, d, T, d, 64, 128) &&
               encode_2d(&tm_wqkvg, w->w_qkvg, d, h->n_qkvg, d, 64, 128) &&
@@ -604,13 +615,14 @@ int forward_impl(krea_dit_block_t h, const void* x_img, const void* x_txt, const
               encode_3d(&tm_q, h->q, c.head_dim, L, static_cast<uint64_t>(B) * c.n_q, c.head_dim, 64, 128) &&
               encode_3d(&tm_k, h->k, c.head_dim, L, static_cast<uint64_t>(B) * c.n_kv, c.head_dim, 64, 128) &&
               encode_3d(&tm_vt, h->vt, L, c.head_dim, static_cast<uint64_t>(B) * c.n_kv, f.Lp, 64, 128) &&
-              encode_2d_f32(&tm_h1, h->h1, d, T) && encode_2d(&tm_out, out, d, T, d, 64, 32);
+              encode_2d_f32(&tm_h1, h->h1, d, T) && encode_2d(&tm_out, out, d, T, d, 64, 32) &&
+              encode_attn_gate_out(&tm_g, &tm_og_st, h, B, L);
     if (!ok) return KREA_DIT_ERR_CUDA;
     const int sms = h->num_sms;
     KD_RUN(S_NORM1, kd::launch_norm_modulate(kd::NormIO::BF16_BF16, f, xsrc, w->norm1_w, t_emb, w->mod_bias, 0, 1,
                                              h->xn, sms, st));
     KD_RUN(S_QKVG_TC, kd::launch_gemm_qkvg(f, &tm_xn, &tm_wqkvg, h->n_qkvg, dst, nullptr, sms, h->err, st));
-    KD_RUN(S_ATTN, kd::launch_attn_tc(f, &tm_q, &tm_k, &tm_vt, h->g, h->og, nullptr, h->bw_stats ? h->f_lse : nullptr,
+    KD_RUN(S_ATTN, kd::launch_attn_tc(f, &tm_q, &tm_k, &tm_vt, &tm_g, &tm_og_st, nullptr, h->bw_stats ? h->f_lse : nullptr,
                                         h->bw_stats ? h->f_o : nullptr, sms, h->err, st));
     KD_RUN(S_OPROJ_TC, kd::launch_gemm_resid_attn(f, &tm_og, &tm_wo, nqhd, xsrc, t_emb, w->mod_bias, &tm_h1, nullptr,
                                                   h->bw_stats ? h->f_fa : nullptr, sms, h->err, st));

@@ -18,7 +18,11 @@
 // is raised only when a row's tile max exceeds it by more than 2^8, so most tiles skip
 // the rescale. The two tiles ping-pong: the tensor core runs one tile's products while
 // the other tile's softmax runs.
-// Epilogue: O_t / l_t * sigmoid(g) -> bf16 [T, n_q*hd].
+// Epilogue: O_t / l_t * sigmoid(g) -> bf16 [T, n_q*hd]. Once S_t of the last K/V tile has
+// landed, Q_t is no longer read, so its buffer takes the gate tile (one TMA load issued by
+// the softmax warpgroup while the last P V runs); each thread then overwrites its row of
+// the gate with the gated output, and every warp hands its 32 rows to a TMA store. The
+// gate never waits on a DRAM round trip per row and the output leaves as whole lines.
 //
 // Warps 0-3: softmax/epilogue for tile 0, warps 4-7: tile 1, warp 8: TMA loads,
 // warp 9: TMEM allocation + MMA issue for tile 0, warp 10: MMA issue for tile 1. The
@@ -50,8 +54,6 @@ constexpr float RESCALE_THRESHOLD = 8.0f;  // log2 units: rescale O only if the 
 struct AttnArgs {
   int B, L, Lp, n_q, n_kv, G, nqt, nkt, npairs, gate_on;
   float scale_log2;  // log2(e) / sqrt(hd)
-  const bf16* g;     // [T, n_q*hd] gate pre-activation
-  bf16* og;          // [T, n_q*hd]
   float* rowamax;    // optional [T]: largest |og| of each row, as stored (for an 8-bit o_proj)
   float* lse;        // optional [B, n_q, Lp]: log2 of each row's softmax normaliser, in the
                      // scaled-log2 units of the scores (for the backward)
@@ -83,7 +85,8 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, int* 
 
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                   const __grid_constant__ CUtensorMap tm_vt, AttnArgs a) {
+                   const __grid_constant__ CUtensorMap tm_vt, const __grid_constant__ CUtensorMap tm_g,
+                   const __grid_constant__ CUtensorMap tm_og, AttnArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + SMEM_BAR);
@@ -95,7 +98,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   uint64_t* o_done = p_full + 2;            // [2] the last O_t += P_t V landed
   uint64_t* done = o_done + 2;              // [2] every MMA of issuing thread t finished
   uint64_t* turn = done + 2;                // [2] turn[t]: the other issuer finished its MMAs
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(turn + 2);
+  uint64_t* g_full = turn + 2;              // [2] the gate tile of query tile t is in Q_t's buffer
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(g_full + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -124,6 +128,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       mbar_init(&o_done[t], 1);
       mbar_init(&done[t], 1);
       mbar_init(&turn[t], 1);
+      mbar_init(&g_full[t], 1);
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -257,12 +262,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
       const uint32_t tS = tmem + lane_off + t * 128;
       const uint32_t tO = tmem + lane_off + 256 + t * 128;
+      uint8_t* qbuf = smem + SMEM_Q + t * TILE_BYTES;  // Q_t, then the gate / output tile
       float m_run = -INFINITY, l_run = 0.f;
       bool ok = true;
+      bool g_issued = false;  // (quad 0, lane 0) the gate tile's load was started
       for (int j = 0; j < nkt; ++j) {
         const bool got = mbar_wait(&s_full[t], static_cast<uint32_t>(j & 1), wc, SITE_ATTN_SOFTMAX);
         if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
         tc_fence_after();
+        if (j == nkt - 1 && a.gate_on && quad == 0 && lane == 0) {
+          // the last S_t landed, so no MMA reads Q_t any more: its buffer takes the gate tile
+          mbar_arrive_expect_tx(&g_full[t], TILE_BYTES);
+          for (int kh = 0; kh < 2; ++kh)
+            tma_load_3d(qbuf + kh * HALF_BYTES, &tm_g, &g_full[t], tile_head(t) * HD + kh * 64, tile_qt(t) * BQ, b);
+          g_issued = true;
+        }
         uint32_t sv[128];
         tmem_ld128(tS, sv);
         const int kvalid = a.L - j * BKV;  // keys of this tile inside the sequence (>= 1)
@@ -325,10 +339,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         tc_fence_before();
         mbar_arrive(&p_full[t]);
       }
-      // ---- epilogue: wait for the last P V, O / l * sigmoid(g) -> og
+      // ---- epilogue: wait for the last P V (and the gate tile), O / l * sigmoid(g) -> og
       if (ok) {
         const bool w4 = mbar_wait(&o_done[t], 0, wc, SITE_ATTN_SOFTMAX);
         ok = __all_sync(0xffffffffu, w4);
+      }
+      if (ok && a.gate_on) {
+        const bool wg = mbar_wait(&g_full[t], 0, wc, SITE_ATTN_SOFTMAX);
+        ok = __all_sync(0xffffffffu, wg);
       }
       if (ok) {
         tc_fence_after();
@@ -337,44 +355,57 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const float inv_l = 1.0f / l_run;
         const size_t off =
             (static_cast<size_t>(b) * a.L + (valid ? ql : 0)) * (a.n_q * HD) + tile_head(t) * HD;
+        // this row in the two 64-column halves of the tile (128-byte swizzle: unit u of
+        // row r sits at u ^ (r & 7))
+        uint8_t* rb = qbuf + row * 128;
+        const int sw = row & 7;
         float amax = 0.0f;
-        uint32_t r[32];
-#pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-          tmem_ld32(tO + c * 32, r);
-          if (valid) {
-            float o[32];
+        // one 32-column chunk c of O (in r): scale, gate, write back over the gate in place
+        auto chunk = [&](const uint32_t (&r)[32], int c) {
+          float o[32];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] = __uint_as_float(r[i]) * inv_l;
-            if (a.o_raw) {
-              float4* w4 = reinterpret_cast<float4*>(a.o_raw + off + c * 32);
+          for (int i = 0; i < 32; ++i) o[i] = __uint_as_float(r[i]) * inv_l;
+          if (a.o_raw && valid) {
+            float4* w4 = reinterpret_cast<float4*>(a.o_raw + off + c * 32);
 #pragma unroll
-              for (int q = 0; q < 8; ++q) w4[q] = make_float4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
-            }
+            for (int q = 0; q < 8; ++q) w4[q] = make_float4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+          }
+          uint8_t* hb = rb + (c >> 1) * HALF_BYTES;
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            uint4* p16 = reinterpret_cast<uint4*>(hb + ((((c & 1) * 4 + q4) ^ sw) << 4));
             if (a.gate_on) {
-              const uint4* g4 = reinterpret_cast<const uint4*>(a.g + off + c * 32);
+              const uint4 u = *p16;
+              const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-              for (int q4 = 0; q4 < 4; ++q4) {
-                const uint4 u = __ldg(g4 + q4);
-                const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                  const float2 gg = unpack_bf16x2(w4[e]);
-                  o[8 * q4 + 2 * e] *= sigmoidf_(gg.x);
-                  o[8 * q4 + 2 * e + 1] *= sigmoidf_(gg.y);
-                }
+              for (int e = 0; e < 4; ++e) {
+                const float2 gg = unpack_bf16x2(w4[e]);
+                o[8 * q4 + 2 * e] *= sigmoid_fast(gg.x);
+                o[8 * q4 + 2 * e + 1] *= sigmoid_fast(gg.y);
               }
             }
-            uint4* o4 = reinterpret_cast<uint4*>(a.og + off + c * 32);
-#pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4)
-              o4[q4] = make_uint4(pack_bf16x2(o[8 * q4 + 0], o[8 * q4 + 1]), pack_bf16x2(o[8 * q4 + 2], o[8 * q4 + 3]),
-                                  pack_bf16x2(o[8 * q4 + 4], o[8 * q4 + 5]), pack_bf16x2(o[8 * q4 + 6], o[8 * q4 + 7]));
-            if (a.rowamax) {
-#pragma unroll
-              for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(o[i]));
-            }
+            *p16 = make_uint4(pack_bf16x2(o[8 * q4 + 0], o[8 * q4 + 1]), pack_bf16x2(o[8 * q4 + 2], o[8 * q4 + 3]),
+                              pack_bf16x2(o[8 * q4 + 4], o[8 * q4 + 5]), pack_bf16x2(o[8 * q4 + 6], o[8 * q4 + 7]));
           }
+          if (a.rowamax && valid) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(o[i]));
+          }
+        };
+#pragma unroll 1
+        for (int cc = 0; cc < 2; ++cc) {  // two TMEM round trips of 64 columns
+          uint32_t ra[32], rb2[32];
+          tmem_ld32x2(tO + cc * 64, tO + cc * 64 + 32, ra, rb2);
+          chunk(ra, 2 * cc);
+          chunk(rb2, 2 * cc + 1);
+        }
+        fence_proxy_async_smem();  // the rows are visible to the TMA engine
+        __syncwarp();
+        const int r0 = tile_qt(t) * BQ + quad * 32;  // first sequence row of this warp's 32 rows
+        if (lane == 0 && r0 < a.L) {  // rows past L are clipped by the store (3D map over [B, L, .])
+          for (int kh = 0; kh < 2; ++kh)
+            tma_store_3d(&tm_og, qbuf + kh * HALF_BYTES + quad * 32 * 128, tile_head(t) * HD + kh * 64, r0, b);
+          bulk_commit();
         }
         // bf16 rounding is monotone, so the largest stored magnitude is the rounded largest
         if (a.lse && valid)
@@ -382,6 +413,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (a.rowamax && valid)
           atomic_max_nonneg(a.rowamax + static_cast<size_t>(b) * a.L + ql, round_bf16(amax));
       }
+      // the gate load (if started) and this warp's output stores have completed before exit
+      if (g_issued) drain_wait(&g_full[t], 0, a.err, SITE_ATTN_TEARDOWN);
+      if (lane == 0) bulk_wait_all();
+      __syncwarp();
       tc_fence_before();
     }
   }
@@ -400,8 +435,8 @@ cudaError_t attn_tc_init() {
 }
 
 cudaError_t launch_attn_tc(const Fwd& f, const CUtensorMap* tm_q, const CUtensorMap* tm_k, const CUtensorMap* tm_vt,
-                           const void* g, void* og, float* rowamax, float* lse, float* o_raw, int num_sms, int* err,
-                           cudaStream_t st) {
+                           const CUtensorMap* tm_g, const CUtensorMap* tm_og, float* rowamax, float* lse, float* o_raw,
+                           int num_sms, int* err, cudaStream_t st) {
   (void)num_sms;
   AttnArgs a;
   a.B = f.B;
@@ -415,15 +450,15 @@ cudaError_t launch_attn_tc(const Fwd& f, const CUtensorMap* tm_q, const CUtensor
   a.npairs = (a.G * a.nqt + 1) / 2;
   a.gate_on = f.gate_on;
   a.scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(HD));
-  a.g = reinterpret_cast<const bf16*>(g);
-  a.og = reinterpret_cast<bf16*>(og);
   a.rowamax = rowamax;
   a.lse = lse;
   a.o_raw = o_raw;
   a.err = err;
   const long long units = static_cast<long long>(f.B) * f.n_kv * a.npairs;
   if (units == 0) return cudaSuccess;
-  attn_tc_kernel<<<static_cast<unsigned>(units), NUM_THREADS, SMEM_BYTES, st>>>(*tm_q, *tm_k, *tm_vt, a);
+  if (!tm_og || (f.gate_on && !tm_g)) return cudaErrorInvalidValue;
+  attn_tc_kernel<<<static_cast<unsigned>(units), NUM_THREADS, SMEM_BYTES, st>>>(*tm_q, *tm_k, *tm_vt,
+                                                                                f.gate_on ? *tm_g : *tm_q, *tm_og, a);
   return cudaGetLastError();
 }
 

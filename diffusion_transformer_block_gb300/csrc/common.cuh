@@ -55,6 +55,14 @@ __device__ __forceinline__ float warp_max(float v) {
 // few ulp, far below the bf16 storage rounding that follows).
 __device__ __forceinline__ float sigmoidf_(float x) { return 1.0f / (1.0f + __expf(-x)); }
 __device__ __forceinline__ float siluf_(float x) { return x / (1.0f + __expf(-x)); }
+// sigmoid from the hardware's approximate 2^x and reciprocal (relative error a few 1e-7,
+// far below bf16 rounding): 1 / (1 + 2^(-x log2 e)); saturates to 0 and 1 at the ends
+__device__ __forceinline__ float sigmoid_fast(float x) {
+  float e, y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(-1.4426950408889634f * x));
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(1.0f + e));
+  return y;
+}
 
 // ------------------------------------------------------------------ error sites
 // Bits written to the device error word when a bounded wait gives up.
@@ -168,6 +176,11 @@ __device__ __forceinline__ void tma_load_2d_mc(void* dst, const void* map, uint6
 __device__ __forceinline__ void tma_store_2d(const void* map, const void* src, int x, int y) {
   asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(map),
                "r"(smem_u32(src)), "r"(x), "r"(y)
+               : "memory");
+}
+__device__ __forceinline__ void tma_store_3d(const void* map, const void* src, int x, int y, int z) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(map),
+               "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z)
                : "memory");
 }
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }

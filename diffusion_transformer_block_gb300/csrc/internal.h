@@ -139,14 +139,16 @@ cudaError_t launch_gemm_plain(const CUtensorMap* tm_a, const CUtensorMap* tm_b, 
 
 // ---- attn_tc.cu (bf16 mode, tcgen05 + TMA) ----
 cudaError_t attn_tc_init();
-// og = softmax(q k^T / sqrt(hd)) v * sigmoid(g); rowamax (optional, pre-zeroed [T]) gets
-// each row's largest |og| as stored (bf16)
+// og = softmax(q k^T / sqrt(hd)) v * sigmoid(g); g is read through tm_g and og written
+// through tm_og, both 3D bf16 maps over [B, L, n_q*hd] with the 128-byte swizzle (box 64 x
+// 128 rows for g, 64 x 32 rows for og; tm_g unused without the gate); rowamax (optional,
+// pre-zeroed [T]) gets each row's largest |og| as stored (bf16)
 // lse (optional, [B, n_q, Lp]: row pitch Lp) gets m + log2(l) per row in the scores'
 // scaled-log2 units, o_raw (optional, fp32 [T, n_q*hd]) the output before the gate; both
 // for the backward
 cudaError_t launch_attn_tc(const Fwd& f, const CUtensorMap* tm_q, const CUtensorMap* tm_k, const CUtensorMap* tm_vt,
-                           const void* g, void* og, float* rowamax, float* lse, float* o_raw, int num_sms, int* err,
-                           cudaStream_t st);
+                           const CUtensorMap* tm_g, const CUtensorMap* tm_og, float* rowamax, float* lse, float* o_raw,
+                           int num_sms, int* err, cudaStream_t st);
 
 // ---- attn_bwd.cu (flash-style attention backward, tcgen05 + TMA) ----
 cudaError_t attn_bwd_init();
