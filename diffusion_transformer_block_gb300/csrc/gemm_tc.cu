@@ -399,7 +399,7 @@ struct EpiSwiGLUT {
           float h[8];
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
-            h[i] = siluf_(u2f(rg[8 * q4 + i])) * u2f(ru[8 * q4 + i]);
+            h[i] = u2f(rg[8 * q4 + i]) * sigmoid_fast(u2f(rg[8 * q4 + i])) * u2f(ru[8 * q4 + i]);
             if constexpr (S8) amax = fmaxf(amax, fabsf(h[i]));
           }
           o4[q4] = make_uint4(pack_bf16x2(h[0], h[1]), pack_bf16x2(h[2], h[3]), pack_bf16x2(h[4], h[5]),
@@ -449,7 +449,7 @@ struct EpiSwiGLUBwd {
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
             const float dh = u2f(r[8 * q + i]);
-            const float sg = 1.0f / (1.0f + __expf(-av[i]));
+            const float sg = sigmoid_fast(av[i]);
             ga[i] = dh * uv[i] * sg * (1.0f + av[i] * (1.0f - sg));
             gu[i] = dh * av[i] * sg;
           }
@@ -460,7 +460,7 @@ struct EpiSwiGLUBwd {
         }
       } else {
         for (int i = 0; i < F - col; ++i) {
-          const float dh = u2f(r[i]), av = a[off + i], sg = 1.0f / (1.0f + __expf(-av));
+          const float dh = u2f(r[i]), av = a[off + i], sg = sigmoid_fast(av);
           da[i] = __float2bfloat16_rn(dh * u[off + i] * sg * (1.0f + av * (1.0f - sg)));
           da[F + i] = __float2bfloat16_rn(dh * av * sg);
         }
@@ -512,7 +512,7 @@ struct EpiGateBwd {
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const float2 gg = unpack_bf16x2(gw[e]);
-            const float s0 = sigmoidf_(gg.x), s1 = sigmoidf_(gg.y);
+            const float s0 = sigmoid_fast(gg.x), s1 = sigmoid_fast(gg.y);
             const float a0 = u2f(r[8 * q + 2 * e]), a1 = u2f(r[8 * q + 2 * e + 1]);
             dov[2 * e] = a0 * s0;
             dov[2 * e + 1] = a1 * s1;
