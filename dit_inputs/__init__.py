@@ -100,6 +100,9 @@ CONFIGS["small_txtonly"] = _cfg("small_txtonly", 2, 0, 0, 45, 512, 4, 2, 128, 14
 # Odd number of query tiles per KV group (G = 3, 3 tiles): one-tile attention units, and
 # 160 units (more than one per SM), so a persistent CTA meets both kinds in one sequence.
 CONFIGS["units_odd"] = _cfg("units_odd", 32, 16, 16, 44, 384, 3, 1, 128, 1024, "bf16", 17)
+# Many attention units per persistent CTA (64 x 2 KV groups x 5 units = 640 on 152 SMs),
+# a one-tile unit closing every KV group and a ragged last query / key tile (L = 300).
+CONFIGS["units_many"] = _cfg("units_many", 64, 16, 16, 44, 256, 6, 2, 128, 512, "bf16", 18)
 CONFIGS["tiny_ragged32"] = _cfg("tiny_ragged32", 2, 5, 7, 9, 192, 3, 1, 64, 320, "fp32", 15)
 CONFIGS["small_fp32_hd128"] = _cfg("small_fp32_hd128", 1, 9, 11, 13, 256, 2, 1, 128, 704, "fp32", 16)
 
