@@ -460,7 +460,7 @@ int krea_dit_timestep_embed(krea_dit_block_t h, const float* t, int B, const kre
 namespace {
 // Shared body of the split-input and joint-input forwards. `x_joint` non-null selects
 // the joint input [B, L, d] (then x_img / x_txt are ignored) and allows out == x_joint.
-// 3D maps over [B, L, n_q*hd] of the gate pre-activation (box 64 x 128 rows: the attention
+// 3D maps over [B, L, n_q*hd] of the gate value (box 64 x 128 rows: the attention
 // epilogue loads a query tile's gate with it; only with the gate) and of the attention
 // output (box 64 x 32 rows: the epilogue's stores)
 bool encode_attn_gate_out(CUtensorMap* tm_g, CUtensorMap* tm_og, krea_dit_block_t h, int B, int L) {

@@ -18,11 +18,11 @@
 // is raised only when a row's tile max exceeds it by more than 2^8, so most tiles skip
 // the rescale. The two tiles ping-pong: the tensor core runs one tile's products while
 // the other tile's softmax runs.
-// Epilogue: O_t / l_t * sigmoid(g) -> bf16 [T, n_q*hd]. The softmax warps read O_t into
-// registers and hand it back at once (the next unit's first P V may overwrite it); the
-// gate tile arrives by TMA in a ring slot after the unit's last V, each thread overwrites
-// its row of it with the gated output, and every warp TMA-stores its 32 rows; the sigmoid
-// is 1 / (1 + 2^(-x log2 e)) from the approximate exp2 and reciprocal.
+// Epilogue: O_t / l_t * s -> bf16 [T, n_q*hd], s = sigmoid(xn W_g^T) as the QKV+G
+// projection stored it (so no exponential is left here). The softmax warps read O_t into
+// registers and hand it back (the next unit's first P V may overwrite it); the gate tile
+// arrives by TMA in a ring slot after the unit's last V, each thread overwrites its row
+// of it with the gated output, and every warp TMA-stores its 32 rows.
 //
 // Persistent: one CTA per SM walks the units u = blockIdx.x, + gridDim.x, ... with one
 // TMEM allocation and one set of barriers, and every barrier phase is counted across
@@ -423,7 +423,7 @@ __global__ void __maxnreg__(184)
         mbar_arrive(&p_full[t]);
       }
       if (!ok) break;
-      // ---- epilogue: O_t / l * sigmoid(g) -> og. O_t is handed back once it is all in
+      // ---- epilogue: O_t / l * s -> og (s: the stored gate). O_t is handed back once it is all in
       // registers; the gate tile (or an empty staging slot) is the ring slot after this
       // unit's last V.
       const bool w4 = mbar_wait(&o_done[t], static_cast<uint32_t>(uq & 1), wc, SITE_ATTN_SOFTMAX);
@@ -464,8 +464,8 @@ __global__ void __maxnreg__(184)
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               const float2 gg = unpack_bf16x2(gw[e]);
-              o[8 * q4 + 2 * e] *= sigmoid_fast(gg.x);
-              o[8 * q4 + 2 * e + 1] *= sigmoid_fast(gg.y);
+              o[8 * q4 + 2 * e] *= gg.x;
+              o[8 * q4 + 2 * e + 1] *= gg.y;
             }
           }
           *p16 = make_uint4(pack_bf16x2(o[8 * q4 + 0], o[8 * q4 + 1]), pack_bf16x2(o[8 * q4 + 2], o[8 * q4 + 3]),

@@ -221,13 +221,16 @@ struct EpiQKVGT {
         tmem_ld32(t0 + c * 32, r);
         deq32<S8>(r, dq, fa, dq.b, n0 + c * 32);
         if (ok) {
+          // the gate value sigmoid(xn W_g^T) itself: the attention epilogue and the gate
+          // backward only multiply by it
+          float sg[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) sg[i] = sigmoid_fast(u2f(r[i]));
           uint4* o4 = reinterpret_cast<uint4*>(g + c * 32);
 #pragma unroll
           for (int q4 = 0; q4 < 4; ++q4)
-            o4[q4] = make_uint4(pack_bf16x2(u2f(r[8 * q4 + 0]), u2f(r[8 * q4 + 1])),
-                                pack_bf16x2(u2f(r[8 * q4 + 2]), u2f(r[8 * q4 + 3])),
-                                pack_bf16x2(u2f(r[8 * q4 + 4]), u2f(r[8 * q4 + 5])),
-                                pack_bf16x2(u2f(r[8 * q4 + 6]), u2f(r[8 * q4 + 7])));
+            o4[q4] = make_uint4(pack_bf16x2(sg[8 * q4 + 0], sg[8 * q4 + 1]), pack_bf16x2(sg[8 * q4 + 2], sg[8 * q4 + 3]),
+                                pack_bf16x2(sg[8 * q4 + 4], sg[8 * q4 + 5]), pack_bf16x2(sg[8 * q4 + 6], sg[8 * q4 + 7]));
         }
       }
     }
@@ -470,16 +473,17 @@ struct EpiSwiGLUBwd {
 };
 
 // Output-gate backward finished in the epilogue of d_og = d_fa W_o (one 128-column half of
-// a tile is one head): with og = o sigmoid(g), d_o = d_og sigmoid(g) goes as bf16 to the
-// head-major [B, n_q, L, 128] buffer the attention backward reads, the gate's gradient
-// d_og o sigmoid(g) (1 - sigmoid(g)) to d_P's g columns (bf16, from column goff), and the
+// a tile is one head): with og = o s, s = sigmoid(g) as the forward stored it, d_o = d_og s
+// goes as bf16 to the head-major [B, n_q, L, 128] buffer the attention backward reads,
+// the gradient of the pre-activation d_og o s (1 - s) to d_P's g columns (bf16, from
+// column goff), and the
 // softmax row term D = sum over the head of d_o (as stored) times o to D[b, head, l] (row
 // pitch Lp). Without the gate, d_o = d_og.
 struct EpiGateBwd {
   static constexpr bool kS8 = false;
   Fwd f;
   const float* o;    // [T, n_q*128] fp32, the ungated attention output
-  const bf16* g;     // [T, n_q*128] gate pre-activation
+  const bf16* g;     // [T, n_q*128] the gate value sigmoid(xn W_g^T)
   bf16* d_o;         // [B, n_q, L, 128]
   bf16* d_P;         // [T, ldp]
   int ldp, goff;
@@ -512,7 +516,7 @@ struct EpiGateBwd {
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const float2 gg = unpack_bf16x2(gw[e]);
-            const float s0 = sigmoid_fast(gg.x), s1 = sigmoid_fast(gg.y);
+            const float s0 = gg.x, s1 = gg.y;  // the stored gate values
             const float a0 = u2f(r[8 * q + 2 * e]), a1 = u2f(r[8 * q + 2 * e + 1]);
             dov[2 * e] = a0 * s0;
             dov[2 * e + 1] = a1 * s1;

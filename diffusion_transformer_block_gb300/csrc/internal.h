@@ -139,7 +139,8 @@ cudaError_t launch_gemm_plain(const CUtensorMap* tm_a, const CUtensorMap* tm_b, 
 
 // ---- attn_tc.cu (bf16 mode, tcgen05 + TMA) ----
 cudaError_t attn_tc_init();
-// og = softmax(q k^T / sqrt(hd)) v * sigmoid(g); g is read through tm_g and og written
+// og = softmax(q k^T / sqrt(hd)) v * s with s = sigmoid(xn W_g^T) as stored by the QKV+G
+// projection; s is read through tm_g and og written
 // through tm_og, both 3D bf16 maps over [B, L, n_q*hd] with the 128-byte swizzle (box 64 x
 // 128 rows for g, 64 x 32 rows for og; tm_g unused without the gate); rowamax (optional,
 // pre-zeroed [T]) gets each row's largest |og| as stored (bf16)

@@ -145,7 +145,7 @@ __global__ void qkvg_post_f32_kernel(Fwd f, const float* __restrict__ raw, QkvgD
   } else {
     float* g = reinterpret_cast<float*>(dst.g);
 #pragma unroll
-    for (int i = 0; i < E; ++i) g[static_cast<size_t>(m) * f.n_q * hd + head * hd + lane * E + i] = v[i];
+    for (int i = 0; i < E; ++i) g[static_cast<size_t>(m) * f.n_q * hd + head * hd + lane * E + i] = sigmoidf_(v[i]);
   }
 }
 
@@ -201,7 +201,7 @@ __global__ void __launch_bounds__(128) attn_simt_kernel(Fwd f, const T* __restri
 #pragma unroll
   for (int i = 0; i < E; ++i) {
     float o = acc[i] / den;
-    if (f.gate_on) o *= sigmoidf_(Conv<T>::to_f(g[o_off + i]));
+    if (f.gate_on) o *= Conv<T>::to_f(g[o_off + i]);  // g holds the gate value
     og[o_off + i] = Conv<T>::from_f(o);
   }
 }

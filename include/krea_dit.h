@@ -340,7 +340,7 @@ int krea_dit_block_host_sync(krea_dit_block_t h);
  *  Q    [B, n_q, L, hd]    dtype, after QK-norm and RoPE
  *  K    [B, n_kv, L, hd]   dtype, after QK-norm and RoPE
  *  VT   [B, n_kv, hd, Lp]  dtype, values transposed, Lp = L rounded up to 64
- *  G    [T, n_q hd]        dtype, gate pre-activation (unused when gate_on = 0)
+ *  G    [T, n_q hd]        dtype, the gate sigmoid(xn W_g^T) (unused when gate_on = 0)
  *  OG   [T, n_q hd]        dtype, o * sigmoid(g)
  *  H1   [T, d]             fp32 in both modes, block state after the attention residual
  *                          (the residual stream between the two residual adds)

@@ -104,8 +104,8 @@ def forward_saved(X: np.ndarray, mod: Dict[str, np.ndarray], w: Dict[str, np.nda
     s["A"] = A
     s["o"] = o.transpose(1, 0, 2).reshape(L, qr)
     if gate_on:
-        s["g"] = R("g", P[:, qr + 2 * kr:2 * qr + 2 * kr])
-        s["og"] = R("o_g", s["o"] * sigmoid(s["g"]))
+        s["g"] = R("g", sigmoid(P[:, qr + 2 * kr:2 * qr + 2 * kr]))  # the gate value, as stored
+        s["og"] = R("o_g", s["o"] * s["g"])
     else:
         s["og"] = R("o_g", s["o"])
     s["fa"] = s["og"] @ np.asarray(w["w_o"], F64).T
@@ -153,9 +153,9 @@ def element_backward(s: Dict[str, np.ndarray], dout: np.ndarray, mod: Dict[str, 
     d_fa = d_h1 * mod["gate_a"]
     gw["w_o"] = d_fa.T @ s["og"]
     d_og = d_fa @ f64(w["w_o"])
-    # output gate: og = o * sigmoid(g)
+    # output gate: og = o * sg, sg = sigmoid(x W_g^T); d/dx sigmoid = sg (1 - sg)
     if gate_on:
-        sg = sigmoid(s["g"])
+        sg = s["g"]
         d_o = d_og * sg
         d_g = d_og * s["o"] * sg * (1.0 - sg)
     else:

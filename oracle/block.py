@@ -245,8 +245,9 @@ def block_forward(
     stores stays float64.
 
     Returns a dict of per-batch lists: ``rows`` and, for those rows, q and k
-    (after QK-norm and RoPE, [n_q|n_kv, R, hd]), v, g, o_g ([R, n_q*hd], the
-    gated attention output), h1, hn, hmid (SwiGLU hidden [R, F]) and out [R, d].
+    (after QK-norm and RoPE, [n_q|n_kv, R, hd]), v, g (the gate sigmoid(xn W_g^T),
+    [R, n_q*hd]), o_g ([R, n_q*hd], the gated attention output), h1, hn, hmid (SwiGLU
+    hidden [R, F]) and out [R, d].
     """
     x_txt = np.asarray(x_txt, F64)
     x_img = np.asarray(x_img, F64)
@@ -296,8 +297,10 @@ def block_forward(
         o = gqa_attention(q, k, v)  # [n_q, R, hd]
         o = o.transpose(1, 0, 2).reshape(len(R), n_q * hd)
         if gate_on:
-            g = rnd["g"](xn[R] @ Wg.T)
-            o_g = o * sigmoid(g)  # head-specific elementwise sigmoid gate on the SDPA output
+            # head-specific elementwise sigmoid gate on the SDPA output; g is the gate
+            # value itself, rounded where an implementation stores it
+            g = rnd["g"](sigmoid(xn[R] @ Wg.T))
+            o_g = o * g
         else:
             g = np.zeros_like(o)
             o_g = o

@@ -158,8 +158,8 @@ def block_forward8(
         q, k = rnd["q"](apply_rope_2d(q, ang)), rnd["k"](apply_rope_2d(k, ang))
         o = gqa_attention(q, k, v).transpose(1, 0, 2).reshape(L, qr)
         if gate_on:
-            g = rnd["g"](p[:, qr + 2 * kr:2 * qr + 2 * kr])
-            o_g = o * sigmoid(g)
+            g = rnd["g"](sigmoid(p[:, qr + 2 * kr:2 * qr + 2 * kr]))  # the gate value, as stored
+            o_g = o * g
         else:
             g = np.zeros_like(o)
             o_g = o

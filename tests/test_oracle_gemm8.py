@@ -163,7 +163,7 @@ def textbook_block8(case, ms, per_row: bool):
     q, k = _bf(rope(q)), _bf(rope(k))
     o = Fn.scaled_dot_product_attention(q, k, v, enable_gqa=True).transpose(1, 2).reshape(B, L, qr)
     if cfg.gate_on:
-        o = o * torch.sigmoid(_bf(p[..., qr + 2 * kr:]))
+        o = o * _bf(torch.sigmoid(p[..., qr + 2 * kr:]))  # the gate is stored as its value
     o = _bf(o)
     h1 = _bf(X + mod["gate_a"][:, None] * lin8(o, "w_o"))
     hn = norm_mod(h1, w["norm2_w"], "shift_m", "scale_m")
