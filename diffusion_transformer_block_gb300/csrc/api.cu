@@ -883,7 +883,7 @@ int krea_dit_block_backward(krea_dit_block_t h, const void* x_img, const void* x
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const int sms = h->num_sms;
   const int T = f.T, d = c.d_model, F = c.ffn, hd = c.head_dim, L = f.L;
-  const int nq = c.n_q * hd, nkv = c.n_kv * hd, nqkvg = h->n_qkvg, G = c.n_q / c.n_kv;
+  const int nq = c.n_q * hd, nkv = c.n_kv * hd, nqkvg = h->n_qkvg;
   const int Tp = static_cast<int>(round_up(static_cast<size_t>(T), 64));
   const int Lp = static_cast<int>(round_up(static_cast<size_t>(L), 64));
   const float scale = 1.0f / sqrtf(static_cast<float>(hd));
