@@ -17,7 +17,7 @@ import torch
 import dit_inputs as di
 import oracle
 
-from gpu_helpers import TOL, check_parity, make_block, oracle_pair, parity_report, run_gpu
+from gpu_helpers import check_parity, make_block, oracle_pair, parity_report, run_gpu
 
 pytestmark = pytest.mark.gpu
 
