@@ -103,6 +103,10 @@ CONFIGS["units_odd"] = _cfg("units_odd", 32, 16, 16, 44, 384, 3, 1, 128, 1024, "
 # Many attention units per persistent CTA (64 x 2 KV groups x 5 units = 640 on 152 SMs),
 # a one-tile unit closing every KV group and a ragged last query / key tile (L = 300).
 CONFIGS["units_many"] = _cfg("units_many", 64, 16, 16, 44, 256, 6, 2, 128, 512, "bf16", 18)
+# Many units per CTA with one K/V tile each (L = 100 <= 128), three query tiles per KV
+# group (a one-tile unit in every group), gate off (empty staging slots in the ring).
+CONFIGS["units_short_nogate"] = _cfg("units_short_nogate", 96, 8, 8, 36, 256, 6, 2, 128, 512, "bf16", 19,
+                                     gate_on=False)
 CONFIGS["tiny_ragged32"] = _cfg("tiny_ragged32", 2, 5, 7, 9, 192, 3, 1, 64, 320, "fp32", 15)
 CONFIGS["small_fp32_hd128"] = _cfg("small_fp32_hd128", 1, 9, 11, 13, 256, 2, 1, 128, 704, "fp32", 16)
 

@@ -22,7 +22,7 @@ from gpu_helpers import check_parity, make_block, oracle_pair, parity_report, ru
 pytestmark = pytest.mark.gpu
 
 SMALL_FP32 = ["tiny", "tiny_ragged32", "small_fp32_hd128"]
-SMALL_BF16 = ["small_a", "small_b", "small_c", "small_imgonly", "small_txtonly", "units_odd", "units_many"]
+SMALL_BF16 = ["small_a", "small_b", "small_c", "small_imgonly", "small_txtonly", "units_odd", "units_many", "units_short_nogate"]
 LARGE = ["256px", "512px", "1024px"] + [f"2k_kv{k}_{g}" for k in (24, 8, 4, 1) for g in ("gate", "nogate")]
 
 
