@@ -69,3 +69,39 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(kd, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="missing"):
         kd.lib()
+
+
+def test_every_handle_call_rejects_a_null_handle(lib):
+    """Each entry point that takes a handle answers INVALID_ARG for a null one, on the host,
+    before any device work; the graph calls do the same for a null graph."""
+    L = lib.lib()
+    inv = lib.KREA_DIT_ERR_INVALID_ARG
+    i = ctypes.c_int(0)
+    p = ctypes.c_void_p(0)
+    n = ctypes.c_size_t(0)
+    calls = {
+        "krea_dit_timestep_embed": lambda: L.krea_dit_timestep_embed(None, None, 1, None, None, None),
+        "krea_dit_block_workspace": lambda: L.krea_dit_block_workspace(None, 0, ctypes.byref(p), ctypes.byref(n)),
+        "krea_dit_block_set_timing": lambda: L.krea_dit_block_set_timing(None, 1),
+        "krea_dit_block_timing_reset": lambda: L.krea_dit_block_timing_reset(None),
+        "krea_dit_block_device_status": lambda: L.krea_dit_block_device_status(None, None, ctypes.byref(i)),
+        "krea_dit_block_inject_fault": lambda: L.krea_dit_block_inject_fault(None, 0),
+        "krea_dit_block_enable_host_io": lambda: L.krea_dit_block_enable_host_io(None),
+        "krea_dit_block_forward_host": lambda: L.krea_dit_block_forward_host(None, None, None, 1, 1, 1, 1, None, None,
+                                                                             None, None),
+        "krea_dit_block_host_sync": lambda: L.krea_dit_block_host_sync(None),
+        "krea_dit_block_forward_joint": lambda: L.krea_dit_block_forward_joint(None, None, 1, 1, 1, 1, None, None, None,
+                                                                               None),
+        "krea_dit_stack_forward": lambda: L.krea_dit_stack_forward(None, None, 1, 1, 1, 1, None, None, 1, None),
+        "krea_dit_graph_launch": lambda: L.krea_dit_graph_launch(None, None),
+        "krea_dit_block_enable_backward": lambda: L.krea_dit_block_enable_backward(None),
+        "krea_dit_stack_graph_create": lambda: L.krea_dit_stack_graph_create(None, None, 1, 1, 1, 1, None, None, 1, None,
+                                                                             ctypes.byref(p)),
+        "krea_dit_weights8_quantize": lambda: L.krea_dit_weights8_quantize(None, None, None, None),
+        "krea_dit_block_backward": lambda: L.krea_dit_block_backward(None, None, None, 1, 1, 1, 1, None, None, None,
+                                                                     None, None),
+        "krea_dit_block_forward8": lambda: L.krea_dit_block_forward8(None, None, None, 1, 1, 1, 1, None, None, None,
+                                                                     None, None),
+    }
+    for name, call in calls.items():
+        assert call() == inv, name
