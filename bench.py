@@ -20,6 +20,7 @@ from __future__ import annotations
 import argparse
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -309,6 +310,36 @@ def time_oracle(cfg, rows_per_step: int, seed: int):
     return dt, len(rows[0]), blas_threads()
 
 
+def host_cpu() -> dict:
+    """The host's logical CPU count and CPU model (lscpu's model name, else
+    /proc/cpuinfo's model name or implementer/part codes, else the platform string)."""
+    import platform
+
+    model = ""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.strip().lower().startswith("model name:"):
+                model = ln.split(":", 1)[1].strip()
+                break
+    except Exception:
+        pass
+    if not model:
+        try:
+            info = open("/proc/cpuinfo").read()
+            m = re.search(r"^model name\s*:\s*(.+)$", info, re.M)
+            if m:
+                model = m.group(1).strip()
+            else:
+                imp = re.search(r"^CPU implementer\s*:\s*(\S+)$", info, re.M)
+                part = re.search(r"^CPU part\s*:\s*(\S+)$", info, re.M)
+                if imp and part:
+                    model = f"implementer {imp.group(1)} part {part.group(1)}"
+        except Exception:
+            pass
+    return {"nproc": os.cpu_count() or 1, "model": model or platform.processor() or platform.machine()}
+
+
 def blas_threads() -> int:
     try:
         from threadpoolctl import threadpool_info
@@ -342,7 +373,7 @@ def run_reference(args, cfg):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": cfg.name, "B": cfg.B, "L": cfg.L, "d_model": cfg.d, "n_q": cfg.n_q,
                    "n_kv": cfg.n_kv, "head_dim": cfg.hd, "ffn": cfg.F},
-        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle", **host_cpu(),
                          "sample": f"one batch element of {cfg.name}: K/V for all {cfg.L} tokens, the rest of the "
                                    f"block for {rows} query rows per step (tokens credited = rows)"},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -534,7 +565,7 @@ def run_ours(args, cfg):
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         dt, n, threads = time_oracle(cfg, args.cpu_rows, cfg.seed)
-        cpu = {"value": n / dt, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+        cpu = {"value": n / dt, "unit": "tokens/s", "cores": threads, "kind": "oracle", **host_cpu(),
                "sample": f"one batch element of {cfg.name}: K/V for all {cfg.L} tokens, the rest of the block for "
                          f"{n} query rows ({dt:.1f} s; tokens credited = rows)"}
 

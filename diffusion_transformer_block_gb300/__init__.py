@@ -26,6 +26,9 @@ KREA_DIT_ERR_DEVICE_TIMEOUT = -7
 KREA_DIT_ERR_INJECTED = -8
 KREA_DIT_ERR_SCRATCH_TOO_SMALL = -9
 KREA_DIT_NOALLOC_SCRATCH_FLOATS = 262144
+# sites of the bounded on-device waits (krea_dit_block_device_status)
+SITES = {"GEMM_PRODUCER": 0x01, "GEMM_MMA": 0x02, "GEMM_EPILOGUE": 0x04, "GEMM_TEARDOWN": 0x08, "ATTN_LOAD": 0x10,
+         "ATTN_MMA": 0x20, "ATTN_SOFTMAX": 0x40, "ATTN_TEARDOWN": 0x80}
 KREA_DIT_BF16 = 0
 KREA_DIT_FP32 = 1
 KREA_DIT_FP8_TENSOR = 2
@@ -42,7 +45,7 @@ EXPORTS = [
     "krea_dit_block_enable_host_io", "krea_dit_block_forward_host", "krea_dit_block_host_sync",
     "krea_dit_block_forward_joint", "krea_dit_stack_forward", "krea_dit_stack_graph_create", "krea_dit_graph_launch",
     "krea_dit_graph_destroy", "krea_dit_weights8_quantize", "krea_dit_block_forward8",
-    "krea_dit_block_enable_backward", "krea_dit_block_backward",
+    "krea_dit_block_enable_backward", "krea_dit_block_backward", "krea_dit_block_selftest_wait",
 ]
 
 
@@ -103,6 +106,7 @@ def lib() -> ctypes.CDLL:
                                                   ctypes.POINTER(ci), ci, ctypes.POINTER(ci)]
         L.krea_dit_block_device_status.argtypes = [vp, vp, ctypes.POINTER(ci)]
         L.krea_dit_block_inject_fault.argtypes = [vp, ci]
+        L.krea_dit_block_selftest_wait.argtypes = [vp, ci, ctypes.c_longlong, vp]
         L.krea_dit_kernel_names.argtypes = [ctypes.POINTER(ctypes.c_char_p), ci]
         L.krea_dit_timestep_embed_noalloc.argtypes = [vp, ci, ci, ctypes.POINTER(krea_dit_temb_weights), vp, vp]
         L.krea_dit_block_enable_host_io.argtypes = [vp]
@@ -292,6 +296,10 @@ def krea_dit_block_device_status(handle: int, stream=None) -> Tuple[int, int]:
     site = ctypes.c_int()
     st = lib().krea_dit_block_device_status(handle, _stream(stream), ctypes.byref(site))
     return st, site.value
+
+
+def krea_dit_block_selftest_wait(handle: int, site: int, limit_ns: int, stream=None) -> None:
+    _check(lib().krea_dit_block_selftest_wait(handle, site, limit_ns, _stream(stream)), "krea_dit_block_selftest_wait")
 
 
 def krea_dit_block_inject_fault(handle: int, count: int) -> None:

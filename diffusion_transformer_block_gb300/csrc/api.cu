@@ -2,6 +2,7 @@
 // kernel sequencing, per-kernel timing and device-side failure reporting.
 // The operation and every argument are documented in include/krea_dit.h.
 #include <cudaTypedefs.h>
+#include <nvtx3/nvToolsExt.h>
 #include <math.h>
 #include <stdlib.h>
 #include <string.h>
@@ -234,8 +235,20 @@ cudaEvent_t take_event(krea_dit_block_s* h) {
 }
 
 // Runs one launch; when timing is on, brackets it with events on `st`.
+// Host-side NVTX range for the lifetime of the object (header-only NVTX v3).
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
+
 template <class F>
 cudaError_t timed(krea_dit_block_s* h, int slot, cudaStream_t st, F&& launch) {
+  // Every launch sits in an NVTX range named after its kernel slot, so a profiler can
+  // select one kernel of the block by name (ncu --nvtx --nvtx-include "<slot>/"). With no
+  // tool attached an NVTX call returns at once.
+  NvtxRange range(kSlotNames[slot]);
   if (!h->timing) return launch();
   cudaEvent_t b = take_event(h), e = take_event(h);
   if (!b || !e) return cudaErrorMemoryAllocation;
@@ -1152,6 +1165,14 @@ int krea_dit_block_device_status(krea_dit_block_t h, krea_dit_stream_t stream, i
     return KREA_DIT_ERR_DEVICE_TIMEOUT;
   }
   return KREA_DIT_OK;
+}
+
+int krea_dit_block_selftest_wait(krea_dit_block_t h, int site, long long limit_ns, krea_dit_stream_t stream) {
+  if (!h || site == 0 || (site & ~0xFF) != 0) return KREA_DIT_ERR_INVALID_ARG;
+  if (limit_ns < 1000 || limit_ns > 1000000000LL) return KREA_DIT_ERR_INVALID_ARG;
+  const cudaError_t e = kd::launch_wait_selftest(h->err, site, static_cast<unsigned long long>(limit_ns), h->num_sms,
+                                                 reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? KREA_DIT_OK : KREA_DIT_ERR_CUDA;
 }
 
 int krea_dit_block_inject_fault(krea_dit_block_t h, int count) {

@@ -119,6 +119,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 struct WaitCtx {
   volatile int* abort;  // shared memory, set once any thread of the CTA gave up
   int* err;             // global error word
+  unsigned long long limit_ns = kWaitLimitNs;  // how long one wait may take
 };
 
 // Wait until the phase with the given parity has completed. Returns false (and the
@@ -131,7 +132,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
     for (int i = 0; i < 32; ++i)
       if (mbar_try_wait(bar, parity)) return true;
     if (*w.abort) return false;
-    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+    if (globaltimer_ns() - t0 > w.limit_ns) {
       *w.abort = 1;
       atomicOr(w.err, site);
       __threadfence();

@@ -190,4 +190,9 @@ cudaError_t launch_qkv_bwd(const Fwd& f, const float* raw, int ldr, const float*
                            const float* q_norm_w, const float* k_norm_w, const float2* rope, void* d_P, int ldp,
                            float* d_qw, float* d_kw, cudaStream_t st);
 
+// ---- selftest.cu ----
+// one CTA per SM waits (bounded by limit_ns) on an mbarrier nothing arrives at, records
+// `site` in *err, frees its tensor memory and returns
+cudaError_t launch_wait_selftest(int* err, int site, unsigned long long limit_ns, int num_sms, cudaStream_t st);
+
 }  // namespace kd

@@ -7,8 +7,12 @@
 // point computes the same shared timestep embedding as krea_dit_timestep_embed with
 // its scratch in a fixed, file-scope device array instead of the handle's workspace.
 //
-// The array is KREA_DIT_NOALLOC_SCRATCH_FLOATS floats (1 MiB); every GPU that loads the
-// library holds it until the process exits. It holds the sinusoid e [B, 256] and the
+// The array is KREA_DIT_NOALLOC_SCRATCH_FLOATS floats (1 MiB). With CUDA's lazy module
+// loading (the default) a device gets its copy of the array at the first call on that
+// device, which looks up the array's address, and holds it until the process exits.
+// A caller that reserves all device memory for its own pool must therefore make one call
+// on each device at start-up, before the reservation (and before any stream capture);
+// later calls allocate nothing. It holds the sinusoid e [B, 256] and the
 // hidden layer [B, d] between the two MLP layers, so a call needs B * (256 + d) floats.
 // Every call overwrites all of the scratch it uses before reading it, so nothing needs
 // clearing between calls; calls that overlap on the GPU share the array and race.

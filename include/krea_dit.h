@@ -187,9 +187,11 @@ int krea_dit_block_forward(krea_dit_block_t h, const void* x_img, const void* x_
  *  w          timestep-MLP weights as for krea_dit_timestep_embed
  *  mod_shared device fp32 [B, 6, d_model], written
  * Scratch lives in one fixed file-scope device array of KREA_DIT_NOALLOC_SCRATCH_FLOATS
- * floats (1 MiB) that every GPU loading the library holds until the process exits. The
- * first call on a device looks up the array's device address (with that device
- * current) and caches it; make that first call before any stream capture. Every call
+ * floats (1 MiB). The first call on a device looks up the array's device address (with
+ * that device current) and caches it; under CUDA's lazy module loading (the default) that
+ * first call is also when the device gets its copy of the array, which it then holds
+ * until the process exits. So make one call on each device at start-up, before reserving
+ * the device's memory for a pool and before any stream capture. Every call
  * shares the array and writes all scratch it reads, so nothing carries over between
  * calls, but calls that overlap on the GPU (two streams, two threads) race. It calls
  * no cudaMalloc, cudaFree or allocating library routine. */
@@ -384,6 +386,26 @@ int krea_dit_block_timing_reset(krea_dit_block_t h);
  * KREA_DIT_OK or KREA_DIT_ERR_DEVICE_TIMEOUT (*site = the first wait that gave up, a
  * bit mask of sites otherwise 0). */
 int krea_dit_block_device_status(krea_dit_block_t h, krea_dit_stream_t stream, int* site);
+
+/* Sites reported by krea_dit_block_device_status: which kind of wait gave up. */
+#define KREA_DIT_SITE_GEMM_PRODUCER 0x01 /* GEMM TMA-load warp waiting for a free stage */
+#define KREA_DIT_SITE_GEMM_MMA 0x02      /* GEMM MMA warp waiting for operands or an accumulator */
+#define KREA_DIT_SITE_GEMM_EPILOGUE 0x04 /* GEMM epilogue waiting for an accumulator */
+#define KREA_DIT_SITE_GEMM_TEARDOWN 0x08 /* GEMM draining its own copies before exit */
+#define KREA_DIT_SITE_ATTN_LOAD 0x10     /* attention TMA-load warp waiting for a free slot */
+#define KREA_DIT_SITE_ATTN_MMA 0x20      /* attention MMA warp waiting for K/V, P or its turn */
+#define KREA_DIT_SITE_ATTN_SOFTMAX 0x40  /* attention softmax/epilogue warps waiting for S or O */
+#define KREA_DIT_SITE_ATTN_TEARDOWN 0x80 /* attention draining its own copies before exit */
+
+/* Testing aid for the bounded waits above: enqueue on `stream` one CTA per SM that
+ * takes 32 tensor-memory columns, waits on an mbarrier that nothing ever arrives at
+ * (the same wait routine as the tensor-core kernels, with a limit of limit_ns instead
+ * of about one second), gives up, records `site` in the handle's device error word,
+ * frees its tensor memory and returns. No copy or MMA is in flight at any point. A
+ * following krea_dit_block_device_status returns KREA_DIT_ERR_DEVICE_TIMEOUT with that
+ * site; the handle stays usable. site: a nonzero mask of KREA_DIT_SITE_* bits;
+ * limit_ns: 1000 (1 us) to 1000000000 (1 s); else INVALID_ARG. */
+int krea_dit_block_selftest_wait(krea_dit_block_t h, int site, long long limit_ns, krea_dit_stream_t stream);
 
 /* Testing aid: make the next `count` calls of krea_dit_block_forward fail with
  * KREA_DIT_ERR_INJECTED after validation and before any launch. */

@@ -2,6 +2,8 @@
 with the fp64 oracle on the same rounded inputs."""
 from __future__ import annotations
 
+import json
+import os
 from typing import Dict, List, Optional, Sequence
 
 import numpy as np
@@ -169,6 +171,54 @@ def parity_report(case: di.Case, gpu: Dict, ref: Dict, ref_st: Dict) -> Dict[str
     return rep
 
 
+def output_split(case: di.Case, gpu: Dict, ref: Dict) -> Dict[str, object]:
+    """Splits the block output's error against the exact oracle into the output's own
+    rounding and the error of the value it rounds.
+
+    pre = h1 + gate_m * (hmid W_down^T), in fp64 from the GPU's stored h1 (fp32) and hmid:
+    the value the down-projection epilogue rounds to the output (up to its fp32
+    accumulation, ~1e-6 relative). So |out - pre| is the output's rounding and
+    |pre - ref| the error of everything upstream of it, which splits further into the
+    residual h1 (|h1 - h1_ref|) and the MLP branch. Returned per workload: the largest
+    of each over all compared elements (x RMS(ref)), and the element with the largest
+    literal error, with its position, |ref| / RMS and the three parts there."""
+    mod = oracle.modulation(np.asarray(gpu["mod_shared"], np.float64), case.w["mod_bias"])
+    W = np.asarray(case.w["w_down"], np.float64)
+    pre = [gpu["h1"][b] + mod["gate_m"][b] * (gpu["hmid"][b] @ W.T) for b in range(case.cfg.B)]
+    out_g, ref_o, pre_c = _cat(gpu["out"]), _cat(ref["out"]), _cat(pre)
+    h1_g, h1_r = _cat(gpu["h1"]), _cat(ref["h1"])
+    if ref_o.size == 0:
+        return {}
+    rms = float(np.sqrt(np.mean(ref_o * ref_o)))
+    err = np.abs(out_g - ref_o)
+    i = int(np.argmax(err))
+    d = case.cfg.d
+    sizes = [x.size for x in gpu["out"]]
+    b = int(np.searchsorted(np.cumsum(sizes), i, side="right"))
+    j = i - int(sum(sizes[:b]))
+    row, col = int(gpu["rows"][b][j // d]), j % d
+    return {
+        "maxabs_rms": float(err.max() / rms),
+        "rounding_max_rms": float(np.abs(out_g - pre_c).max() / rms),
+        "upstream_max_rms": float(np.abs(pre_c - ref_o).max() / rms),
+        "h1_max_rms": float(np.abs(h1_g - h1_r).max() / rms),
+        "worst": {"batch": b, "row": row, "col": col, "ref_rms": float(abs(ref_o[i]) / rms),
+                  "err_rms": float(err[i] / rms), "rounding_rms": float(abs(out_g[i] - pre_c[i]) / rms),
+                  "upstream_rms": float(abs(pre_c[i] - ref_o[i]) / rms),
+                  "h1_rms": float(abs(h1_g[i] - h1_r[i]) / rms),
+                  "mlp_branch_rms": float(abs((pre_c[i] - h1_g[i]) - (ref_o[i] - h1_r[i])) / rms)},
+    }
+
+
+def record(entry: Dict[str, object]) -> None:
+    """Appends one JSON line to the file named by KREA_PARITY_RECORD (if set), so a test
+    run keeps its parity figures."""
+    path = os.environ.get("KREA_PARITY_RECORD")
+    if path:
+        with open(path, "a") as fh:
+            fh.write(json.dumps(entry) + "\n")
+
+
 def oracle_pair(case: di.Case, rows=None, mod_shared: Optional[np.ndarray] = None):
     ms = oracle.mod_shared_for(case) if mod_shared is None else mod_shared
     ref = oracle.run_case(case, rows=rows, mod_shared=ms)
@@ -180,6 +230,10 @@ def oracle_pair(case: di.Case, rows=None, mod_shared: Optional[np.ndarray] = Non
 def check_parity(case: di.Case, gpu: Dict, rows=None, mod_shared: Optional[np.ndarray] = None) -> Dict[str, float]:
     ref, ref_st = oracle_pair(case, rows, mod_shared)
     rep = parity_report(case, gpu, ref, ref_st)
+    if os.environ.get("KREA_PARITY_RECORD"):
+        record({"case": case.cfg.name, "dtype": case.cfg.dtype, "B": case.cfg.B, "L": case.cfg.L,
+                "rows_per_batch": int(len(gpu["rows"][0])) if gpu["rows"] else 0, "report": rep,
+                "output_split": output_split(case, gpu, ref)})
     bad = {k: v for k, v in rep.items() if k != "out_maxabs_rms" and v > 1.0}
     assert not bad, f"{case.cfg.name}: parity failures {bad}; full report {rep}"
     return rep

@@ -86,6 +86,7 @@ def test_every_handle_call_rejects_a_null_handle(lib):
         "krea_dit_block_timing_reset": lambda: L.krea_dit_block_timing_reset(None),
         "krea_dit_block_device_status": lambda: L.krea_dit_block_device_status(None, None, ctypes.byref(i)),
         "krea_dit_block_inject_fault": lambda: L.krea_dit_block_inject_fault(None, 0),
+        "krea_dit_block_selftest_wait": lambda: L.krea_dit_block_selftest_wait(None, 1, 1000000, None),
         "krea_dit_block_enable_host_io": lambda: L.krea_dit_block_enable_host_io(None),
         "krea_dit_block_forward_host": lambda: L.krea_dit_block_forward_host(None, None, None, 1, 1, 1, 1, None, None,
                                                                              None, None),

@@ -1,5 +1,7 @@
 """Host-side error handling through the C ABI on a GPU (nothing here faults the GPU:
 every bad argument is rejected on the host before anything is enqueued)."""
+import time
+
 import pytest
 import torch
 
@@ -63,6 +65,35 @@ def test_injected_fault_enqueues_nothing(setup):
     assert _fwd(blk, x_img, x_txt, cfg.B, cfg.img_h, cfg.img_w, cfg.n_txt, ms, out) == kd.KREA_DIT_OK
     torch.cuda.synchronize()
     assert out.abs().max().item() > 0.0
+
+
+def test_bounded_wait_gives_up_and_the_handle_stays_usable(setup):
+    """A wait on an mbarrier that nothing arrives at, through the same routine every
+    tensor-core kernel waits with (limit 1 ms here instead of about a second), gives up:
+    the call returns, the device status names the site, the tensor memory the waiting
+    CTAs held is free again (the next forward's kernels allocate 512 columns per SM),
+    and the next forward on the same handle gives the same result as before."""
+    cfg, blk, x_img, x_txt, ms = setup
+    before = blk.forward(x_img, x_txt, cfg.B, cfg.img_h, cfg.img_w, cfg.n_txt, ms).clone()
+    torch.cuda.synchronize()
+    assert kd.krea_dit_block_device_status(blk.handle) == (kd.KREA_DIT_OK, 0)
+    for site in (kd.SITES["ATTN_MMA"], kd.SITES["GEMM_PRODUCER"]):
+        t0 = time.perf_counter()
+        kd.krea_dit_block_selftest_wait(blk.handle, site, 1_000_000)
+        st, got = kd.krea_dit_block_device_status(blk.handle)
+        assert time.perf_counter() - t0 < 10.0
+        assert st == kd.KREA_DIT_ERR_DEVICE_TIMEOUT and got == site
+        assert kd.krea_dit_block_device_status(blk.handle) == (kd.KREA_DIT_OK, 0)  # read and cleared
+        after = blk.forward(x_img, x_txt, cfg.B, cfg.img_h, cfg.img_w, cfg.n_txt, ms)
+        torch.cuda.synchronize()
+        assert torch.equal(after, before)
+        assert kd.krea_dit_block_device_status(blk.handle) == (kd.KREA_DIT_OK, 0)
+    # out-of-range arguments are rejected on the host
+    L = kd.lib()
+    assert L.krea_dit_block_selftest_wait(blk.handle, 0, 1_000_000, None) == kd.KREA_DIT_ERR_INVALID_ARG
+    assert L.krea_dit_block_selftest_wait(blk.handle, 0x100, 1_000_000, None) == kd.KREA_DIT_ERR_INVALID_ARG
+    assert L.krea_dit_block_selftest_wait(blk.handle, 1, 10, None) == kd.KREA_DIT_ERR_INVALID_ARG
+    assert L.krea_dit_block_selftest_wait(blk.handle, 1, 2_000_000_000, None) == kd.KREA_DIT_ERR_INVALID_ARG
 
 
 def test_timing_counts_launches(setup):
