@@ -110,8 +110,9 @@ __device__ __forceinline__ int tile_head(const AttnArgs& a, const Unit& w, int t
 }
 __device__ __forceinline__ int tile_qt(const AttnArgs& a, const Unit& w, int t) { return (2 * w.p + t) % a.nqt; }
 
-// 352 threads x at most 184 registers fit the SM's 64K (one CTA per SM)
-__global__ void __maxnreg__(184)
+// 352 threads x at most 168 registers per thread: with 178 the launch is refused for lack
+// of registers (allocation granularity), so the cap stays where the kernel fits today
+__global__ void __maxnreg__(168)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_vt, const __grid_constant__ CUtensorMap tm_g,
                    const __grid_constant__ CUtensorMap tm_og, AttnArgs a) {

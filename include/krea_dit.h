@@ -403,7 +403,7 @@ int krea_dit_block_device_status(krea_dit_block_t h, krea_dit_stream_t stream, i
  * of about one second), gives up, records `site` in the handle's device error word,
  * frees its tensor memory and returns. No copy or MMA is in flight at any point. A
  * following krea_dit_block_device_status returns KREA_DIT_ERR_DEVICE_TIMEOUT with that
- * site; the handle stays usable. site: a nonzero mask of KREA_DIT_SITE_* bits;
+ * site; the handle stays usable. site: a nonzero mask of KREA_DIT_SITE_* bits (0xFF);
  * limit_ns: 1000 (1 us) to 1000000000 (1 s); else INVALID_ARG. */
 int krea_dit_block_selftest_wait(krea_dit_block_t h, int site, long long limit_ns, krea_dit_stream_t stream);
 

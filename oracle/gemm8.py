@@ -111,7 +111,7 @@ def block_forward8(
     so the block runs stage by stage over all batch elements (all rows; no row
     sampling). ``store`` rounds intermediates where an implementation stores them,
     as in ``block_forward``; an activation is cast to e4m3 from its stored value.
-    Returns per-batch lists q, k, v, g, o_g, h1, hn, hmid, out over all rows, plus
+    Returns per-batch lists xn, q, k, v, g, o_g, h1, hn, hmid, out over all rows, plus
     the dequantised GEMM operands xn8, og8, hn8, hmid8 ([L, K] per batch element)."""
     if scaling not in ("tensor", "row"):
         raise ValueError(f"scaling must be 'tensor' or 'row', not {scaling!r}")
@@ -185,7 +185,7 @@ def block_forward8(
     out = [rnd["out"](h1[b] + mod["gate_m"][b] * down[b]) for b in range(B)]
 
     res["og8"] = og8
-    res.update(h1=h1, hn=hn, hmid=hmid, out=out, hn8=hn8, hmid8=hmid8, rows=[np.arange(L)] * B)
+    res.update(xn=xn, h1=h1, hn=hn, hmid=hmid, out=out, hn8=hn8, hmid8=hmid8, rows=[np.arange(L)] * B)
     return res
 
 

@@ -1,0 +1,103 @@
+"""A-priori allowances for the 8-bit GEMM parity checks (host logic, no GPU).
+
+An 8-bit GEMM casts an activation operand from a stored bf16 value v with one
+power-of-two scale 2^k per group (a token row, or the whole tensor), k fixed by the
+group's largest magnitude. The cast is discontinuous: a device value v' that differs
+from the oracle's v by a little can land on another e4m3 code, and near a scale
+boundary the whole group can change scale. These functions bound that change from the
+oracle's values and a stated deviation budget alone (no device value enters a bound);
+the GPU tests then assert that the device's operands and every downstream result stay
+inside those bounds.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+from oracle import gemm8 as g8
+
+F64 = np.float64
+Z = 6.0  # standard deviations of a sum of sign-symmetric terms covered by ``carry``
+
+
+def bf16_ulp(v) -> np.ndarray:
+    """Spacing of bf16 values at |v|: 2^(e-7) for |v| in [2^e, 2^(e+1)); 2^-133 (the
+    smallest subnormal step) at 0."""
+    a = np.abs(np.asarray(v, F64))
+    _, e = np.frexp(a)  # a = m 2^e, 0.5 <= m < 1: binade exponent e - 1
+    return np.where(a > 0, np.ldexp(1.0, e - 8), np.ldexp(1.0, -133))
+
+
+def cast_change_bound(v, delta, per_row: bool):
+    """The oracle's dequantised operand cast(v) and a bound on how far the cast of any
+    v' with |v' - v| <= delta (elementwise) can land from it.
+
+    The group's largest magnitude of v' lies in [lo, hi] = [max(|v| - delta),
+    max(|v| + delta)], so its scale exponent is any k between k(hi) and k(lo) (k falls
+    as the magnitude grows). For each such k the cast is monotone in v', so the largest
+    distance over the interval [v - delta, v + delta] is reached at one of its ends.
+    Returns (cast(v) as q * 2^-k, bound), both shaped like v; the bound is 0 where no
+    admissible v' changes the cast."""
+    v = np.asarray(v, F64)
+    delta = np.broadcast_to(np.asarray(delta, F64), v.shape)
+    q, d = g8.quantize(v, per_row)
+    ref = q * d
+    a = np.abs(v)
+    if per_row:
+        lo = np.max(np.maximum(a - delta, 0.0), axis=-1, keepdims=True)
+        hi = np.max(a + delta, axis=-1, keepdims=True)
+    else:
+        lo = np.max(np.maximum(a - delta, 0.0), initial=0.0)
+        hi = np.max(a + delta, initial=0.0)
+    if v.size and np.any(lo <= 0):
+        raise ValueError("a scaling group could be all zeros within its budget")
+    k_lo, k_hi = g8.scale_exponent(hi), g8.scale_exponent(lo)
+    bound = np.zeros_like(v)
+    for k in range(int(np.min(k_lo)) if v.size else 0, (int(np.max(k_hi)) + 1) if v.size else 0):
+        live = (k >= k_lo) & (k <= k_hi)
+        if not np.any(live):
+            continue
+        for s in (v - delta, v + delta):
+            dev = np.abs(np.ldexp(g8.round_to_e4m3(np.ldexp(s, k)), -k) - ref)
+            bound = np.where(live, np.maximum(bound, dev), bound)
+    return ref, bound
+
+
+def carry(d_op, W) -> np.ndarray:
+    """Spread that operand changes of at most d_op [R, K] carry through a projection
+    with weights W [N, K]: Z * sqrt(d_op^2 (W^2)^T). The weights are sign-symmetric, so
+    the carried terms d_j W_cj have independent random signs; for a single changed
+    value the bound is Z times that value's whole effect."""
+    return Z * np.sqrt((np.asarray(d_op, F64) ** 2) @ (np.asarray(W, F64) ** 2).T)
+
+
+def norm_carry(h, gamma, dh, eps: float) -> np.ndarray:
+    """Bound on the change of gamma * h / sqrt(mean(h^2) + eps) (row-wise) when h moves
+    by at most dh elementwise: to first order
+    |gamma_j| rstd (dh_j + |h_j| rstd ||dh||_2 / sqrt(d)), with 5% added for the
+    second-order terms (dh is far below |h| here)."""
+    h = np.asarray(h, F64)
+    rstd = 1.0 / np.sqrt(np.mean(h * h, axis=-1, keepdims=True) + eps)
+    nd = np.sqrt(np.sum(np.asarray(dh, F64) ** 2, axis=-1, keepdims=True) / h.shape[-1])
+    return 1.05 * np.abs(gamma) * rstd * (dh + np.abs(h) * rstd * nd)
+
+
+def attention_spread(q, k, v) -> np.ndarray:
+    """sqrt(sum_k p_jk^2 v_kc^2) for every query row j and channel c of every head, with
+    p the softmax probabilities of q k^T / sqrt(hd) (GQA: query head h reads key/value
+    head h // (n_q / n_kv)). q [n_q, L, hd], k and v [n_kv, L, hd] -> [L, n_q * hd].
+
+    When every probability carries an independent relative rounding error of at most
+    r, the attention output's error has this spread times r (random signs); a device
+    that rounds P to bf16 before the P V product has r = 2^-9."""
+    q, k, v = (np.asarray(x, F64) for x in (q, k, v))
+    n_q, L, hd = q.shape
+    G = n_q // k.shape[0]
+    out = np.empty((L, n_q * hd))
+    for h in range(n_q):
+        kv = h // G
+        s = q[h] @ k[kv].T / np.sqrt(hd)
+        s -= s.max(axis=1, keepdims=True)
+        p = np.exp(s)
+        p /= p.sum(axis=1, keepdims=True)
+        out[:, h * hd:(h + 1) * hd] = np.sqrt((p * p) @ (v[kv] ** 2))
+    return out

@@ -230,10 +230,15 @@ def oracle_pair(case: di.Case, rows=None, mod_shared: Optional[np.ndarray] = Non
 def check_parity(case: di.Case, gpu: Dict, rows=None, mod_shared: Optional[np.ndarray] = None) -> Dict[str, float]:
     ref, ref_st = oracle_pair(case, rows, mod_shared)
     rep = parity_report(case, gpu, ref, ref_st)
+    split = output_split(case, gpu, ref)
+    tol = TOL[case.cfg.dtype]
+    # the literal criterion (max-abs error <= tol x RMS), and the error of the value the
+    # output rounds (everything upstream of the output's own rounding) within half of it
+    rep["out_literal"] = rep["out_maxabs_rms"] / tol
+    rep["out_upstream"] = split.get("upstream_max_rms", 0.0) / (0.5 * tol)
     if os.environ.get("KREA_PARITY_RECORD"):
         record({"case": case.cfg.name, "dtype": case.cfg.dtype, "B": case.cfg.B, "L": case.cfg.L,
-                "rows_per_batch": int(len(gpu["rows"][0])) if gpu["rows"] else 0, "report": rep,
-                "output_split": output_split(case, gpu, ref)})
+                "rows": int(sum(len(r) for r in gpu["rows"])), "report": rep, "output_split": split})
     bad = {k: v for k, v in rep.items() if k != "out_maxabs_rms" and v > 1.0}
     assert not bad, f"{case.cfg.name}: parity failures {bad}; full report {rep}"
     return rep

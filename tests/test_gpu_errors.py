@@ -77,7 +77,7 @@ def test_bounded_wait_gives_up_and_the_handle_stays_usable(setup):
     before = blk.forward(x_img, x_txt, cfg.B, cfg.img_h, cfg.img_w, cfg.n_txt, ms).clone()
     torch.cuda.synchronize()
     assert kd.krea_dit_block_device_status(blk.handle) == (kd.KREA_DIT_OK, 0)
-    for site in (kd.SITES["ATTN_MMA"], kd.SITES["GEMM_PRODUCER"]):
+    for site in (kd.SITES["ATTN_MMA"], kd.SITES["GEMM_PRODUCER"], kd.SITES["ATTN_TEARDOWN"]):
         t0 = time.perf_counter()
         kd.krea_dit_block_selftest_wait(blk.handle, site, 1_000_000)
         st, got = kd.krea_dit_block_device_status(blk.handle)

@@ -3,9 +3,12 @@
 Small cases compare every row; the full-size workloads compare a stratified row sample
 (exact in the oracle, see oracle.block_forward) in the launch configuration the
 benchmark times. Criteria:
-  * the block output against the exact fp64 oracle: |out - ref| <= 2e-2 x RMS(ref) in
-    bf16 (1e-4 x RMS(ref) in the fp32 check mode) plus the output's own rounding to its
-    storage dtype (half an ulp of the value); the literal max-abs / RMS is reported too;
+  * the block output against the exact fp64 oracle, literally: max |out - ref| <=
+    2e-2 x RMS(ref) in bf16 (1e-4 x RMS(ref) in the fp32 check mode);
+  * the same elementwise with the output's own rounding to its storage dtype excused
+    (|out - ref| <= tol x RMS(ref) + half an ulp of the value), and the value the output
+    rounds (h1 + gate_m (hmid W_down^T) from the stored h1 and hmid) within half the
+    tolerance of the exact output;
   * every stored intermediate (q, k, v, g, o_g, h1, hn, hmid), the output and both
     residual branches against the oracle with the path's storage rounding: elementwise
     |gpu - ref| <= tol x RMS(ref) + 1 ulp x |ref| (a stored value may land one ulp away).
