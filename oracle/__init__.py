@@ -6,7 +6,9 @@ with the CUDA path. Parity pins: every function here is pinned by the CPU tests
 (textbook library routines, closed forms, invariants, brute force on tiny
 inputs); none is "parity unpinned". ``oracle.gemm8`` adds the block with 8-bit
 (e4m3, scaled) GEMM operands, pinned in ``tests/test_oracle_gemm8.py``; ``oracle.backward``
-the analytic gradients of the block, pinned in ``tests/test_oracle_backward.py``.
+the analytic gradients of the block, pinned in ``tests/test_oracle_backward.py``;
+``oracle.nvfp4`` the block with NVFP4 GEMM operands (E2M1 elements, E4M3 scales per 16
+elements, a power-of-two tensor scale), pinned in ``tests/test_oracle_nvfp4.py``.
 """
 from __future__ import annotations
 

@@ -104,6 +104,7 @@ def block_forward8(
     rope_base: float = 10000.0,
     gate_on: bool = True,
     store=None,
+    deq=None,
 ) -> Dict[str, list]:
     """The block forward of ``block.block_forward`` with 8-bit GEMM operands.
 
@@ -112,10 +113,17 @@ def block_forward8(
     sampling). ``store`` rounds intermediates where an implementation stores them,
     as in ``block_forward``; an activation is cast to e4m3 from its stored value.
     Returns per-batch lists xn, q, k, v, g, o_g, h1, hn, hmid, out over all rows, plus
-    the dequantised GEMM operands xn8, og8, hn8, hmid8 ([L, K] per batch element)."""
-    if scaling not in ("tensor", "row"):
+    the dequantised GEMM operands xn8, og8, hn8, hmid8 ([L, K] per batch element).
+
+    ``deq`` (optional) replaces the cast: a function from a [R, K] operand (an
+    activation over all rows of the step, or a weight matrix) to its dequantised values;
+    ``scaling`` is then ignored. The NVFP4 oracle (``oracle.nvfp4``) uses it."""
+    if deq is None and scaling not in ("tensor", "row"):
         raise ValueError(f"scaling must be 'tensor' or 'row', not {scaling!r}")
     per_row = scaling == "row"
+    if deq is None:
+        def deq(x):
+            return dequantized(x, per_row)
     x_txt = np.asarray(x_txt, F64)
     x_img = np.asarray(x_img, F64)
     B, Nt, d = x_txt.shape
@@ -134,14 +142,14 @@ def block_forward8(
         return [m[b * L:(b + 1) * L] for b in range(B)]
 
     def mat8(name):
-        return dequantized(w[name], per_row)
+        return deq(w[name])
 
     X = [np.concatenate([x_txt[b], x_img[b]], axis=0) for b in range(B)]
 
     # norm1 + modulation, stored, then cast for the fused projection
     xn = [rnd["xn"](zero_centred_rms_norm(X[b], w["norm1_w"], eps) * (1.0 + mod["scale_a"][b])
                     + mod["shift_a"][b]) for b in range(B)]
-    xn8 = split(dequantized(rows_of(xn), per_row))
+    xn8 = split(deq(rows_of(xn)))
     proj = split(rows_of(xn8) @ mat8("w_qkvg").T)
 
     qr, kr = n_q * hd, n_kv * hd
@@ -171,16 +179,16 @@ def block_forward8(
         res["xn8"].append(xn8[b])
 
     # attention output projection + gated residual
-    og8 = split(dequantized(rows_of(res["o_g"]), per_row))
+    og8 = split(deq(rows_of(res["o_g"])))
     attn = split(rows_of(og8) @ mat8("w_o").T)
     h1 = [rnd["h1"](X[b] + mod["gate_a"][b] * attn[b]) for b in range(B)]
     hn = [rnd["hn"](zero_centred_rms_norm(h1[b], w["norm2_w"], eps) * (1.0 + mod["scale_m"][b])
                     + mod["shift_m"][b]) for b in range(B)]
-    hn8 = split(dequantized(rows_of(hn), per_row))
+    hn8 = split(deq(rows_of(hn)))
     hn_all = rows_of(hn8)
     hmid = split(silu(hn_all @ mat8("w_gate").T) * (hn_all @ mat8("w_up").T))
     hmid = [rnd["hmid"](m) for m in hmid]
-    hmid8 = split(dequantized(rows_of(hmid), per_row))
+    hmid8 = split(deq(rows_of(hmid)))
     down = split(rows_of(hmid8) @ mat8("w_down").T)
     out = [rnd["out"](h1[b] + mod["gate_m"][b] * down[b]) for b in range(B)]
 
