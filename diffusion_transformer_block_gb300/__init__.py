@@ -33,8 +33,11 @@ KREA_DIT_BF16 = 0
 KREA_DIT_FP32 = 1
 KREA_DIT_FP8_TENSOR = 2
 KREA_DIT_FP8_ROW = 3
+KREA_DIT_NVFP4 = 4
 BUFFERS = {"XN": 0, "Q": 1, "K": 2, "VT": 3, "G": 4, "OG": 5, "H1": 6, "HN": 7, "HMID": 8, "XN8": 9, "OG8": 10,
-           "HN8": 11, "HMID8": 12, "DQ_XN": 13, "DQ_OG": 14, "DQ_HN": 15, "DQ_HMID": 16}
+           "HN8": 11, "HMID8": 12, "DQ_XN": 13, "DQ_OG": 14, "DQ_HN": 15, "DQ_HMID": 16, "XN4": 17, "OG4": 18,
+           "HN4": 19, "HMID4": 20, "SF_XN4": 21, "SF_OG4": 22, "SF_HN4": 23, "SF_HMID4": 24, "TS_XN4": 25,
+           "TS_OG4": 26, "TS_HN4": 27, "TS_HMID4": 28}
 
 # C symbols the header declares (checked by the CPU tests against the built library)
 EXPORTS = [
@@ -46,6 +49,7 @@ EXPORTS = [
     "krea_dit_block_forward_joint", "krea_dit_stack_forward", "krea_dit_stack_graph_create", "krea_dit_graph_launch",
     "krea_dit_graph_destroy", "krea_dit_weights8_quantize", "krea_dit_block_forward8",
     "krea_dit_block_enable_backward", "krea_dit_block_backward", "krea_dit_block_selftest_wait",
+    "krea_dit_nvfp4_scale_bytes", "krea_dit_weights4_quantize", "krea_dit_block_forward4",
 ]
 
 
@@ -65,6 +69,12 @@ class krea_dit_config(ctypes.Structure):
 class krea_dit_weights(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in (
         "w_qkvg", "w_o", "w_gate", "w_up", "w_down", "norm1_w", "norm2_w", "q_norm_w", "k_norm_w", "mod_bias")]
+
+
+class krea_dit_weights4(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in (
+        "w_qkvg", "w_o", "w_gate", "w_up", "w_down", "sf_qkvg", "sf_o", "sf_gate", "sf_up", "sf_down", "ts_qkvg",
+        "ts_o", "ts_gate", "ts_up", "ts_down")]
 
 
 class krea_dit_weights8(ctypes.Structure):
@@ -120,6 +130,12 @@ def lib() -> ctypes.CDLL:
         L.krea_dit_graph_destroy.argtypes = [vp]
         L.krea_dit_weights8_quantize.argtypes = [vp, ctypes.POINTER(krea_dit_weights), ctypes.POINTER(krea_dit_weights8),
                                                  vp]
+        L.krea_dit_nvfp4_scale_bytes.argtypes = [ci, ci]
+        L.krea_dit_nvfp4_scale_bytes.restype = ctypes.c_size_t
+        L.krea_dit_weights4_quantize.argtypes = [vp, ctypes.POINTER(krea_dit_weights), ctypes.POINTER(krea_dit_weights4),
+                                                 vp]
+        L.krea_dit_block_forward4.argtypes = [vp, vp, vp, ci, ci, ci, ci, vp, ctypes.POINTER(krea_dit_weights),
+                                              ctypes.POINTER(krea_dit_weights4), vp, vp]
         L.krea_dit_block_enable_backward.argtypes = [vp]
         L.krea_dit_block_backward.argtypes = [vp, vp, vp, ci, ci, ci, ci, vp, ctypes.POINTER(krea_dit_weights), vp,
                                               ctypes.POINTER(krea_dit_grads), vp]
@@ -189,6 +205,22 @@ def krea_dit_block_forward(handle: int, x_img, x_txt, B: int, img_h: int, img_w:
 def krea_dit_weights8_quantize(handle: int, w: krea_dit_weights, q: krea_dit_weights8, stream=None) -> None:
     _check(lib().krea_dit_weights8_quantize(handle, ctypes.byref(w), ctypes.byref(q), _stream(stream)),
            "krea_dit_weights8_quantize")
+
+
+def krea_dit_nvfp4_scale_bytes(rows: int, cols: int) -> int:
+    return int(lib().krea_dit_nvfp4_scale_bytes(rows, cols))
+
+
+def krea_dit_weights4_quantize(handle: int, w: krea_dit_weights, q: krea_dit_weights4, stream=None) -> None:
+    _check(lib().krea_dit_weights4_quantize(handle, ctypes.byref(w), ctypes.byref(q), _stream(stream)),
+           "krea_dit_weights4_quantize")
+
+
+def krea_dit_block_forward4(handle: int, x_img, x_txt, B: int, img_h: int, img_w: int, n_txt: int, t_emb,
+                            w: krea_dit_weights, q: krea_dit_weights4, out, stream=None) -> None:
+    _check(lib().krea_dit_block_forward4(handle, _ptr(x_img), _ptr(x_txt), B, img_h, img_w, n_txt, _ptr(t_emb),
+                                         ctypes.byref(w), ctypes.byref(q), _ptr(out), _stream(stream)),
+           "krea_dit_block_forward4")
 
 
 def krea_dit_block_forward8(handle: int, x_img, x_txt, B: int, img_h: int, img_w: int, n_txt: int, t_emb,
@@ -329,6 +361,11 @@ def make_weights(t: Dict[str, object]) -> krea_dit_weights:
 def make_weights8(t: Dict[str, object]) -> krea_dit_weights8:
     """8-bit weights struct from a dict of device tensors keyed by the struct's field names."""
     return krea_dit_weights8(*[_ptr(t[n]) for n, _ in krea_dit_weights8._fields_])
+
+
+def make_weights4(t: Dict[str, object]) -> krea_dit_weights4:
+    """NVFP4 weights struct from a dict of device tensors keyed by the struct's field names."""
+    return krea_dit_weights4(*[_ptr(t[n]) for n, _ in krea_dit_weights4._fields_])
 
 
 def make_temb_weights(t: Dict[str, object]) -> krea_dit_temb_weights:

@@ -17,7 +17,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libkrea_dit.so")
-SOURCES = ["api.cu", "kernels_simt.cu", "norm.cu", "gemm_tc.cu", "attn_tc.cu", "noalloc.cu", "quant8.cu", "backward.cu", "attn_bwd.cu", "selftest.cu"]
+SOURCES = ["api.cu", "kernels_simt.cu", "norm.cu", "gemm_tc.cu", "attn_tc.cu", "noalloc.cu", "quant8.cu", "backward.cu", "attn_bwd.cu", "selftest.cu", "quant4.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

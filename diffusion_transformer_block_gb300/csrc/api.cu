@@ -51,6 +51,9 @@ enum Slot {
   S_BWD_TRANSPOSE,
   S_BWD_POINTWISE,
   S_BWD_ATTN,
+  S_Q4_AMAX,
+  S_Q4_SCALE,
+  S_Q4_CAST,
   S_COUNT
 };
 const char* const kSlotNames[S_COUNT] = {
@@ -61,7 +64,7 @@ const char* const kSlotNames[S_COUNT] = {
     "temb_sinusoid",        "temb_mlp1",             "temb_mlp2",       "norm1_amax",
     "quant_og_e4m3",        "norm2_amax",            "quant_hmid_e4m3", "weights8_row_amax",
     "weights8_quant_e4m3",  "bwd_gemm",              "bwd_transpose",   "bwd_pointwise",
-    "bwd_attention"};
+    "bwd_attention",        "nvfp4_row_amax",        "nvfp4_tensor_scale", "nvfp4_cast"};
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
@@ -169,6 +172,11 @@ struct krea_dit_block_s {
   void *xn8 = nullptr, *og8 = nullptr, *hn8 = nullptr, *hmid8 = nullptr;
   float *dq_xn = nullptr, *dq_og = nullptr, *dq_hn = nullptr, *dq_hmid = nullptr;
   float *am_xn = nullptr, *am_og = nullptr, *am_hn = nullptr, *am_hmid = nullptr, *am_w = nullptr;
+  // NVFP4 mode: E2M1 GEMM operands, their block scales and tensor scales
+  bool mode4 = false;
+  void *xn4 = nullptr, *og4 = nullptr, *hn4 = nullptr, *hmid4 = nullptr;
+  void *sf_xn4 = nullptr, *sf_og4 = nullptr, *sf_hn4 = nullptr, *sf_hmid4 = nullptr;
+  float* ts4 = nullptr;  // [4]: xn, og, hn, hmid
   // backward workspace (krea_dit_block_enable_backward): one allocation, carved below
   char* bw = nullptr;
   size_t bw_Tp = 0, bw_Lp = 0;
@@ -299,7 +307,7 @@ int krea_dit_block_create(const krea_dit_config* c, krea_dit_block_t* out) {
   *out = nullptr;
   if (!c) return KREA_DIT_ERR_INVALID_ARG;
   if (c->mode != KREA_DIT_BF16 && c->mode != KREA_DIT_FP32 && c->mode != KREA_DIT_FP8_TENSOR &&
-      c->mode != KREA_DIT_FP8_ROW)
+      c->mode != KREA_DIT_FP8_ROW && c->mode != KREA_DIT_NVFP4)
     return KREA_DIT_ERR_INVALID_ARG;
   if (c->max_batch < 1 || c->max_seq < 1 || c->img_h_max < 0 || c->img_w_max < 0) return KREA_DIT_ERR_INVALID_ARG;
   if (!(c->eps > 0.f) || !(c->rope_base > 0.f) || (c->gate_on != 0 && c->gate_on != 1))
@@ -329,6 +337,7 @@ int krea_dit_block_create(const krea_dit_config* c, krea_dit_block_t* out) {
   h->num_sms = sms;
   h->bf16 = c->mode != KREA_DIT_FP32;
   h->mode8 = c->mode == KREA_DIT_FP8_TENSOR ? 1 : (c->mode == KREA_DIT_FP8_ROW ? 2 : 0);
+  h->mode4 = c->mode == KREA_DIT_NVFP4;
   h->esz = h->bf16 ? 2 : 4;
   h->max_T = static_cast<size_t>(c->max_batch) * c->max_seq;
   h->n_qkvg = ((c->gate_on ? 2 : 1) * c->n_q + 2 * c->n_kv) * c->head_dim;
@@ -376,6 +385,24 @@ int krea_dit_block_create(const krea_dit_config* c, krea_dit_block_t* out) {
       items.push_back({reinterpret_cast<void**>(p), T * 4, nullptr});
     items.push_back({reinterpret_cast<void**>(&h->am_w), wrows * 4, nullptr});
   }
+  if (h->mode4) {
+    const size_t nqhd = static_cast<size_t>(c->n_q) * hd;
+    size_t wrows = static_cast<size_t>(h->n_qkvg);
+    if (d > wrows) wrows = d;
+    if (F > wrows) wrows = F;
+    items.push_back({&h->xn4, T * d / 2, nullptr});
+    items.push_back({&h->og4, T * nqhd / 2, nullptr});
+    items.push_back({&h->hn4, T * d / 2, nullptr});
+    items.push_back({&h->hmid4, T * F / 2, nullptr});
+    items.push_back({&h->sf_xn4, kd::nvfp4_scale_bytes(static_cast<long long>(T), d), nullptr});
+    items.push_back({&h->sf_og4, kd::nvfp4_scale_bytes(static_cast<long long>(T), nqhd), nullptr});
+    items.push_back({&h->sf_hn4, kd::nvfp4_scale_bytes(static_cast<long long>(T), d), nullptr});
+    items.push_back({&h->sf_hmid4, kd::nvfp4_scale_bytes(static_cast<long long>(T), F), nullptr});
+    items.push_back({reinterpret_cast<void**>(&h->ts4), 4 * sizeof(float), nullptr});
+    for (float** p : {&h->am_xn, &h->am_og, &h->am_hn, &h->am_hmid})
+      items.push_back({reinterpret_cast<void**>(p), T * 4, nullptr});
+    items.push_back({reinterpret_cast<void**>(&h->am_w), wrows * 4, nullptr});
+  }
   items.push_back({reinterpret_cast<void**>(&h->temb_e), static_cast<size_t>(c->max_batch) * 256 * 4, nullptr});
   items.push_back({reinterpret_cast<void**>(&h->temb_h), static_cast<size_t>(c->max_batch) * d * 4, nullptr});
   items.push_back({reinterpret_cast<void**>(&h->rope), static_cast<size_t>(h->rope_rows) * (hd / 4) * 8, nullptr});
@@ -415,6 +442,7 @@ int krea_dit_block_create(const krea_dit_config* c, krea_dit_block_t* out) {
     }
   }
   if (kd::norm_init(c->d_model) != cudaSuccess ||
+      (h->mode4 && kd::gemm_fp4_init() != cudaSuccess) ||
       (h->bf16 && (!get_encode() || kd::gemm_tc_init(sms) != cudaSuccess || kd::attn_tc_init() != cudaSuccess ||
                       kd::attn_bwd_init() != cudaSuccess))) {
     cudaFree(h->ws);
@@ -484,15 +512,23 @@ bool encode_attn_gate_out(CUtensorMap* tm_g, CUtensorMap* tm_og, krea_dit_block_
 
 int forward_impl(krea_dit_block_t h, const void* x_img, const void* x_txt, const void* x_joint, int B, int img_h,
                  int img_w, int n_txt, const float* t_emb, const krea_dit_weights* w, const krea_dit_weights8* w8,
-                 void* out, krea_dit_stream_t stream) {
+                 void* out, krea_dit_stream_t stream, const krea_dit_weights4* w4 = nullptr) {
   if (!h || !w || !t_emb || !out) return KREA_DIT_ERR_INVALID_ARG;
   if ((h->mode8 != 0) != (w8 != nullptr)) return KREA_DIT_ERR_INVALID_ARG;  // 8-bit handles need forward8
+  if (h->mode4 != (w4 != nullptr)) return KREA_DIT_ERR_INVALID_ARG;        // NVFP4 handles need forward4
   if (B < 0 || img_h < 0 || img_w < 0 || n_txt < 0) return KREA_DIT_ERR_INVALID_ARG;
   if (!w->norm1_w || !w->norm2_w || !w->q_norm_w || !w->k_norm_w || !w->mod_bias) return KREA_DIT_ERR_INVALID_ARG;
   if (w8) {
     const void* p8[] = {w8->w_qkvg, w8->w_o,    w8->w_gate, w8->w_up,    w8->w_down,
                         w8->dq_qkvg, w8->dq_o, w8->dq_gate, w8->dq_up, w8->dq_down};
     for (const void* p : p8) {
+      if (!p) return KREA_DIT_ERR_INVALID_ARG;
+      if (!aligned16(p)) return KREA_DIT_ERR_MISALIGNED;
+    }
+  } else if (w4) {
+    const void* p4[] = {w4->w_qkvg,  w4->w_o,  w4->w_gate,  w4->w_up,  w4->w_down,  w4->sf_qkvg, w4->sf_o, w4->sf_gate,
+                        w4->sf_up, w4->sf_down, w4->ts_qkvg, w4->ts_o, w4->ts_gate, w4->ts_up, w4->ts_down};
+    for (const void* p : p4) {
       if (!p) return KREA_DIT_ERR_INVALID_ARG;
       if (!aligned16(p)) return KREA_DIT_ERR_MISALIGNED;
     }
@@ -562,7 +598,61 @@ int forward_impl(krea_dit_block_t h, const void* x_img, const void* x_txt, const
     if (e == cudaSuccess) e = timed(h, slot, st, [&] { return (expr); }); \
   } while (0)
 
-  if (h->mode8) {
+  if (h->mode4) {
+    const uint64_t T = static_cast<uint64_t>(f.T);
+    const uint64_t F = static_cast<uint64_t>(c.ffn), nq = static_cast<uint64_t>(nqhd);
+    CUtensorMap tm_xn4, tm_wqkvg4, tm_og4, tm_wo4, tm_hn4, tm_wgate4, tm_wup4, tm_hmid4, tm_wdown4, tm_q, tm_k, tm_vt,
+        tm_h1, tm_out, tm_g, tm_og;
+    bool ok = encode_2d_u8(&tm_xn4, h->xn4, d / 2, T, 128) &&
+              encode_2d_u8(&tm_wqkvg4, w4->w_qkvg, d / 2, h->n_qkvg, 128) &&
+              encode_2d_u8(&tm_og4, h->og4, nq / 2, T, 128) && encode_2d_u8(&tm_wo4, w4->w_o, nq / 2, d, 128) &&
+              encode_2d_u8(&tm_hn4, h->hn4, d / 2, T, 128) && encode_2d_u8(&tm_wgate4, w4->w_gate, d / 2, F, 128) &&
+              encode_2d_u8(&tm_wup4, w4->w_up, d / 2, F, 128) && encode_2d_u8(&tm_hmid4, h->hmid4, F / 2, T, 128) &&
+              encode_2d_u8(&tm_wdown4, w4->w_down, F / 2, d, 128) &&
+              encode_3d(&tm_q, h->q, c.head_dim, L, static_cast<uint64_t>(B) * c.n_q, c.head_dim, 64, 128) &&
+              encode_3d(&tm_k, h->k, c.head_dim, L, static_cast<uint64_t>(B) * c.n_kv, c.head_dim, 64, 128) &&
+              encode_3d(&tm_vt, h->vt, L, c.head_dim, static_cast<uint64_t>(B) * c.n_kv, f.Lp, 64, 128) &&
+              encode_2d_f32(&tm_h1, h->h1, d, T) && encode_2d(&tm_out, out, d, T, d, 64, 32) &&
+              encode_attn_gate_out(&tm_g, &tm_og, h, B, L);
+    if (!ok) return KREA_DIT_ERR_CUDA;
+    const int sms = h->num_sms;
+    const auto u8 = [](const void* p) { return static_cast<const uint8_t*>(p); };
+    const kd::Op4 a_xn{&tm_xn4, u8(h->sf_xn4)}, a_og{&tm_og4, u8(h->sf_og4)}, a_hn{&tm_hn4, u8(h->sf_hn4)},
+        a_hmid{&tm_hmid4, u8(h->sf_hmid4)};
+    const kd::Op4 b_qkvg{&tm_wqkvg4, u8(w4->sf_qkvg)}, b_o{&tm_wo4, u8(w4->sf_o)}, b_gate{&tm_wgate4, u8(w4->sf_gate)},
+        b_up{&tm_wup4, u8(w4->sf_up)}, b_down{&tm_wdown4, u8(w4->sf_down)};
+    const kd::Deq dq_qkvg{h->ts4 + 0, w4->ts_qkvg, nullptr, 0};
+    const kd::Deq dq_o{h->ts4 + 1, w4->ts_o, nullptr, 0};
+    const kd::Deq dq_ff{h->ts4 + 2, w4->ts_gate, w4->ts_up, 0};
+    const kd::Deq dq_down{h->ts4 + 3, w4->ts_down, nullptr, 0};
+    // NVFP4 cast of a bf16 activation [T, K] whose row amaxes are in am: tensor scale, codes
+    const auto cast4 = [&](const void* src, int K, float* am, float* ts, void* codes, void* sf) {
+      KD_RUN(S_Q4_SCALE, kd::launch_nvfp4_scale(am, f.T, ts, st));
+      KD_RUN(S_Q4_CAST, kd::launch_nvfp4_cast(src, f.T, K, ts, codes, sf, sms, st));
+    };
+    // row amax accumulators of the attention and SwiGLU outputs (atomic max from zero)
+    e = cudaMemsetAsync(h->am_og, 0, T * sizeof(float), st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(h->am_hmid, 0, T * sizeof(float), st);
+    KD_RUN(S_NORM1, kd::launch_norm_modulate(kd::NormIO::BF16_BF16, f, xsrc, w->norm1_w, t_emb, w->mod_bias, 0, 1,
+                                             h->xn, sms, st));
+    KD_RUN(S_Q4_AMAX, kd::launch_row_amax(h->xn, f.T, c.d_model, h->am_xn, sms, st));
+    cast4(h->xn, c.d_model, h->am_xn, h->ts4 + 0, h->xn4, h->sf_xn4);
+    KD_RUN(S_QKVG_TC, kd::launch_gemm_qkvg_fp4(f, a_xn, b_qkvg, h->n_qkvg, dst, dq_qkvg, sms, h->err, st));
+    KD_RUN(S_ATTN, kd::launch_attn_tc(f, &tm_q, &tm_k, &tm_vt, &tm_g, &tm_og, h->am_og, nullptr, nullptr, sms, h->err,
+                                        st));
+    cast4(h->og, nqhd, h->am_og, h->ts4 + 1, h->og4, h->sf_og4);
+    KD_RUN(S_OPROJ_TC, kd::launch_gemm_resid_attn_fp4(f, a_og, b_o, nqhd, xsrc, t_emb, w->mod_bias, &tm_h1, dq_o, sms,
+                                                      h->err, st));
+    KD_RUN(S_NORM2, kd::launch_norm_modulate(kd::NormIO::F32_BF16, f, h1src, w->norm2_w, t_emb, w->mod_bias, 3, 4,
+                                             h->hn, sms, st));
+    KD_RUN(S_Q4_AMAX, kd::launch_row_amax(h->hn, f.T, c.d_model, h->am_hn, sms, st));
+    cast4(h->hn, c.d_model, h->am_hn, h->ts4 + 2, h->hn4, h->sf_hn4);
+    KD_RUN(S_UPGATE_TC, kd::launch_gemm_swiglu_fp4(f, a_hn, b_gate, b_up, h->hmid, h->am_hmid, dq_ff, sms, h->err,
+                                                   st));
+    cast4(h->hmid, c.ffn, h->am_hmid, h->ts4 + 3, h->hmid4, h->sf_hmid4);
+    KD_RUN(S_DOWN_TC, kd::launch_gemm_resid_mlp_fp4(f, a_hmid, b_down, c.ffn, static_cast<const float*>(h->h1), t_emb,
+                                                    w->mod_bias, &tm_out, dq_down, sms, h->err, st));
+  } else if (h->mode8) {
     const int per_row = h->mode8 == 2;
     const uint64_t T = static_cast<uint64_t>(f.T);
     CUtensorMap tm_xn8, tm_wqkvg, tm_og8, tm_wo, tm_hn8, tm_wgate, tm_wup, tm_hmid8, tm_wdown, tm_q, tm_k, tm_vt,
@@ -695,6 +785,51 @@ int krea_dit_block_forward8(krea_dit_block_t h, const void* x_img, const void* x
   return forward_impl(h, x_img, x_txt, nullptr, B, img_h, img_w, n_txt, t_emb, w, q, out, stream);
 }
 
+size_t krea_dit_nvfp4_scale_bytes(int rows, int cols) { return kd::nvfp4_scale_bytes(rows, cols); }
+
+int krea_dit_block_forward4(krea_dit_block_t h, const void* x_img, const void* x_txt, int B, int img_h, int img_w,
+                            int n_txt, const float* t_emb, const krea_dit_weights* w, const krea_dit_weights4* q,
+                            void* out, krea_dit_stream_t stream) {
+  if (!q) return KREA_DIT_ERR_INVALID_ARG;
+  return forward_impl(h, x_img, x_txt, nullptr, B, img_h, img_w, n_txt, t_emb, w, nullptr, out, stream, q);
+}
+
+int krea_dit_weights4_quantize(krea_dit_block_t h, const krea_dit_weights* w, const krea_dit_weights4* q,
+                               krea_dit_stream_t stream) {
+  if (!h || !w || !q || !h->mode4) return KREA_DIT_ERR_INVALID_ARG;
+  const krea_dit_config& c = h->cfg;
+  const int d = c.d_model, F = c.ffn, nqhd = c.n_q * c.head_dim;
+  struct Mat {
+    const void* src;
+    int rows, cols;
+    void* codes;
+    void* sf;
+    float* ts;
+  };
+  const Mat mats[5] = {{w->w_qkvg, h->n_qkvg, d, q->w_qkvg, q->sf_qkvg, q->ts_qkvg},
+                       {w->w_o, d, nqhd, q->w_o, q->sf_o, q->ts_o},
+                       {w->w_gate, F, d, q->w_gate, q->sf_gate, q->ts_gate},
+                       {w->w_up, F, d, q->w_up, q->sf_up, q->ts_up},
+                       {w->w_down, d, F, q->w_down, q->sf_down, q->ts_down}};
+  for (const Mat& m : mats) {
+    if (!m.src || !m.codes || !m.sf || !m.ts) return KREA_DIT_ERR_INVALID_ARG;
+    if (!aligned16(m.src) || !aligned16(m.codes) || !aligned16(m.sf) || !aligned16(m.ts))
+      return KREA_DIT_ERR_MISALIGNED;
+  }
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaSuccess;
+  for (const Mat& m : mats) {
+    if (e == cudaSuccess)
+      e = timed(h, S_Q4_AMAX, st, [&] { return kd::launch_row_amax(m.src, m.rows, m.cols, h->am_w, h->num_sms, st); });
+    if (e == cudaSuccess) e = timed(h, S_Q4_SCALE, st, [&] { return kd::launch_nvfp4_scale(h->am_w, m.rows, m.ts, st); });
+    if (e == cudaSuccess)
+      e = timed(h, S_Q4_CAST, st, [&] {
+        return kd::launch_nvfp4_cast(m.src, m.rows, m.cols, m.ts, m.codes, m.sf, h->num_sms, st);
+      });
+  }
+  return e == cudaSuccess ? KREA_DIT_OK : KREA_DIT_ERR_CUDA;
+}
+
 int krea_dit_weights8_quantize(krea_dit_block_t h, const krea_dit_weights* w, const krea_dit_weights8* q,
                                krea_dit_stream_t stream) {
   if (!h || !w || !q || !h->mode8) return KREA_DIT_ERR_INVALID_ARG;
@@ -803,7 +938,7 @@ int krea_dit_graph_destroy(krea_dit_graph_t g) {
 
 int krea_dit_block_enable_backward(krea_dit_block_t h) {
   if (!h) return KREA_DIT_ERR_INVALID_ARG;
-  if (!h->bf16 || h->mode8) return KREA_DIT_ERR_INVALID_ARG;  // bf16 mode only
+  if (!h->bf16 || h->mode8 || h->mode4) return KREA_DIT_ERR_INVALID_ARG;  // bf16 mode only
   if (h->bw) return KREA_DIT_OK;
   const krea_dit_config& c = h->cfg;
   const size_t T = h->max_T, d = c.d_model, F = c.ffn, hd = c.head_dim;
@@ -1109,6 +1244,39 @@ int krea_dit_block_workspace(krea_dit_block_t h, int which, void** dev_ptr, size
     case KREA_DIT_BUF_OG8: *dev_ptr = h->og8; *bytes = h->mode8 ? T * h->cfg.n_q * hd : 0; break;
     case KREA_DIT_BUF_HN8: *dev_ptr = h->hn8; *bytes = h->mode8 ? T * h->cfg.d_model : 0; break;
     case KREA_DIT_BUF_HMID8: *dev_ptr = h->hmid8; *bytes = h->mode8 ? T * h->cfg.ffn : 0; break;
+    case KREA_DIT_BUF_XN4:
+    case KREA_DIT_BUF_OG4:
+    case KREA_DIT_BUF_HN4:
+    case KREA_DIT_BUF_HMID4:
+    case KREA_DIT_BUF_SF_XN4:
+    case KREA_DIT_BUF_SF_OG4:
+    case KREA_DIT_BUF_SF_HN4:
+    case KREA_DIT_BUF_SF_HMID4:
+    case KREA_DIT_BUF_TS_XN4:
+    case KREA_DIT_BUF_TS_OG4:
+    case KREA_DIT_BUF_TS_HN4:
+    case KREA_DIT_BUF_TS_HMID4: {
+      const size_t nq = static_cast<size_t>(h->cfg.n_q) * hd;
+      const size_t K[4] = {static_cast<size_t>(h->cfg.d_model), nq, static_cast<size_t>(h->cfg.d_model),
+                           static_cast<size_t>(h->cfg.ffn)};
+      void* const codes[4] = {h->xn4, h->og4, h->hn4, h->hmid4};
+      void* const sfs[4] = {h->sf_xn4, h->sf_og4, h->sf_hn4, h->sf_hmid4};
+      const int which4 = (which - KREA_DIT_BUF_XN4) % 4, kind = (which - KREA_DIT_BUF_XN4) / 4;
+      if (!h->mode4) {
+        *dev_ptr = nullptr;
+        *bytes = 0;
+      } else if (kind == 0) {
+        *dev_ptr = codes[which4];
+        *bytes = T * K[which4] / 2;
+      } else if (kind == 1) {
+        *dev_ptr = sfs[which4];
+        *bytes = kd::nvfp4_scale_bytes(static_cast<long long>(T), static_cast<long long>(K[which4]));
+      } else {
+        *dev_ptr = h->ts4 + which4;
+        *bytes = T ? sizeof(float) : 0;
+      }
+      break;
+    }
     case KREA_DIT_BUF_DQ_XN:
     case KREA_DIT_BUF_DQ_OG:
     case KREA_DIT_BUF_DQ_HN:

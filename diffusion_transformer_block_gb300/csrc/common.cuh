@@ -152,6 +152,21 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const void* map, uint64_t
       "l"(map), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z)
       : "memory");
 }
+__device__ __forceinline__ void tma_load_2d(void* dst, const void* map, uint64_t* bar, int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];" ::"r"(
+          smem_u32(dst)),
+      "l"(map), "r"(smem_u32(bar)), "r"(x), "r"(y)
+      : "memory");
+}
+// 1D bulk copy of `bytes` (a multiple of 16, both addresses 16-byte aligned) from global
+// to shared memory, counted in bytes on `bar`
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   smem_u32(dst)),
+               "l"(src), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
+}
 // 2D TMA store of a shared-memory box (laid out as the map's swizzle says) to global
 // memory; completion is tracked per thread by bulk groups. Rows or columns of the box
 // outside the tensor are not written.
@@ -314,6 +329,54 @@ __device__ __forceinline__ void tmem_st64(uint32_t taddr, const uint32_t (&r)[64
       : "memory");
 }
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// ------------------------------------------------------------------ NVFP4 (block-scaled e2m1)
+// Instruction descriptor, kind::mxf4nvf4: E2M1 x E2M1 -> fp32 with E4M3 block scales
+// (scale_vec::4X: four scales per 64-element K step), both operands K-major.
+__host__ __device__ constexpr uint32_t idesc_nvf4_f32(int M, int N) {
+  return (1u << 7)                                 // A format: E2M1
+         | (1u << 10)                              // B format: E2M1
+         | (static_cast<uint32_t>(N >> 3) << 17)   // N / 8
+         | (static_cast<uint32_t>(M >> 4) << 24);  // M / 16 (scale format bit 23 = 0: E4M3)
+}
+// D[tmem] (+)= (A .* SFA) * (B .* SFB)^T, K = 64 per instruction, one CTA, single thread.
+// Row m of A takes its four scales (byte j for elements 16j .. 16j + 15 of the step) from
+// the 32-bit word in TMEM column sfa + m / 32 (lane m % 32 of any lane quadrant); B alike.
+__device__ __forceinline__ void mma_nvf4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                         uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+          d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+// Shared-memory descriptor of a 32-row x 16-byte block without swizzle (8-row groups 128 B
+// apart): the source of a scale-factor copy.
+__device__ __forceinline__ uint64_t sdesc_rows16(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>(128 >> 4) << 16;  // leading byte offset
+  d |= static_cast<uint64_t>(128 >> 4) << 32;  // stride byte offset: 8 rows x 16 B
+  d |= static_cast<uint64_t>(1) << 46;          // descriptor version; layout type 0: no swizzle
+  return d;
+}
+// Copy a 512-byte scale atom (32 rows of 16 bytes: row r holds the words of matrix rows r,
+// r + 32, r + 64, r + 96) from shared memory into TMEM columns taddr .. taddr + 3, every
+// lane quadrant receiving the same 32 lanes; ordered with this thread's MMAs.
+__device__ __forceinline__ void tmem_cp_scales(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+// Two fp32 values -> one byte of two E2M1 codes (lo in the low nibble); nearest, ties to
+// even, saturating at +-6.
+__device__ __forceinline__ uint32_t cvt_e2m1x2(float lo, float hi) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\tcvt.u32.u8 %0, t;\n\t}"
+      : "=r"(r)
+      : "f"(hi), "f"(lo));
+  return r;
+}
 
 // ------------------------------------------------------------------ e4m3 casts
 // Scaled e4m3 operands: a group (a tensor, or one row) with largest magnitude amax is

@@ -772,6 +772,249 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   }
 }
 
+// ------------------------------------------------------------------ NVFP4 GEMM
+// Operands are E2M1 codes (two per byte) with E4M3 scales per 16 elements of K (see
+// quant4.cu for the formats) and one power-of-two tensor scale each; the tensor scales
+// reach the epilogue as the per-tensor factors of an 8-bit epilogue (Deq).
+//
+// One CTA per 128 x 256 output tile (no CTA pairs), persistent over the tiles. A stage
+// covers 256 elements of K (128 bytes of each operand row): A 128 x 128 B and the two
+// 128-row halves of B by TMA with the 128-byte swizzle, and the stage's scale atoms of A
+// and of both B halves by 1D bulk copies (54 KB). Per 64-element step the MMA thread
+// copies the step's three scale atoms into tensor memory (tcgen05.cp, ordered with its
+// MMAs) and issues two kind::mxf4nvf4 MMAs (M = 128, N = 128, K = 64), one per half of B,
+// into the two halves of the 256-column accumulator, which therefore has the layout the
+// bf16 kernel's epilogues read. The accumulator is single-buffered (the scale copies take
+// tensor-memory columns 256 .. 303), so a tile's epilogue does not overlap the next
+// tile's main loop. Warp roles as in the bf16 kernel: 0 TMA, 1 TMEM + MMA, 2..9 epilogue.
+constexpr int F4_BM = 128, F4_BN = 256;
+constexpr int F4_A_BYTES = F4_BM * 128;
+constexpr int F4_BH_BYTES = (F4_BN / 2) * 128;
+constexpr int F4_ATOM = 512;                       // scales of 128 rows x 64 elements
+constexpr int F4_SF_BYTES = 3 * 4 * F4_ATOM;       // A, B half 0, B half 1; four 64-element steps
+constexpr int F4_STAGE = F4_A_BYTES + 2 * F4_BH_BYTES + F4_SF_BYTES;
+constexpr int F4_SF_TMEM = 256;                    // first TMEM column of the scale copies
+template <class Epi>
+__host__ __device__ constexpr int f4_stages() {
+  return StgOf<Epi>::value > 0 ? 3 : 4;
+}
+template <class Epi>
+__host__ __device__ constexpr int f4_smem_bytes() {
+  return f4_stages<Epi>() * F4_STAGE + NUM_EPI_WARPS * StgOf<Epi>::value + 1024 + 256;
+}
+
+template <class Epi, bool DUAL>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    gemm_fp4_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
+                    const __grid_constant__ CUtensorMap tm_b2, const __grid_constant__ CUtensorMap tm_c, int M,
+                    int num_n, int K, int group, int b_blocks, const uint8_t* __restrict__ sf_a,
+                    const uint8_t* __restrict__ sf_b, const uint8_t* __restrict__ sf_b2, Epi epi, int* err) {
+  constexpr int NST = f4_stages<Epi>();
+  constexpr int STG = StgOf<Epi>::value;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* stg_base = smem + NST * F4_STAGE;
+  uint64_t* full = reinterpret_cast<uint64_t*>(stg_base + NUM_EPI_WARPS * STG);
+  uint64_t* empty = full + NST;
+  uint64_t* tfull = empty + NST;
+  uint64_t* tempty = tfull + 1;
+  uint64_t* done = tempty + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int num_m = (M + F4_BM - 1) / F4_BM;
+  const int num_tiles = num_m * num_n;
+  const int KS = K / 64;                  // 64-element steps (scale atoms per 128-row block)
+  const int num_kb = (KS + 3) / 4;        // stages of 256 elements
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NST; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(tfull, 1);
+    mbar_init(tempty, NUM_EPI_WARPS);
+    mbar_init(done, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  // zero every stage's scale area: a B half past the matrix's last 128-row block is not
+  // copied (its codes arrive as TMA zero fill), so its scales must be finite
+  for (int i = threadIdx.x; i < NST * (F4_SF_BYTES / 16); i += blockDim.x) {
+    const int st = i / (F4_SF_BYTES / 16), u = i % (F4_SF_BYTES / 16);
+    reinterpret_cast<uint4*>(smem + st * F4_STAGE + F4_A_BYTES + 2 * F4_BH_BYTES)[u] = make_uint4(0, 0, 0, 0);
+  }
+  fence_proxy_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const WaitCtx wc{abort_flag, err};
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA / bulk-copy producer
+      tma_prefetch_desc(&tm_a);
+      tma_prefetch_desc(&tm_b);
+      if (DUAL) tma_prefetch_desc(&tm_b2);
+      int stage = 0;
+      uint32_t phase = 0;
+      long long issued = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+        int mb, nb;
+        tile_coords(tile, num_m, num_n, group, mb, nb);
+        // B halves: rows of W (or of W_gate / W_up for the SwiGLU GEMM) and their scale blocks
+        const CUtensorMap* map_b1 = DUAL ? &tm_b2 : &tm_b;
+        const int yb0 = DUAL ? nb * 128 : nb * F4_BN, yb1 = DUAL ? nb * 128 : nb * F4_BN + 128;
+        const int rb0 = DUAL ? nb : 2 * nb, rb1 = DUAL ? nb : 2 * nb + 1;  // scale blocks of the halves
+        const bool has1 = rb1 < b_blocks;  // the second half lies (partly) inside the matrix
+        const uint8_t* sfb0 = sf_b + static_cast<size_t>(rb0) * KS * F4_ATOM;
+        const uint8_t* sfb1 = (DUAL ? sf_b2 : sf_b) + static_cast<size_t>(has1 ? rb1 : rb0) * KS * F4_ATOM;
+        const uint8_t* sfa = sf_a + static_cast<size_t>(mb) * KS * F4_ATOM;
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1, wc, SITE_GEMM_PRODUCER)) {
+            ok = false;
+            break;
+          }
+          uint8_t* sa = smem + stage * F4_STAGE;
+          uint8_t* sb = sa + F4_A_BYTES;
+          uint8_t* ssf = sb + 2 * F4_BH_BYTES;
+          const int nks = min(4, KS - 4 * kb);
+          const uint32_t sf_bytes = static_cast<uint32_t>(nks) * F4_ATOM;
+          mbar_arrive_expect_tx(&full[stage], F4_A_BYTES + 2 * F4_BH_BYTES + (has1 ? 3 : 2) * sf_bytes);
+          tma_load_2d(sa, &tm_a, &full[stage], kb * 128, mb * F4_BM);
+          tma_load_2d(sb, &tm_b, &full[stage], kb * 128, yb0);
+          tma_load_2d(sb + F4_BH_BYTES, map_b1, &full[stage], kb * 128, yb1);
+          bulk_load(ssf, sfa + static_cast<size_t>(4 * kb) * F4_ATOM, sf_bytes, &full[stage]);
+          bulk_load(ssf + 4 * F4_ATOM, sfb0 + static_cast<size_t>(4 * kb) * F4_ATOM, sf_bytes, &full[stage]);
+          if (has1)
+            bulk_load(ssf + 8 * F4_ATOM, sfb1 + static_cast<size_t>(4 * kb) * F4_ATOM, sf_bytes, &full[stage]);
+          ++issued;
+          if (++stage == NST) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+      // every copy this thread started has landed before the CTA exits
+      for (long long i = (issued > NST ? issued - NST : 0); i < issued; ++i)
+        drain_wait(&full[i % NST], static_cast<uint32_t>((i / NST) & 1), err, SITE_GEMM_TEARDOWN);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------- scale copies + MMA issue
+      constexpr uint32_t idesc = idesc_nvf4_f32(F4_BM, F4_BN / 2);
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+        if (!mbar_wait(tempty, acc_phase ^ 1, wc, SITE_GEMM_MMA)) break;
+        tc_fence_after();
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait(&full[stage], phase, wc, SITE_GEMM_MMA)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(smem + stage * F4_STAGE);
+          const uint32_t sb = sa + F4_A_BYTES;
+          const uint32_t ssf = sb + 2 * F4_BH_BYTES;
+          const int nks = min(4, KS - 4 * kb);
+          for (int k = 0; k < nks; ++k) {  // 64 elements = 32 bytes of each row per step
+            const uint32_t t_sf = tmem_base + F4_SF_TMEM + static_cast<uint32_t>(k * 12);
+            tmem_cp_scales(t_sf, sdesc_rows16(ssf + k * F4_ATOM));
+            tmem_cp_scales(t_sf + 4, sdesc_rows16(ssf + (4 + k) * F4_ATOM));
+            tmem_cp_scales(t_sf + 8, sdesc_rows16(ssf + (8 + k) * F4_ATOM));
+            const uint32_t acc = (kb | k) != 0 ? 1u : 0u;
+            const uint64_t adesc = sdesc_kmajor_sw128(sa + k * 32);
+            mma_nvf4(tmem_base, adesc, sdesc_kmajor_sw128(sb + k * 32), idesc, t_sf, t_sf + 4, acc);
+            mma_nvf4(tmem_base + 128, adesc, sdesc_kmajor_sw128(sb + F4_BH_BYTES + k * 32), idesc, t_sf, t_sf + 8,
+                     acc);
+          }
+          mma_commit(&empty[stage]);  // frees the stage once these MMAs have read it
+          if (++stage == NST) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (!ok) break;
+        mma_commit(tfull);  // accumulator ready for the epilogue
+        acc_phase ^= 1;
+      }
+      mma_commit(done);  // completes when every MMA and copy issued above has finished
+      drain_wait(done, 0, err, SITE_GEMM_TEARDOWN);
+    }
+  } else {
+    // ---------------- epilogue warps
+    const int quad = warp & 3;        // TMEM lanes this warp may access: 32*quad ..
+    const int half = (warp - 2) / 4;  // 128-column half of the accumulator
+    uint32_t acc_phase = 0;
+    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+      int mb, nb;
+      tile_coords(tile, num_m, num_n, group, mb, nb);
+      const bool got = mbar_wait(tfull, acc_phase, wc, SITE_GEMM_EPILOGUE);
+      if (!__all_sync(0xffffffffu, got)) break;
+      tc_fence_after();
+      const int row = mb * F4_BM + quad * 32 + lane;
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16);
+      if constexpr (STG > 0)
+        epi.apply(row, nb, half, taddr, M, stg_base + (warp - 2) * STG, lane, &tm_c);
+      else
+        epi.apply(row, nb, half, taddr, M);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty);
+      acc_phase ^= 1;
+    }
+    if constexpr (STG > 0) {  // this warp's TMA stores have completed
+      if (lane == 0) bulk_wait_all();
+      __syncwarp();
+    }
+  }
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, 512);
+  }
+}
+
+template <class Epi, bool DUAL>
+cudaError_t set_smem_attr_fp4() {
+  static_assert(f4_smem_bytes<Epi>() <= 232448, "shared memory per CTA");
+  return cudaFuncSetAttribute(gemm_fp4_kernel<Epi, DUAL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              f4_smem_bytes<Epi>());
+}
+
+// NVFP4 operands: tm_a / tm_b / tm_b2 are byte maps over the codes ([rows, K/2], 128-byte
+// boxes); sf_* the scale atoms; K in elements (a multiple of 64).
+template <class Epi, bool DUAL>
+cudaError_t launch_fp4(const CUtensorMap* a, const CUtensorMap* b, const CUtensorMap* b2, const uint8_t* sf_a,
+                       const uint8_t* sf_b, const uint8_t* sf_b2, int M, int N, int num_n, int K, const Epi& epi,
+                       int num_sms, int* err, cudaStream_t st, const CUtensorMap* c = nullptr) {
+  if (StgOf<Epi>::value > 0 && !c) return cudaErrorInvalidValue;
+  if (K % 64 || !sf_a || !sf_b || (DUAL && !sf_b2)) return cudaErrorInvalidValue;
+  const int num_m = (M + F4_BM - 1) / F4_BM;
+  const int tiles = num_m * num_n;
+  if (tiles == 0) return cudaSuccess;
+  // tile raster: B resident (n-fastest) when all of it fits and is no larger than A
+  const long long a_all = static_cast<long long>(num_m) * F4_BM * (K / 2);
+  const long long b_all = static_cast<long long>(num_n) * F4_BN * (K / 2);
+  const int group = (b_all <= a_all && b_all <= (80ll << 20)) ? 1 : 16;
+  const int grid = tiles < num_sms ? tiles : num_sms;  // persistent: one CTA per SM
+  const int b_blocks = (N + 127) / 128;  // 128-row scale blocks of B (of W_gate / W_up for the SwiGLU GEMM)
+  gemm_fp4_kernel<Epi, DUAL><<<grid, NUM_THREADS, f4_smem_bytes<Epi>(), st>>>(
+      *a, *b, *b2, c ? *c : *a, M, num_n, K, group, b_blocks, sf_a, sf_b, DUAL ? sf_b2 : sf_b, epi, err);
+  return cudaGetLastError();
+}
+
 // Co-resident CTA pairs per instantiation, queried once by gemm_tc_init.
 template <class Epi, bool DUAL>
 struct MaxClusters {
@@ -859,6 +1102,14 @@ cudaError_t gemm_tc_init_set(int num_sms) {
   return set_smem_attr<EpiSwiGLUT<S8>, true>(num_sms);
 }
 
+cudaError_t gemm_fp4_init() {
+  cudaError_t e;
+  if ((e = set_smem_attr_fp4<EpiQKVGT<true>, false>()) != cudaSuccess) return e;
+  if ((e = set_smem_attr_fp4<EpiResidAttnT<true>, false>()) != cudaSuccess) return e;
+  if ((e = set_smem_attr_fp4<EpiResidMlpT<true>, false>()) != cudaSuccess) return e;
+  return set_smem_attr_fp4<EpiSwiGLUT<true>, true>();
+}
+
 cudaError_t gemm_tc_init(int num_sms) {
   cudaError_t e = gemm_tc_init_set<false>(num_sms);
   if (e == cudaSuccess) e = gemm_tc_init_set<true>(num_sms);
@@ -942,6 +1193,42 @@ cudaError_t launch_gemm_swiglu(const Fwd& f, const CUtensorMap* tm_a, const CUte
   }
   EpiSwiGLUT<false> epi{f.F, reinterpret_cast<bf16*>(hmid), rowamax, Deq{}, pre_a, pre_u};
   return launch<EpiSwiGLUT<false>, true>(tm_a, tm_gate, tm_up, f.T, num_n, f.d, epi, num_sms, err, st);
+}
+
+// ---- NVFP4 launchers (Op4: codes' tensor map, scale atoms; dq: the tensor scales)
+cudaError_t launch_gemm_qkvg_fp4(const Fwd& f, const Op4& a, const Op4& b, int N, const QkvgDst& dst, const Deq& dq,
+                                 int num_sms, int* err, cudaStream_t st) {
+  const int num_n = (N + BN - 1) / BN;
+  EpiQKVGT<true> epi{f, dst, N, dq};
+  return launch_fp4<EpiQKVGT<true>, false>(a.map, b.map, b.map, a.sf, b.sf, b.sf, f.T, N, num_n, f.d, epi, num_sms,
+                                           err, st);
+}
+
+cudaError_t launch_gemm_resid_attn_fp4(const Fwd& f, const Op4& a, const Op4& b, int K, RowSrc x,
+                                       const float* mod_shared, const float* mod_bias, const CUtensorMap* tm_h1,
+                                       const Deq& dq, int num_sms, int* err, cudaStream_t st) {
+  const int num_n = (f.d + BN - 1) / BN;
+  EpiResidAttnT<true> epi{f, x, mod_shared, mod_bias, 2, dq};
+  return launch_fp4<EpiResidAttnT<true>, false>(a.map, b.map, b.map, a.sf, b.sf, b.sf, f.T, f.d, num_n, K, epi,
+                                                num_sms, err, st, tm_h1);
+}
+
+cudaError_t launch_gemm_resid_mlp_fp4(const Fwd& f, const Op4& a, const Op4& b, int K, const float* h1,
+                                      const float* mod_shared, const float* mod_bias, const CUtensorMap* tm_out,
+                                      const Deq& dq, int num_sms, int* err, cudaStream_t st) {
+  const int num_n = (f.d + BN - 1) / BN;
+  const RowSrc res{nullptr, nullptr, h1};
+  EpiResidMlpT<true> epi{f, res, mod_shared, mod_bias, 5, dq};
+  return launch_fp4<EpiResidMlpT<true>, false>(a.map, b.map, b.map, a.sf, b.sf, b.sf, f.T, f.d, num_n, K, epi,
+                                               num_sms, err, st, tm_out);
+}
+
+cudaError_t launch_gemm_swiglu_fp4(const Fwd& f, const Op4& a, const Op4& gate, const Op4& up, void* hmid,
+                                   float* rowamax, const Deq& dq, int num_sms, int* err, cudaStream_t st) {
+  const int num_n = (f.F + 127) / 128;
+  EpiSwiGLUT<true> epi{f.F, reinterpret_cast<bf16*>(hmid), rowamax, dq};
+  return launch_fp4<EpiSwiGLUT<true>, true>(a.map, gate.map, up.map, a.sf, gate.sf, up.sf, f.T, f.F, num_n, f.d,
+                                            epi, num_sms, err, st);
 }
 
 }  // namespace kd

@@ -190,6 +190,33 @@ cudaError_t launch_qkv_bwd(const Fwd& f, const float* raw, int ldr, const float*
                            const float* q_norm_w, const float* k_norm_w, const float2* rope, void* d_P, int ldp,
                            float* d_qw, float* d_kw, cudaStream_t st);
 
+// ---- NVFP4 (quant4.cu casts, gemm_tc.cu GEMMs) ----
+// one NVFP4 GEMM operand: a byte tensor map over its E2M1 codes ([rows, K/2], 128-byte
+// boxes, 128-byte swizzle) and its scale atoms (see quant4.cu)
+struct Op4 {
+  const CUtensorMap* map;
+  const uint8_t* sf;
+};
+// bytes of the scale atoms of a [rows, cols] operand (rows padded to 128)
+size_t nvfp4_scale_bytes(long long rows, long long cols);
+// ts[0] = power-of-two tensor scale from rowamax[0..R)
+cudaError_t launch_nvfp4_scale(const float* rowamax, int R, float* ts, cudaStream_t st);
+// codes / scale atoms of a bf16 [R, K] operand (K % 64 == 0) with the tensor scale ts[0]
+cudaError_t launch_nvfp4_cast(const void* src, int R, int K, const float* ts, void* codes, void* sf, int num_sms,
+                              cudaStream_t st);
+// sets the NVFP4 GEMM kernels' shared-memory limits (once per handle, before any capture)
+cudaError_t gemm_fp4_init();
+cudaError_t launch_gemm_qkvg_fp4(const Fwd& f, const Op4& a, const Op4& b, int N, const QkvgDst& dst, const Deq& dq,
+                                 int num_sms, int* err, cudaStream_t st);
+cudaError_t launch_gemm_resid_attn_fp4(const Fwd& f, const Op4& a, const Op4& b, int K, RowSrc x,
+                                       const float* mod_shared, const float* mod_bias, const CUtensorMap* tm_h1,
+                                       const Deq& dq, int num_sms, int* err, cudaStream_t st);
+cudaError_t launch_gemm_resid_mlp_fp4(const Fwd& f, const Op4& a, const Op4& b, int K, const float* h1,
+                                      const float* mod_shared, const float* mod_bias, const CUtensorMap* tm_out,
+                                      const Deq& dq, int num_sms, int* err, cudaStream_t st);
+cudaError_t launch_gemm_swiglu_fp4(const Fwd& f, const Op4& a, const Op4& gate, const Op4& up, void* hmid,
+                                   float* rowamax, const Deq& dq, int num_sms, int* err, cudaStream_t st);
+
 // ---- selftest.cu ----
 // one CTA per SM waits (bounded by limit_ns) on an mbarrier nothing arrives at, records
 // `site` in *err, frees its tensor memory and returns

@@ -1,0 +1,119 @@
+// NVFP4 casts of GEMM operands (Krea 2 Technical Report, "讨论与未来工作" / Discussion and
+// future work: NVFP4 pretraining as a next step).
+//
+// An operand [R, K] (K a multiple of 64) becomes E2M1 codes, two per byte (element 2i in
+// the low nibble), with one E4M3 scale per 16 consecutive elements of a row and one
+// power-of-two tensor scale s_t = 2^j, j the smallest integer with amax <= 448 * 6 * 2^j:
+//   s_b = E4M3(amax_b / (6 s_t)),  q_i = E2M1(x_i / (s_b s_t))  (q = 0 where s_b = 0),
+// both casts rounding to nearest even and saturating. Every division is by an exact value
+// (6 s_t, s_b s_t), so fp32 takes the same rounding decisions as exact arithmetic.
+//
+// The scales are stored in the order the tensor core's scale copy reads them: for each
+// 128-row block rb and each 64-element step ks of K, a 512-byte atom whose byte
+// (r % 32) * 16 + (r / 32) * 4 + j holds the scale of row r (of the block) for elements
+// 16 j .. 16 j + 15 of the step. Rows of the last block past R get scale 0.
+#include <cuda_fp8.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace kd {
+namespace {
+
+constexpr int Q4T = 256;  // threads per CTA of the cast
+
+// ts[0] = the tensor scale from the row amaxes (one CTA)
+__global__ void __launch_bounds__(1024) nvfp4_scale_kernel(const float* __restrict__ rowamax, int R,
+                                                           float* __restrict__ ts) {
+  __shared__ float red[32];
+  float m = 0.0f;
+  for (int i = threadIdx.x; i < R; i += blockDim.x) m = fmaxf(m, rowamax[i]);
+  m = warp_max(m);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float amax = 0.0f;
+    for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) amax = fmaxf(amax, red[w]);
+    float s = 1.0f;
+    if (amax > 0.0f) {
+      int e = 0;
+      const float m0 = frexpf(amax / 2688.0f, &e);  // amax / (448 * 6) = m0 2^e, 0.5 <= m0 < 1
+      s = pow2f(m0 == 0.5f ? e - 1 : e);
+    }
+    ts[0] = s;
+  }
+}
+
+// One thread per 16-element block of the padded rows.
+__global__ void __launch_bounds__(Q4T) nvfp4_cast_kernel(const bf16* __restrict__ src, int R, int K,
+                                                         const float* __restrict__ ts_p, uint8_t* __restrict__ codes,
+                                                         uint8_t* __restrict__ sf) {
+  const int KB = K / 16, KS = K / 64;
+  const long long rows = (static_cast<long long>(R) + 127) / 128 * 128;
+  const long long nblk = rows * KB;
+  const float ts = ts_p[0];
+  const float six_ts = 6.0f * ts;
+  for (long long i = static_cast<long long>(blockIdx.x) * Q4T + threadIdx.x; i < nblk;
+       i += static_cast<long long>(gridDim.x) * Q4T) {
+    const int r = static_cast<int>(i / KB), kb = static_cast<int>(i - static_cast<long long>(r) * KB);
+    uint32_t sbyte = 0;
+    if (r < R) {
+      const uint4* p = reinterpret_cast<const uint4*>(src + static_cast<size_t>(r) * K + kb * 16);
+      const uint4 u0 = p[0], u1 = p[1];
+      const uint32_t w[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+      float v[16];
+      float amax = 0.0f;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const float2 f = unpack_bf16x2(w[q]);
+        v[2 * q] = f.x;
+        v[2 * q + 1] = f.y;
+        amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
+      }
+      sbyte = cvt_e4m3x2(amax / six_ts, 0.0f) & 0xFFu;  // block scale code
+      __nv_fp8_e4m3 sb8;
+      sb8.__x = static_cast<__nv_fp8_storage_t>(sbyte);
+      const float den = static_cast<float>(sb8) * ts;  // exact: an E4M3 value times a power of two
+      uint32_t lo = 0, hi = 0;
+      if (den > 0.0f) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          lo |= cvt_e2m1x2(v[2 * q] / den, v[2 * q + 1] / den) << (8 * q);
+          hi |= cvt_e2m1x2(v[8 + 2 * q] / den, v[8 + 2 * q + 1] / den) << (8 * q);
+        }
+      }
+      *reinterpret_cast<uint2*>(codes + static_cast<size_t>(r) * (K / 2) + kb * 8) = make_uint2(lo, hi);
+    }
+    const int rb = r / 128, rr = r % 128, ks = kb / 4, j = kb % 4;
+    sf[(static_cast<size_t>(rb) * KS + ks) * 512 + (rr % 32) * 16 + (rr / 32) * 4 + j] = static_cast<uint8_t>(sbyte);
+  }
+}
+
+}  // namespace
+
+size_t nvfp4_scale_bytes(long long rows, long long cols) {
+  if (rows <= 0 || cols <= 0) return 0;
+  return static_cast<size_t>((rows + 127) / 128 * 128) * static_cast<size_t>(cols / 16);
+}
+
+cudaError_t launch_nvfp4_scale(const float* rowamax, int R, float* ts, cudaStream_t st) {
+  if (R <= 0) return cudaSuccess;
+  nvfp4_scale_kernel<<<1, 1024, 0, st>>>(rowamax, R, ts);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_nvfp4_cast(const void* src, int R, int K, const float* ts, void* codes, void* sf, int num_sms,
+                              cudaStream_t st) {
+  if (R <= 0 || K <= 0) return cudaSuccess;
+  if (K % 64) return cudaErrorInvalidValue;
+  const long long nblk = (static_cast<long long>(R) + 127) / 128 * 128 * (K / 16);
+  long long grid = (nblk + Q4T - 1) / Q4T;
+  const long long cap = 8LL * num_sms;
+  if (grid > cap) grid = cap;
+  nvfp4_cast_kernel<<<static_cast<unsigned>(grid), Q4T, 0, st>>>(reinterpret_cast<const bf16*>(src), R, K, ts,
+                                                                  reinterpret_cast<uint8_t*>(codes),
+                                                                  reinterpret_cast<uint8_t*>(sf));
+  return cudaGetLastError();
+}
+
+}  // namespace kd

@@ -9,18 +9,21 @@ from typing import Dict, Optional, Sequence
 
 import torch
 
-from . import (KREA_DIT_BF16, KREA_DIT_FP8_ROW, KREA_DIT_FP8_TENSOR, KREA_DIT_FP32, krea_dit_block_create,
-               krea_dit_block_destroy, krea_dit_block_forward, krea_dit_block_forward8, krea_dit_block_forward_joint,
-               krea_dit_block_workspace, krea_dit_weights8_quantize, make_weights8, krea_dit_block_backward,
-               krea_dit_block_enable_backward, make_grads,
-               krea_dit_graph_destroy, krea_dit_graph_launch, krea_dit_stack_forward, krea_dit_stack_graph_create,
-               krea_dit_timestep_embed, make_config, make_temb_weights, make_weights)
+from . import (KREA_DIT_BF16, KREA_DIT_FP32, KREA_DIT_FP8_ROW, KREA_DIT_FP8_TENSOR, KREA_DIT_NVFP4,
+               krea_dit_block_backward, krea_dit_block_create, krea_dit_block_destroy,
+               krea_dit_block_enable_backward, krea_dit_block_forward, krea_dit_block_forward4,
+               krea_dit_block_forward8, krea_dit_block_forward_joint, krea_dit_block_workspace,
+               krea_dit_graph_destroy, krea_dit_graph_launch, krea_dit_nvfp4_scale_bytes, krea_dit_stack_forward,
+               krea_dit_stack_graph_create, krea_dit_timestep_embed, krea_dit_weights4_quantize,
+               krea_dit_weights8_quantize, make_config, make_grads, make_temb_weights, make_weights, make_weights4,
+               make_weights8)
 
 WEIGHT_KEYS = ("w_qkvg", "w_o", "w_gate", "w_up", "w_down", "norm1_w", "norm2_w", "q_norm_w", "k_norm_w",
                "mod_bias")
 TEMB_KEYS = ("w1", "b1", "w2", "b2")
 MATRIX_KEYS = ("w_qkvg", "w_o", "w_gate", "w_up", "w_down")
-MODES = {"bf16": KREA_DIT_BF16, "fp32": KREA_DIT_FP32, "fp8_tensor": KREA_DIT_FP8_TENSOR, "fp8_row": KREA_DIT_FP8_ROW}
+MODES = {"bf16": KREA_DIT_BF16, "fp32": KREA_DIT_FP32, "fp8_tensor": KREA_DIT_FP8_TENSOR, "fp8_row": KREA_DIT_FP8_ROW,
+         "nvfp4": KREA_DIT_NVFP4}
 
 
 class _DevView:
@@ -33,7 +36,8 @@ class _DevView:
 
 class DitBlock:
     """One block handle. ``mode`` is "bf16", "fp32" (the storage / arithmetic mode) or
-    "fp8_tensor" / "fp8_row" (bf16 storage, 8-bit GEMMs with tensor-wise / row-wise scales)."""
+    "fp8_tensor" / "fp8_row" (bf16 storage, 8-bit GEMMs with tensor-wise / row-wise scales) or "nvfp4"
+    (bf16 storage, NVFP4 GEMMs)."""
 
     def __init__(self, *, max_batch: int, max_seq: int, d: int, n_q: int, n_kv: int, hd: int, F: int,
                  img_h_max: int, img_w_max: int, gate_on: bool = True, mode: str = "bf16", eps: float = 1e-6,
@@ -41,6 +45,7 @@ class DitBlock:
         self.device = torch.device(device)
         self.mode = mode
         self.mode8 = mode.startswith("fp8")
+        self.mode4 = mode == "nvfp4"
         self.dtype = torch.float32 if mode == "fp32" else torch.bfloat16
         self.dims = dict(d=d, n_q=n_q, n_kv=n_kv, hd=hd, F=F, gate_on=gate_on)
         cfg = make_config(max_batch=max_batch, max_seq=max_seq, d_model=d, n_q=n_q, n_kv=n_kv, head_dim=hd, ffn=F,
@@ -54,6 +59,8 @@ class DitBlock:
         self._twstruct = None
         self.w8: Dict[str, torch.Tensor] = {}
         self._w8struct = None
+        self.w4: Dict[str, torch.Tensor] = {}
+        self._w4struct = None
 
     def set_weights(self, w: Dict[str, torch.Tensor], stream=None) -> None:
         """Uploads the weights; in an 8-bit mode also casts the matrices to e4m3 codes."""
@@ -69,6 +76,18 @@ class DitBlock:
             self.w8 = w8
             self._w8struct = make_weights8(w8)
             krea_dit_weights8_quantize(self.handle, self._wstruct, self._w8struct,
+                                       stream or torch.cuda.current_stream(self.device))
+        if self.mode4:
+            w4: Dict[str, torch.Tensor] = {}
+            for k in MATRIX_KEYS:
+                rows, cols = self.w[k].shape
+                w4[k] = torch.empty(rows, cols // 2, device=self.device, dtype=torch.uint8)
+                w4["sf_" + k[2:]] = torch.empty(krea_dit_nvfp4_scale_bytes(rows, cols), device=self.device,
+                                                dtype=torch.uint8)
+                w4["ts_" + k[2:]] = torch.empty(4, device=self.device, dtype=torch.float32)
+            self.w4 = w4
+            self._w4struct = make_weights4(w4)
+            krea_dit_weights4_quantize(self.handle, self._wstruct, self._w4struct,
                                        stream or torch.cuda.current_stream(self.device))
 
     def set_temb_weights(self, tw: Dict[str, torch.Tensor]) -> None:
@@ -92,6 +111,9 @@ class DitBlock:
         st = stream or torch.cuda.current_stream(self.device)
         if self.mode8:
             krea_dit_block_forward8(self.handle, xi, xt, B, img_h, img_w, n_txt, t_emb, self._wstruct, self._w8struct,
+                                    out, st)
+        elif self.mode4:
+            krea_dit_block_forward4(self.handle, xi, xt, B, img_h, img_w, n_txt, t_emb, self._wstruct, self._w4struct,
                                     out, st)
         else:
             krea_dit_block_forward(self.handle, xi, xt, B, img_h, img_w, n_txt, t_emb, self._wstruct, out, st)
@@ -153,8 +175,10 @@ class DitBlock:
         (H1 and the DQ_* factors are fp32, the *8 e4m3 codes are returned as uint8, every
         other buffer is in the storage dtype)."""
         ptr, nbytes = krea_dit_block_workspace(self.handle, name)
-        if name.endswith("8"):
+        if name.endswith(("8", "4")) or name.startswith("SF_"):
             esz = 1
+        elif name.startswith("TS_"):
+            esz = 4
         elif name == "H1" or name.startswith("DQ_") or self.mode == "fp32":
             esz = 4
         else:

@@ -68,6 +68,11 @@ extern "C" {
  * take e4m3 operands, see krea_dit_block_forward8. */
 #define KREA_DIT_FP8_TENSOR 2
 #define KREA_DIT_FP8_ROW 3
+/* NVFP4 GEMM mode (Krea 2 Technical Report, "Discussion and future work": pretraining at
+ * NVFP4 precision). Activations, outputs and the non-GEMM steps are as in KREA_DIT_BF16;
+ * the four GEMMs take NVFP4 operands (E2M1 elements with an E4M3 scale per 16 elements
+ * along K and a power-of-two scale per tensor), see krea_dit_block_forward4. */
+#define KREA_DIT_NVFP4 4
 
 typedef struct krea_dit_block_s* krea_dit_block_t;
 /* Same object as cudaStream_t / CUstream. NULL means the legacy default stream. */
@@ -83,9 +88,9 @@ typedef struct CUstream_st* krea_dit_stream_t;
  *  eps                 : RMSNorm epsilon (the block uses 1e-6)
  *  rope_base           : RoPE base (10000)
  *  gate_on             : 1 = sigmoid output gate on attention, 0 = off (then w_qkvg has no g rows)
- *  mode                : KREA_DIT_BF16, KREA_DIT_FP32, KREA_DIT_FP8_TENSOR or
- *                        KREA_DIT_FP8_ROW (the 8-bit modes need head_dim 128, like BF16,
- *                        and d_model <= 3072) */
+ *  mode                : KREA_DIT_BF16, KREA_DIT_FP32, KREA_DIT_FP8_TENSOR,
+ *                        KREA_DIT_FP8_ROW or KREA_DIT_NVFP4 (the 8-bit and NVFP4 modes
+ *                        need head_dim 128, like BF16; the 8-bit modes d_model <= 3072) */
 typedef struct {
   int max_batch, max_seq;
   int d_model, n_q, n_kv, head_dim, ffn;
@@ -138,6 +143,37 @@ typedef struct {
   float* dq_up;
   float* dq_down;
 } krea_dit_weights8;
+
+/* NVFP4 GEMM weights of one block (mode KREA_DIT_NVFP4), all device memory, caller-owned,
+ * filled by krea_dit_weights4_quantize. For a bf16 matrix W [rows, cols] of
+ * krea_dit_weights (cols = K, a multiple of 64):
+ *  w_*   E2M1 codes [rows, cols / 2] bytes, element 2i of a row in the low nibble of byte i
+ *  sf_*  E4M3 block scales, krea_dit_nvfp4_scale_bytes(rows, cols) bytes: for each 128-row
+ *        block rb (rows padded to 128) and each 64-element step ks of K a 512-byte atom
+ *        at offset (rb * cols / 64 + ks) * 512 whose byte (r % 32) * 16 + (r / 32) * 4 + j
+ *        scales elements 16j .. 16j + 15 of the step in row r of the block (padding rows 0)
+ *  ts_*  fp32 [1]: the tensor scale s_t
+ * Rule: s_t = 2^j, j the smallest integer with amax <= 448 * 6 * 2^j (1 when amax = 0);
+ * a block of 16 with largest magnitude a_b gets s_b = E4M3(a_b / (6 s_t)) and its elements
+ * q = E2M1(x / (s_b s_t)) (0 where s_b = 0); casts round to nearest even and saturate.
+ * W is approximated by q * s_b * s_t. */
+typedef struct {
+  void* w_qkvg;
+  void* w_o;
+  void* w_gate;
+  void* w_up;
+  void* w_down;
+  void* sf_qkvg;
+  void* sf_o;
+  void* sf_gate;
+  void* sf_up;
+  void* sf_down;
+  float* ts_qkvg;
+  float* ts_o;
+  float* ts_gate;
+  float* ts_up;
+  float* ts_down;
+} krea_dit_weights4;
 
 /* Shared timestep-MLP weights, fp32 device memory: w1 [d, 256], b1 [d], w2 [6d, d], b2 [6d]. */
 typedef struct {
@@ -221,6 +257,29 @@ int krea_dit_weights8_quantize(krea_dit_block_t h, const krea_dit_weights* w, co
  * (INVALID_ARG). */
 int krea_dit_block_forward8(krea_dit_block_t h, const void* x_img, const void* x_txt, int B, int img_h, int img_w,
                             int n_txt, const float* t_emb, const krea_dit_weights* w, const krea_dit_weights8* q,
+                            void* out, krea_dit_stream_t stream);
+
+/* ---- NVFP4 GEMM forward (mode KREA_DIT_NVFP4) ---------------------------------------- */
+
+/* Bytes of the block scales of a [rows, cols] matrix (cols a multiple of 64; rows padded to
+ * a multiple of 128): ceil(rows / 128) * 128 * cols / 16. 0 for rows <= 0 or cols <= 0. */
+size_t krea_dit_nvfp4_scale_bytes(int rows, int cols);
+
+/* Cast the bf16 GEMM weights of w to NVFP4 into the caller's buffers of q (layout and rule
+ * at krea_dit_weights4). Enqueued on `stream`; the other fields of w are not read. Errors:
+ * INVALID_ARG for a NULL pointer or a handle not in KREA_DIT_NVFP4 mode, MISALIGNED. */
+int krea_dit_weights4_quantize(krea_dit_block_t h, const krea_dit_weights* w, const krea_dit_weights4* q,
+                               krea_dit_stream_t stream);
+
+/* krea_dit_block_forward with NVFP4 GEMM operands. Each of the four GEMMs casts its
+ * activation operand (the bf16 value the BF16 mode stores there: xn, o_g, hn, hmid) to
+ * NVFP4 with one tensor scale for the whole [B L, K] activation of the call, and
+ * multiplies it by the weight codes of q on the tensor core (block-scaled E2M1 MMA, fp32
+ * accumulation); the tensor scales multiply the products in the epilogue. Arguments and
+ * errors as krea_dit_block_forward8, with q the NVFP4 weights. A handle in this mode
+ * rejects every other forward (INVALID_ARG). */
+int krea_dit_block_forward4(krea_dit_block_t h, const void* x_img, const void* x_txt, int B, int img_h, int img_w,
+                            int n_txt, const float* t_emb, const krea_dit_weights* w, const krea_dit_weights4* q,
                             void* out, krea_dit_stream_t stream);
 
 /* ---- block backward (KREA_DIT_BF16 mode) -------------------------------------------- */
@@ -367,6 +426,20 @@ int krea_dit_block_host_sync(krea_dit_block_t h);
 #define KREA_DIT_BUF_DQ_OG 14
 #define KREA_DIT_BUF_DQ_HN 15
 #define KREA_DIT_BUF_DQ_HMID 16
+/* NVFP4 mode: the GEMM operands of the last forward: E2M1 codes ([T, K/2] bytes), block
+ * scales (the atom layout of krea_dit_weights4) and tensor scales (fp32 [1]) */
+#define KREA_DIT_BUF_XN4 17
+#define KREA_DIT_BUF_OG4 18
+#define KREA_DIT_BUF_HN4 19
+#define KREA_DIT_BUF_HMID4 20
+#define KREA_DIT_BUF_SF_XN4 21
+#define KREA_DIT_BUF_SF_OG4 22
+#define KREA_DIT_BUF_SF_HN4 23
+#define KREA_DIT_BUF_SF_HMID4 24
+#define KREA_DIT_BUF_TS_XN4 25
+#define KREA_DIT_BUF_TS_OG4 26
+#define KREA_DIT_BUF_TS_HN4 27
+#define KREA_DIT_BUF_TS_HMID4 28
 int krea_dit_block_workspace(krea_dit_block_t h, int which, void** dev_ptr, size_t* bytes);
 
 /* Per-kernel timing. When enabled, each forward records a CUDA event before and after

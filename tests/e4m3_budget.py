@@ -1,4 +1,4 @@
-"""A-priori allowances for the 8-bit GEMM parity checks (host logic, no GPU).
+"""A-priori allowances for the 8-bit and NVFP4 GEMM parity checks (host logic, no GPU).
 
 An 8-bit GEMM casts an activation operand from a stored bf16 value v with one
 power-of-two scale 2^k per group (a token row, or the whole tensor), k fixed by the
@@ -101,3 +101,56 @@ def attention_spread(q, k, v) -> np.ndarray:
         p /= p.sum(axis=1, keepdims=True)
         out[:, h * hd:(h + 1) * hd] = np.sqrt((p * p) @ (v[kv] ** 2))
     return out
+
+
+# ------------------------------------------------------------------ NVFP4 casts
+def _e4m3_grid() -> np.ndarray:
+    """Every non-negative E4M3 value, ascending (0, the subnormals, the normals up to 448)."""
+    vals = [m * 2.0 ** -9 for m in range(8)]
+    vals += [(1 + m / 8.0) * 2.0 ** (e - 7) for e in range(1, 16) for m in range(8) if not (e == 15 and m == 7)]
+    return np.array(sorted(set(vals)))
+
+
+E4M3_GRID = _e4m3_grid()
+
+
+def nvfp4_change_bound(v, delta):
+    """The oracle's NVFP4 cast of v [R, K] (``oracle.nvfp4``) and a bound on how far the cast
+    of any v' with |v' - v| <= delta (elementwise) can land from it.
+
+    The tensor's largest magnitude of v' lies in [max(|v| - delta), max(|v| + delta)], so
+    its tensor scale is any power of two between the ends' scales; each block's largest
+    magnitude lies in its own such interval, so for a given tensor scale its E4M3 block
+    scale is any grid value between the ends' casts. For every such pair the element cast
+    is monotone in v', so the ends of [v - delta, v + delta] give the largest distance."""
+    from oracle import nvfp4 as f4
+
+    v = np.asarray(v, F64)
+    R, K = v.shape
+    delta = np.broadcast_to(np.asarray(delta, F64), v.shape)
+    ref = f4.dequantized(v)
+    a = np.abs(v)
+    lo_t = float(np.max(np.maximum(a - delta, 0.0), initial=0.0))
+    hi_t = float(np.max(a + delta, initial=0.0))
+    st_lo, st_hi = f4.tensor_scale(np.array([[lo_t]])), f4.tensor_scale(np.array([[hi_t]]))
+    ts_cands = [st_lo]
+    while ts_cands[-1] < st_hi:
+        ts_cands.append(ts_cands[-1] * 2.0)
+    nb = K // 16
+    ab = a.reshape(R, nb, 16)
+    db = delta.reshape(R, nb, 16)
+    lo_b = np.max(np.maximum(ab - db, 0.0), axis=-1)
+    hi_b = np.max(ab + db, axis=-1)
+    ends = [(v - delta).reshape(R, nb, 16), (v + delta).reshape(R, nb, 16)]
+    ref_b = ref.reshape(R, nb, 16)
+    bound = np.zeros((R, nb, 16))
+    for st in ts_cands:
+        i_lo = np.searchsorted(E4M3_GRID, g8.round_to_e4m3(lo_b / (6.0 * st)))
+        i_hi = np.searchsorted(E4M3_GRID, g8.round_to_e4m3(hi_b / (6.0 * st)))
+        for k in range(int(np.max(i_hi - i_lo)) + 1):
+            sb = E4M3_GRID[np.minimum(i_lo + k, i_hi)][..., None]
+            den = sb * st
+            for s in ends:
+                q = np.where(den > 0, f4.round_to_e2m1(s / np.where(den > 0, den, 1.0)), 0.0) * den
+                bound = np.maximum(bound, np.abs(q - ref_b))
+    return ref, bound.reshape(R, K)

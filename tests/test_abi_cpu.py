@@ -21,7 +21,7 @@ def lib():
 
 def declared_functions():
     text = open(HEADER).read()
-    return sorted(set(re.findall(r"^(?:int|const char\*)\s+(krea_dit_\w+)\s*\(", text, flags=re.M)))
+    return sorted(set(re.findall(r"^(?:int|size_t|const char\*)\s+(krea_dit_\w+)\s*\(", text, flags=re.M)))
 
 
 def test_header_declares_the_boundary():
@@ -103,6 +103,18 @@ def test_every_handle_call_rejects_a_null_handle(lib):
                                                                      None, None),
         "krea_dit_block_forward8": lambda: L.krea_dit_block_forward8(None, None, None, 1, 1, 1, 1, None, None, None,
                                                                      None, None),
+        "krea_dit_weights4_quantize": lambda: L.krea_dit_weights4_quantize(None, None, None, None),
+        "krea_dit_block_forward4": lambda: L.krea_dit_block_forward4(None, None, None, 1, 1, 1, 1, None, None, None,
+                                                                     None, None),
     }
     for name, call in calls.items():
         assert call() == inv, name
+
+
+def test_nvfp4_scale_bytes(lib):
+    """ceil(rows / 128) * 128 rows of cols / 16 one-byte scales (host arithmetic only)."""
+    f = lib.krea_dit_nvfp4_scale_bytes
+    assert f(9216, 3072) == 9216 * 192
+    assert f(1, 64) == 128 * 4
+    assert f(130, 128) == 256 * 8
+    assert f(0, 64) == 0 and f(5, 0) == 0

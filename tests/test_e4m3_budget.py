@@ -5,7 +5,7 @@ change that leaves the budget."""
 import numpy as np
 import pytest
 
-from e4m3_budget import attention_spread, bf16_ulp, carry, cast_change_bound, norm_carry
+from e4m3_budget import attention_spread, bf16_ulp, carry, cast_change_bound, norm_carry, nvfp4_change_bound
 from oracle import gemm8 as g8
 from oracle.block import round_to_bf16
 
@@ -102,3 +102,23 @@ def test_attention_spread_brute_force_and_one_hot():
     q1 = np.full((1, 3, 4), 1.0)
     v1 = rng.normal(size=(1, 3, 4))
     np.testing.assert_allclose(attention_spread(q1, k1, v1), np.abs(np.broadcast_to(v1[0, 1], (3, 4))), rtol=1e-12)
+
+
+def test_nvfp4_bound_holds_for_every_sampled_perturbation():
+    from oracle import nvfp4 as f4
+    rng = np.random.default_rng(4)
+    v = round_to_bf16(rng.normal(size=(12, 64)) * np.exp(rng.normal(size=(12, 1))))
+    delta = 2 * bf16_ulp(v) + 1e-3
+    ref, bound = nvfp4_change_bound(v, delta)
+    np.testing.assert_array_equal(ref, f4.dequantized(v))
+    for trial in range(200):
+        t = rng.uniform(-1.0, 1.0, size=v.shape)
+        if trial % 4 == 0:
+            t = np.sign(t)
+        assert np.all(np.abs(f4.dequantized(v + t * delta) - ref) <= bound + 1e-15)
+    # nothing moves under a zero budget, and a change larger than the budget is caught
+    _, b0 = nvfp4_change_bound(v, 0.0)
+    assert np.all(b0 == 0.0)
+    w = v.copy()
+    w[3, 5] += 0.7 * np.abs(w[3, 5]) + 0.5
+    assert np.any(np.abs(f4.dequantized(w) - ref) > bound)
