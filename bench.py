@@ -111,13 +111,14 @@ def kernel_work(cfg):
 
 
 FP8_OVER_BF16 = 2.0  # nominal dense e4m3 / bf16 tensor throughput ratio (4.5 / 2.25 PFLOP/s)
+FP4_OVER_BF16 = 6.0  # nominal dense fp4 / bf16 tensor throughput ratio (13.5 / 2.25 PFLOP/s)
 
 
-def time_gemm8(args, cfg, case, dev, flush, bf16_ms):
-    """The block with 8-bit GEMMs (e4m3 operands) under both scalings, same workload and
-    timing protocol as the headline: per scaling, ms per step, tokens/s, the speed-up over
-    the bf16 block and per-kernel times (GEMM rates against the fp8 peak: the measured bf16
-    peak times the nominal ratio)."""
+def time_gemm8(args, cfg, case, dev, flush, bf16_ms, modes=(("tensor", "fp8_tensor"), ("row", "fp8_row"))):
+    """The block with quantised GEMMs (8-bit e4m3 operands under both scalings; NVFP4 with
+    modes=(("nvfp4", "nvfp4"),)), same workload and timing protocol as the headline: per
+    mode, ms per step, tokens/s, the speed-up over the bf16 block and per-kernel times
+    (GEMM rates against the mode's peak: the measured bf16 peak times the nominal ratio)."""
     import torch
 
     import diffusion_transformer_block_gb300 as kd
@@ -129,10 +130,11 @@ def time_gemm8(args, cfg, case, dev, flush, bf16_ms):
     x_img = case.dev["x_img"].to(dev).contiguous()
     x_txt = case.dev["x_txt"].to(dev).contiguous()
     res = {}
-    for scaling in ("tensor", "row"):
+    for scaling, mode in modes:
+        ratio = FP4_OVER_BF16 if mode == "nvfp4" else FP8_OVER_BF16
+        peak_key = "frac_of_fp4_peak" if mode == "nvfp4" else "frac_of_fp8_peak"
         blk = DitBlock(max_batch=cfg.B, max_seq=cfg.L, d=cfg.d, n_q=cfg.n_q, n_kv=cfg.n_kv, hd=cfg.hd, F=cfg.F,
-                       img_h_max=cfg.img_h, img_w_max=cfg.img_w, gate_on=cfg.gate_on, mode="fp8_" + scaling,
-                       device=str(dev))
+                       img_h_max=cfg.img_h, img_w_max=cfg.img_w, gate_on=cfg.gate_on, mode=mode, device=str(dev))
         blk.set_weights({k: case.dev[k] for k in ("w_qkvg", "w_o", "w_gate", "w_up", "w_down", "norm1_w",
                                                   "norm2_w", "q_norm_w", "k_norm_w", "mod_bias")})
         blk.set_temb_weights({k: case.dev["temb." + k] for k in ("w1", "b1", "w2", "b2")})
@@ -156,7 +158,7 @@ def time_gemm8(args, cfg, case, dev, flush, bf16_ms):
         ktimes = kd.krea_dit_block_kernel_times(blk.handle)
         st, site = kd.krea_dit_block_device_status(blk.handle)
         if st != kd.KREA_DIT_OK:
-            raise RuntimeError(f"8-bit device status: {kd.krea_dit_status_string(st)} (site {site})")
+            raise RuntimeError(f"{mode} device status: {kd.krea_dit_status_string(st)} (site {site})")
         step_ms = reduce_max(sum(a.elapsed_time(b) for a, b in evs), world) / steps
         kernels = {}
         for name, (tot, n) in ktimes.items():
@@ -164,16 +166,21 @@ def time_gemm8(args, cfg, case, dev, flush, bf16_ms):
             b, amount, _ = work.get(name, ("", 0.0, ""))
             if b == "tensor" and "gemm" in name:
                 k["tflops"] = amount / (k["avg_ms"] / 1000.0) / 1e12
-                k["frac_of_fp8_peak"] = k["tflops"] / (FP8_OVER_BF16 * peaks["bf16_tflops"])
+                k[peak_key] = k["tflops"] / (ratio * peaks["bf16_tflops"])
             kernels[name] = k
         res[scaling] = {"ms_per_step": step_ms, "tokens_per_s": world * cfg.T / (step_ms / 1000.0),
                         "speedup_vs_bf16": bf16_ms / step_ms, "kernels": kernels,
                         "gpu_launches_per_step": sum(v["launches"] for v in kernels.values()) / steps}
         kd.krea_dit_block_set_timing(blk.handle, False)
         blk.close()
-    res["how"] = ("krea_dit_block_forward8 on the headline workload, e4m3 weights cast once before timing; "
-                  "CUDA events per step, L2 flushed before each step outside the events; fp8 peak = measured "
-                  f"bf16 peak x {FP8_OVER_BF16} (nominal ratio)")
+    if any(m == "nvfp4" for _, m in modes):
+        res["how"] = ("krea_dit_block_forward4 on the headline workload, NVFP4 weights cast once before timing; "
+                      "CUDA events per step, L2 flushed before each step outside the events; fp4 peak = measured "
+                      f"bf16 peak x {FP4_OVER_BF16} (nominal ratio)")
+    else:
+        res["how"] = ("krea_dit_block_forward8 on the headline workload, e4m3 weights cast once before timing; "
+                      "CUDA events per step, L2 flushed before each step outside the events; fp8 peak = measured "
+                      f"bf16 peak x {FP8_OVER_BF16} (nominal ratio)")
     return res
 
 
@@ -533,6 +540,9 @@ def run_ours(args, cfg):
     gemm8 = None
     if not args.no_gemm8:
         gemm8 = time_gemm8(args, cfg, case, dev, flush, total_ms_max / args.steps)
+    nvfp4 = None
+    if not args.no_nvfp4:
+        nvfp4 = time_gemm8(args, cfg, case, dev, flush, total_ms_max / args.steps, modes=(("nvfp4", "nvfp4"),))
 
     # ---- numbers
     tokens_per_step = cfg.T
@@ -592,6 +602,7 @@ def run_ours(args, cfg):
                        "with device and copy streams synchronised on both sides"},
         "stack": stack,
         "gemm8": gemm8,
+        "nvfp4": nvfp4,
         "backward": backward,
         "clocks": clk,
         "gpu_launches": sum(pk["launches"] for pk in per_kernel.values()),
@@ -618,6 +629,7 @@ def main(argv=None):
     ap.add_argument("--ref-rows", type=int, default=1024, help="query rows per reference-arm step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-gemm8", action="store_true", help="skip the 8-bit GEMM measurement")
+    ap.add_argument("--no-nvfp4", action="store_true", help="skip the NVFP4 GEMM measurement")
     ap.add_argument("--no-backward", action="store_true", help="skip the block-backward measurement")
     ap.add_argument("--stack-blocks", type=int, default=8, help="blocks of the stack / CUDA-graph measurement (0: skip)")
     args = ap.parse_args(argv)

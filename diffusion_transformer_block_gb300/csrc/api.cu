@@ -52,7 +52,6 @@ enum Slot {
   S_BWD_POINTWISE,
   S_BWD_ATTN,
   S_Q4_AMAX,
-  S_Q4_SCALE,
   S_Q4_CAST,
   S_COUNT
 };
@@ -64,7 +63,7 @@ const char* const kSlotNames[S_COUNT] = {
     "temb_sinusoid",        "temb_mlp1",             "temb_mlp2",       "norm1_amax",
     "quant_og_e4m3",        "norm2_amax",            "quant_hmid_e4m3", "weights8_row_amax",
     "weights8_quant_e4m3",  "bwd_gemm",              "bwd_transpose",   "bwd_pointwise",
-    "bwd_attention",        "nvfp4_row_amax",        "nvfp4_tensor_scale", "nvfp4_cast"};
+    "bwd_attention",        "nvfp4_row_amax",        "nvfp4_cast"};
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
@@ -627,8 +626,7 @@ int forward_impl(krea_dit_block_t h, const void* x_img, const void* x_txt, const
     const kd::Deq dq_down{h->ts4 + 3, w4->ts_down, nullptr, 0};
     // NVFP4 cast of a bf16 activation [T, K] whose row amaxes are in am: tensor scale, codes
     const auto cast4 = [&](const void* src, int K, float* am, float* ts, void* codes, void* sf) {
-      KD_RUN(S_Q4_SCALE, kd::launch_nvfp4_scale(am, f.T, ts, st));
-      KD_RUN(S_Q4_CAST, kd::launch_nvfp4_cast(src, f.T, K, ts, codes, sf, sms, st));
+      KD_RUN(S_Q4_CAST, kd::launch_nvfp4_cast(src, f.T, K, am, ts, codes, sf, sms, st));
     };
     // row amax accumulators of the attention and SwiGLU outputs (atomic max from zero)
     e = cudaMemsetAsync(h->am_og, 0, T * sizeof(float), st);
@@ -821,10 +819,9 @@ int krea_dit_weights4_quantize(krea_dit_block_t h, const krea_dit_weights* w, co
   for (const Mat& m : mats) {
     if (e == cudaSuccess)
       e = timed(h, S_Q4_AMAX, st, [&] { return kd::launch_row_amax(m.src, m.rows, m.cols, h->am_w, h->num_sms, st); });
-    if (e == cudaSuccess) e = timed(h, S_Q4_SCALE, st, [&] { return kd::launch_nvfp4_scale(h->am_w, m.rows, m.ts, st); });
     if (e == cudaSuccess)
       e = timed(h, S_Q4_CAST, st, [&] {
-        return kd::launch_nvfp4_cast(m.src, m.rows, m.cols, m.ts, m.codes, m.sf, h->num_sms, st);
+        return kd::launch_nvfp4_cast(m.src, m.rows, m.cols, h->am_w, m.ts, m.codes, m.sf, h->num_sms, st);
       });
   }
   return e == cudaSuccess ? KREA_DIT_OK : KREA_DIT_ERR_CUDA;

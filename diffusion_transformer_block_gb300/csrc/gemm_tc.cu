@@ -780,11 +780,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 // One CTA per 128 x 256 output tile (no CTA pairs), persistent over the tiles. A stage
 // covers 256 elements of K (128 bytes of each operand row): A 128 x 128 B and the two
 // 128-row halves of B by TMA with the 128-byte swizzle, and the stage's scale atoms of A
-// and of both B halves by 1D bulk copies (54 KB). Per 64-element step the MMA thread
-// copies the step's three scale atoms into tensor memory (tcgen05.cp, ordered with its
-// MMAs) and issues two kind::mxf4nvf4 MMAs (M = 128, N = 128, K = 64), one per half of B,
-// into the two halves of the 256-column accumulator, which therefore has the layout the
-// bf16 kernel's epilogues read. The accumulator is single-buffered (the scale copies take
+// and of both B halves by 1D bulk copies (54 KB). Per stage the MMA thread copies the
+// stage's scale atoms into tensor memory (tcgen05.cp, ordered with its MMAs) and issues
+// one kind::mxf4nvf4 MMA (M = 128, N = 256, K = 64) per 64-element step into the
+// 256-column accumulator, which has the layout the bf16 kernel's epilogues read. The B
+// halves are two TMA boxes of 128 rows stacked in shared memory (so the SwiGLU GEMM's
+// W_gate and W_up rows form one 256-row operand) and their scale atoms two adjacent
+// 4-column groups in tensor memory. The accumulator is single-buffered (the scale copies take
 // tensor-memory columns 256 .. 303), so a tile's epilogue does not overlap the next
 // tile's main loop. Warp roles as in the bf16 kernel: 0 TMA, 1 TMEM + MMA, 2..9 epilogue.
 constexpr int F4_BM = 128, F4_BN = 256;
@@ -909,7 +911,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   } else if (warp == 1) {
     if (lane == 0) {
       // ---------------- scale copies + MMA issue
-      constexpr uint32_t idesc = idesc_nvf4_f32(F4_BM, F4_BN / 2);
+      constexpr uint32_t idesc = idesc_nvf4_f32(F4_BM, F4_BN);
       int stage = 0;
       uint32_t phase = 0;
       uint32_t acc_phase = 0;
@@ -927,16 +929,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const uint32_t sb = sa + F4_A_BYTES;
           const uint32_t ssf = sb + 2 * F4_BH_BYTES;
           const int nks = min(4, KS - 4 * kb);
-          for (int k = 0; k < nks; ++k) {  // 64 elements = 32 bytes of each row per step
+          // the stage's scale atoms first (TMEM columns: A, then the 256 B rows, per step),
+          // then one M = 128, N = 256 MMA per 64-element step: every tcgen05 instruction
+          // costs the single issuing thread about as much as an MMA takes to run
+          for (int k = 0; k < nks; ++k) {
             const uint32_t t_sf = tmem_base + F4_SF_TMEM + static_cast<uint32_t>(k * 12);
             tmem_cp_scales(t_sf, sdesc_rows16(ssf + k * F4_ATOM));
             tmem_cp_scales(t_sf + 4, sdesc_rows16(ssf + (4 + k) * F4_ATOM));
             tmem_cp_scales(t_sf + 8, sdesc_rows16(ssf + (8 + k) * F4_ATOM));
-            const uint32_t acc = (kb | k) != 0 ? 1u : 0u;
-            const uint64_t adesc = sdesc_kmajor_sw128(sa + k * 32);
-            mma_nvf4(tmem_base, adesc, sdesc_kmajor_sw128(sb + k * 32), idesc, t_sf, t_sf + 4, acc);
-            mma_nvf4(tmem_base + 128, adesc, sdesc_kmajor_sw128(sb + F4_BH_BYTES + k * 32), idesc, t_sf, t_sf + 8,
-                     acc);
+          }
+          for (int k = 0; k < nks; ++k) {  // 64 elements = 32 bytes of each row per step
+            const uint32_t t_sf = tmem_base + F4_SF_TMEM + static_cast<uint32_t>(k * 12);
+            // B row n (0 .. 255) takes its scales from column t_sf + 4 + n / 32: the two
+            // halves' atoms sit side by side
+            mma_nvf4(tmem_base, sdesc_kmajor_sw128(sa + k * 32), sdesc_kmajor_sw128(sb + k * 32), idesc, t_sf, t_sf + 4,
+                     (kb | k) != 0 ? 1u : 0u);
           }
           mma_commit(&empty[stage]);  // frees the stage once these MMAs have read it
           if (++stage == NST) {

@@ -199,11 +199,10 @@ struct Op4 {
 };
 // bytes of the scale atoms of a [rows, cols] operand (rows padded to 128)
 size_t nvfp4_scale_bytes(long long rows, long long cols);
-// ts[0] = power-of-two tensor scale from rowamax[0..R)
-cudaError_t launch_nvfp4_scale(const float* rowamax, int R, float* ts, cudaStream_t st);
-// codes / scale atoms of a bf16 [R, K] operand (K % 64 == 0) with the tensor scale ts[0]
-cudaError_t launch_nvfp4_cast(const void* src, int R, int K, const float* ts, void* codes, void* sf, int num_sms,
-                              cudaStream_t st);
+// codes / scale atoms of a bf16 [R, K] operand (K % 64 == 0); the tensor scale comes from
+// rowamax[0..R) (reduced by every CTA) and is stored to ts[0]
+cudaError_t launch_nvfp4_cast(const void* src, int R, int K, const float* rowamax, float* ts, void* codes, void* sf,
+                              int num_sms, cudaStream_t st);
 // sets the NVFP4 GEMM kernels' shared-memory limits (once per handle, before any capture)
 cudaError_t gemm_fp4_init();
 cudaError_t launch_gemm_qkvg_fp4(const Fwd& f, const Op4& a, const Op4& b, int N, const QkvgDst& dst, const Deq& dq,

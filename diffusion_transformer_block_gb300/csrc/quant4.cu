@@ -22,36 +22,40 @@ namespace {
 
 constexpr int Q4T = 256;  // threads per CTA of the cast
 
-// ts[0] = the tensor scale from the row amaxes (one CTA)
-__global__ void __launch_bounds__(1024) nvfp4_scale_kernel(const float* __restrict__ rowamax, int R,
-                                                           float* __restrict__ ts) {
-  __shared__ float red[32];
-  float m = 0.0f;
-  for (int i = threadIdx.x; i < R; i += blockDim.x) m = fmaxf(m, rowamax[i]);
-  m = warp_max(m);
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    float amax = 0.0f;
-    for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) amax = fmaxf(amax, red[w]);
-    float s = 1.0f;
-    if (amax > 0.0f) {
-      int e = 0;
-      const float m0 = frexpf(amax / 2688.0f, &e);  // amax / (448 * 6) = m0 2^e, 0.5 <= m0 < 1
-      s = pow2f(m0 == 0.5f ? e - 1 : e);
-    }
-    ts[0] = s;
-  }
+// the power-of-two tensor scale of a tensor with largest magnitude amax
+__device__ __forceinline__ float nvfp4_tensor_scale(float amax) {
+  if (!(amax > 0.0f)) return 1.0f;
+  int e = 0;
+  const float m0 = frexpf(amax / 2688.0f, &e);  // amax / (448 * 6) = m0 2^e, 0.5 <= m0 < 1
+  return pow2f(m0 == 0.5f ? e - 1 : e);
 }
 
-// One thread per 16-element block of the padded rows.
+// One thread per 16-element block of the padded rows. Every CTA first reduces the row
+// amaxes to the tensor scale itself (a few KB read from L2 per CTA); block 0 also stores it.
 __global__ void __launch_bounds__(Q4T) nvfp4_cast_kernel(const bf16* __restrict__ src, int R, int K,
-                                                         const float* __restrict__ ts_p, uint8_t* __restrict__ codes,
-                                                         uint8_t* __restrict__ sf) {
+                                                         const float* __restrict__ rowamax, float* __restrict__ ts_out,
+                                                         uint8_t* __restrict__ codes, uint8_t* __restrict__ sf) {
+  __shared__ float red[Q4T / 32];
+  __shared__ float ts_sh;
   const int KB = K / 16, KS = K / 64;
   const long long rows = (static_cast<long long>(R) + 127) / 128 * 128;
   const long long nblk = rows * KB;
-  const float ts = ts_p[0];
+  {
+    float m = 0.0f;
+#pragma unroll 8
+    for (int i = threadIdx.x; i < R; i += Q4T) m = fmaxf(m, rowamax[i]);
+    m = warp_max(m);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      float amax = 0.0f;
+      for (int w = 0; w < Q4T / 32; ++w) amax = fmaxf(amax, red[w]);
+      ts_sh = nvfp4_tensor_scale(amax);
+      if (blockIdx.x == 0) ts_out[0] = ts_sh;
+    }
+    __syncthreads();
+  }
+  const float ts = ts_sh;
   const float six_ts = 6.0f * ts;
   for (long long i = static_cast<long long>(blockIdx.x) * Q4T + threadIdx.x; i < nblk;
        i += static_cast<long long>(gridDim.x) * Q4T) {
@@ -96,22 +100,16 @@ size_t nvfp4_scale_bytes(long long rows, long long cols) {
   return static_cast<size_t>((rows + 127) / 128 * 128) * static_cast<size_t>(cols / 16);
 }
 
-cudaError_t launch_nvfp4_scale(const float* rowamax, int R, float* ts, cudaStream_t st) {
-  if (R <= 0) return cudaSuccess;
-  nvfp4_scale_kernel<<<1, 1024, 0, st>>>(rowamax, R, ts);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_nvfp4_cast(const void* src, int R, int K, const float* ts, void* codes, void* sf, int num_sms,
-                              cudaStream_t st) {
+cudaError_t launch_nvfp4_cast(const void* src, int R, int K, const float* rowamax, float* ts, void* codes, void* sf,
+                              int num_sms, cudaStream_t st) {
   if (R <= 0 || K <= 0) return cudaSuccess;
   if (K % 64) return cudaErrorInvalidValue;
   const long long nblk = (static_cast<long long>(R) + 127) / 128 * 128 * (K / 16);
   long long grid = (nblk + Q4T - 1) / Q4T;
   const long long cap = 8LL * num_sms;
   if (grid > cap) grid = cap;
-  nvfp4_cast_kernel<<<static_cast<unsigned>(grid), Q4T, 0, st>>>(reinterpret_cast<const bf16*>(src), R, K, ts,
-                                                                  reinterpret_cast<uint8_t*>(codes),
+  nvfp4_cast_kernel<<<static_cast<unsigned>(grid), Q4T, 0, st>>>(reinterpret_cast<const bf16*>(src), R, K, rowamax,
+                                                                  ts, reinterpret_cast<uint8_t*>(codes),
                                                                   reinterpret_cast<uint8_t*>(sf));
   return cudaGetLastError();
 }

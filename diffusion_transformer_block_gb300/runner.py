@@ -175,10 +175,10 @@ class DitBlock:
         (H1 and the DQ_* factors are fp32, the *8 e4m3 codes are returned as uint8, every
         other buffer is in the storage dtype)."""
         ptr, nbytes = krea_dit_block_workspace(self.handle, name)
-        if name.endswith(("8", "4")) or name.startswith("SF_"):
-            esz = 1
-        elif name.startswith("TS_"):
+        if name.startswith("TS_"):
             esz = 4
+        elif name.endswith(("8", "4")) or name.startswith("SF_"):
+            esz = 1
         elif name == "H1" or name.startswith("DQ_") or self.mode == "fp32":
             esz = 4
         else:
