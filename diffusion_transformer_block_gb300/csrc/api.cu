@@ -631,9 +631,11 @@ int forward_impl(krea_dit_block_t h, const void* x_img, const void* x_txt, const
     // row amax accumulators of the attention and SwiGLU outputs (atomic max from zero)
     e = cudaMemsetAsync(h->am_og, 0, T * sizeof(float), st);
     if (e == cudaSuccess) e = cudaMemsetAsync(h->am_hmid, 0, T * sizeof(float), st);
+    // the norms store bf16 and each row's amax; the casts reduce those to the tensor scale
+    const kd::NormQOut nq_xn{kd::NormQ::STORE_AMAX, nullptr, nullptr, h->am_xn};
+    const kd::NormQOut nq_hn{kd::NormQ::STORE_AMAX, nullptr, nullptr, h->am_hn};
     KD_RUN(S_NORM1, kd::launch_norm_modulate(kd::NormIO::BF16_BF16, f, xsrc, w->norm1_w, t_emb, w->mod_bias, 0, 1,
-                                             h->xn, sms, st));
-    KD_RUN(S_Q4_AMAX, kd::launch_row_amax(h->xn, f.T, c.d_model, h->am_xn, sms, st));
+                                             h->xn, sms, st, &nq_xn));
     cast4(h->xn, c.d_model, h->am_xn, h->ts4 + 0, h->xn4, h->sf_xn4);
     KD_RUN(S_QKVG_TC, kd::launch_gemm_qkvg_fp4(f, a_xn, b_qkvg, h->n_qkvg, dst, dq_qkvg, sms, h->err, st));
     KD_RUN(S_ATTN, kd::launch_attn_tc(f, &tm_q, &tm_k, &tm_vt, &tm_g, &tm_og, h->am_og, nullptr, nullptr, sms, h->err,
@@ -642,8 +644,7 @@ int forward_impl(krea_dit_block_t h, const void* x_img, const void* x_txt, const
     KD_RUN(S_OPROJ_TC, kd::launch_gemm_resid_attn_fp4(f, a_og, b_o, nqhd, xsrc, t_emb, w->mod_bias, &tm_h1, dq_o, sms,
                                                       h->err, st));
     KD_RUN(S_NORM2, kd::launch_norm_modulate(kd::NormIO::F32_BF16, f, h1src, w->norm2_w, t_emb, w->mod_bias, 3, 4,
-                                             h->hn, sms, st));
-    KD_RUN(S_Q4_AMAX, kd::launch_row_amax(h->hn, f.T, c.d_model, h->am_hn, sms, st));
+                                             h->hn, sms, st, &nq_hn));
     cast4(h->hn, c.d_model, h->am_hn, h->ts4 + 2, h->hn4, h->sf_hn4);
     KD_RUN(S_UPGATE_TC, kd::launch_gemm_swiglu_fp4(f, a_hn, b_gate, b_up, h->hmid, h->am_hmid, dq_ff, sms, h->err,
                                                    st));

@@ -909,55 +909,72 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         drain_wait(&full[i % NST], static_cast<uint32_t>((i / NST) & 1), err, SITE_GEMM_TEARDOWN);
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      // ---------------- scale copies + MMA issue
-      constexpr uint32_t idesc = idesc_nvf4_f32(F4_BM, F4_BN);
-      int stage = 0;
-      uint32_t phase = 0;
-      uint32_t acc_phase = 0;
-      bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
-        if (!mbar_wait(tempty, acc_phase ^ 1, wc, SITE_GEMM_MMA)) break;
+    // ---------------- scale copies + MMA issue. The whole warp runs the loop (waits,
+    // addresses and descriptors computed warp-uniformly); lane 0 issues every tcgen05
+    // instruction and commit.
+    constexpr uint32_t idesc = idesc_nvf4_f32(F4_BM, F4_BN);
+    int stage = 0;
+    uint32_t phase = 0;
+    uint32_t acc_phase = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+      if (!__all_sync(0xffffffffu, mbar_wait(tempty, acc_phase ^ 1, wc, SITE_GEMM_MMA))) break;
+      tc_fence_after();
+      for (int kb = 0; kb < num_kb; ++kb) {
+        if (!__all_sync(0xffffffffu, mbar_wait(&full[stage], phase, wc, SITE_GEMM_MMA))) {
+          ok = false;
+          break;
+        }
         tc_fence_after();
-        for (int kb = 0; kb < num_kb; ++kb) {
-          if (!mbar_wait(&full[stage], phase, wc, SITE_GEMM_MMA)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t sa = smem_u32(smem + stage * F4_STAGE);
-          const uint32_t sb = sa + F4_A_BYTES;
-          const uint32_t ssf = sb + 2 * F4_BH_BYTES;
-          const int nks = min(4, KS - 4 * kb);
-          // the stage's scale atoms first (TMEM columns: A, then the 256 B rows, per step),
-          // then one M = 128, N = 256 MMA per 64-element step: every tcgen05 instruction
-          // costs the single issuing thread about as much as an MMA takes to run
-          for (int k = 0; k < nks; ++k) {
-            const uint32_t t_sf = tmem_base + F4_SF_TMEM + static_cast<uint32_t>(k * 12);
-            tmem_cp_scales(t_sf, sdesc_rows16(ssf + k * F4_ATOM));
-            tmem_cp_scales(t_sf + 4, sdesc_rows16(ssf + (4 + k) * F4_ATOM));
-            tmem_cp_scales(t_sf + 8, sdesc_rows16(ssf + (8 + k) * F4_ATOM));
-          }
-          for (int k = 0; k < nks; ++k) {  // 64 elements = 32 bytes of each row per step
-            const uint32_t t_sf = tmem_base + F4_SF_TMEM + static_cast<uint32_t>(k * 12);
-            // B row n (0 .. 255) takes its scales from column t_sf + 4 + n / 32: the two
-            // halves' atoms sit side by side
-            mma_nvf4(tmem_base, sdesc_kmajor_sw128(sa + k * 32), sdesc_kmajor_sw128(sb + k * 32), idesc, t_sf, t_sf + 4,
-                     (kb | k) != 0 ? 1u : 0u);
+        const uint32_t sa = smem_u32(smem + stage * F4_STAGE);
+        const uint32_t sb = sa + F4_A_BYTES;
+        const uint32_t ssf = sb + 2 * F4_BH_BYTES;
+        const uint32_t t_sf0 = tmem_base + F4_SF_TMEM;
+        const uint32_t acc = (kb != 0) ? 1u : 0u;
+        // the stage's scale atoms first (TMEM columns: A, then the 256 B rows, per step),
+        // then one M = 128, N = 256 MMA per 64-element step; B row n (0 .. 255) takes its
+        // scales from column t_sf + 4 + n / 32: the two halves' atoms sit side by side
+        if (lane == 0) {
+          if (4 * kb + 4 <= KS) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              tmem_cp_scales(t_sf0 + k * 12, sdesc_rows16(ssf + k * F4_ATOM));
+              tmem_cp_scales(t_sf0 + k * 12 + 4, sdesc_rows16(ssf + (4 + k) * F4_ATOM));
+              tmem_cp_scales(t_sf0 + k * 12 + 8, sdesc_rows16(ssf + (8 + k) * F4_ATOM));
+            }
+#pragma unroll
+            for (int k = 0; k < 4; ++k)  // 64 elements = 32 bytes of each row per step
+              mma_nvf4(tmem_base, sdesc_kmajor_sw128(sa + k * 32), sdesc_kmajor_sw128(sb + k * 32), idesc,
+                       t_sf0 + k * 12, t_sf0 + k * 12 + 4, (acc | k) != 0 ? 1u : 0u);
+          } else {  // a last stage of fewer than four steps
+            const int nks = KS - 4 * kb;
+            for (int k = 0; k < nks; ++k) {
+              tmem_cp_scales(t_sf0 + k * 12, sdesc_rows16(ssf + k * F4_ATOM));
+              tmem_cp_scales(t_sf0 + k * 12 + 4, sdesc_rows16(ssf + (4 + k) * F4_ATOM));
+              tmem_cp_scales(t_sf0 + k * 12 + 8, sdesc_rows16(ssf + (8 + k) * F4_ATOM));
+            }
+            for (int k = 0; k < nks; ++k)
+              mma_nvf4(tmem_base, sdesc_kmajor_sw128(sa + k * 32), sdesc_kmajor_sw128(sb + k * 32), idesc,
+                       t_sf0 + k * 12, t_sf0 + k * 12 + 4, (acc | k) != 0 ? 1u : 0u);
           }
           mma_commit(&empty[stage]);  // frees the stage once these MMAs have read it
-          if (++stage == NST) {
-            stage = 0;
-            phase ^= 1;
-          }
         }
-        if (!ok) break;
-        mma_commit(tfull);  // accumulator ready for the epilogue
-        acc_phase ^= 1;
+        __syncwarp();
+        if (++stage == NST) {
+          stage = 0;
+          phase ^= 1;
+        }
       }
+      if (!ok) break;
+      if (lane == 0) mma_commit(tfull);  // accumulator ready for the epilogue
+      __syncwarp();
+      acc_phase ^= 1;
+    }
+    if (lane == 0) {
       mma_commit(done);  // completes when every MMA and copy issued above has finished
       drain_wait(done, 0, err, SITE_GEMM_TEARDOWN);
     }
+    __syncwarp();
   } else {
     // ---------------- epilogue warps
     const int quad = warp & 3;        // TMEM lanes this warp may access: 32*quad ..

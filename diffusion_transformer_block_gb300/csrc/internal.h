@@ -65,7 +65,7 @@ enum class NormIO { BF16_BF16, F32_BF16, F32_F32 };
 //   ROW    : row-wise scaled codes -> q8 [T, d], dq [T]
 //   AMAX   : no output; rowamax[m] = largest |bf16 row value|
 //   TENSOR : codes with one scale from max(rowamax[0..T)) -> q8, dq [1]
-enum class NormQ { NONE, ROW, AMAX, TENSOR };
+enum class NormQ { NONE, ROW, AMAX, TENSOR, STORE_AMAX };
 struct NormQOut {
   NormQ mode;
   void* q8;

@@ -63,7 +63,8 @@ struct Raw8<float> {
 
 // QM = output mode (NormQ): 0 plain store of Tout; 1 e4m3 codes with one power-of-two
 // scale per row; 2 row amax only; 3 e4m3 codes with one scale for the whole tensor, from
-// the row amax of a preceding mode-2 pass. The e4m3 modes cast the row as a bf16 store
+// the row amax of a preceding mode-2 pass; 4 plain store plus the row's amax (of the
+// stored bf16 values), for a cast that follows. The e4m3 modes cast the row as a bf16 store
 // would keep it ("训练 › 预训练" / Training › Pretraining: 8-bit GEMM operands).
 template <class Tin, class Tout, int NV, int QM>
 __global__ void __launch_bounds__(NM_WARPS * 32, 1) norm_modulate_kernel(
@@ -188,8 +189,9 @@ __global__ void __launch_bounds__(NM_WARPS * 32, 1) norm_modulate_kernel(
 #pragma unroll
       for (int i = 0; i < 8; ++i) o[i] = fmaf(v[i] * rstd, av[i], sv[i]);
     };
-    if constexpr (QM == 0) {
+    if constexpr (QM == 0 || QM == 4) {
       Tout* y = out + static_cast<size_t>(m) * d;
+      float amax = 0.0f;
 #pragma unroll
       for (int c = 0; c < NV; ++c) {
         const int col = (lane + 32 * c) * 8;
@@ -197,7 +199,15 @@ __global__ void __launch_bounds__(NM_WARPS * 32, 1) norm_modulate_kernel(
           float o[8];
           chunk_out(c, col, o);
           store8<Tout>(y + col, o);
+          if constexpr (QM == 4) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(o[i]));
+          }
         }
+      }
+      if constexpr (QM == 4) {
+        amax = round_bf16(warp_max(amax));  // the largest magnitude of the stored row
+        if (lane == 0) rowamax[m] = amax;
       }
     } else {
       float scale;
@@ -270,7 +280,8 @@ cudaError_t init_nm_modes(int d) {
     if (e != cudaSuccess) return e;
     if ((e = init_nm<Tin, Tout, NV, 1>(d)) != cudaSuccess) return e;
     if ((e = init_nm<Tin, Tout, NV, 2>(d)) != cudaSuccess) return e;
-    return init_nm<Tin, Tout, NV, 3>(d);
+    if ((e = init_nm<Tin, Tout, NV, 3>(d)) != cudaSuccess) return e;
+    return init_nm<Tin, Tout, NV, 4>(d);
   }
   return e;
 }
@@ -317,6 +328,9 @@ cudaError_t launch_nm_mode(const Fwd& f, RowSrc src, const float* gain_w, const 
                                            num_sms, st);
       case NormQ::TENSOR:
         return launch_nm<Tin, Tout, NV, 3>(f, src, gain_w, mod_shared, mod_bias, chunk_shift, chunk_scale, out, q,
+                                           num_sms, st);
+      case NormQ::STORE_AMAX:
+        return launch_nm<Tin, Tout, NV, 4>(f, src, gain_w, mod_shared, mod_bias, chunk_shift, chunk_scale, out, q,
                                            num_sms, st);
     }
   } else {

@@ -30,22 +30,55 @@ __device__ __forceinline__ float nvfp4_tensor_scale(float amax) {
   return pow2f(m0 == 0.5f ? e - 1 : e);
 }
 
-// One thread per 16-element block of the padded rows. Every CTA first reduces the row
-// amaxes to the tensor scale itself (a few KB read from L2 per CTA); block 0 also stores it.
-__global__ void __launch_bounds__(Q4T) nvfp4_cast_kernel(const bf16* __restrict__ src, int R, int K,
-                                                         const float* __restrict__ rowamax, float* __restrict__ ts_out,
-                                                         uint8_t* __restrict__ codes, uint8_t* __restrict__ sf) {
+// One 16-element block (two 16-byte units u0, u1 of bf16) of a row: returns its scale
+// byte and writes its eight code bytes to lo, hi.
+__device__ __forceinline__ uint32_t nvfp4_block(const uint4& u0, const uint4& u1, float six_ts, float ts,
+                                                uint32_t& lo, uint32_t& hi) {
+  const uint32_t w[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+  float v[16];
+  float amax = 0.0f;
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    const float2 f = unpack_bf16x2(w[q]);
+    v[2 * q] = f.x;
+    v[2 * q + 1] = f.y;
+    amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
+  }
+  const uint32_t sbyte = cvt_e4m3x2(amax / six_ts, 0.0f) & 0xFFu;  // block scale code
+  __nv_fp8_e4m3 sb8;
+  sb8.__x = static_cast<__nv_fp8_storage_t>(sbyte);
+  const float den = static_cast<float>(sb8) * ts;  // exact: an E4M3 value times a power of two
+  lo = 0;
+  hi = 0;
+  if (den > 0.0f) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      lo |= cvt_e2m1x2(v[2 * q] / den, v[2 * q + 1] / den) << (8 * q);
+      hi |= cvt_e2m1x2(v[8 + 2 * q] / den, v[8 + 2 * q + 1] / den) << (8 * q);
+    }
+  }
+  return sbyte;
+}
+
+// Persistent, one thread per (row, 64-element step): it reads the step's 128 bytes of the
+// row, writes their 32 code bytes with two 16-byte stores and the row's four scale bytes
+// of the step with one 4-byte store. Items run through the scale atoms in order, 128 rows
+// of one atom after another, so a warp covers 32 rows of one atom and its scale stores
+// fall into one 512-byte atom. Every CTA first reduces the row amaxes to the tensor scale
+// (block 0 also stores it).
+__global__ void __launch_bounds__(Q4T, 3) nvfp4_cast_kernel(const bf16* __restrict__ src, int R, int K,
+                                                            const float* __restrict__ rowamax,
+                                                            float* __restrict__ ts_out, uint8_t* __restrict__ codes,
+                                                            uint8_t* __restrict__ sf) {
   __shared__ float red[Q4T / 32];
   __shared__ float ts_sh;
-  const int KB = K / 16, KS = K / 64;
-  const long long rows = (static_cast<long long>(R) + 127) / 128 * 128;
-  const long long nblk = rows * KB;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   {
     float m = 0.0f;
 #pragma unroll 8
     for (int i = threadIdx.x; i < R; i += Q4T) m = fmaxf(m, rowamax[i]);
     m = warp_max(m);
-    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+    if (lane == 0) red[warp] = m;
     __syncthreads();
     if (threadIdx.x == 0) {
       float amax = 0.0f;
@@ -57,39 +90,26 @@ __global__ void __launch_bounds__(Q4T) nvfp4_cast_kernel(const bf16* __restrict_
   }
   const float ts = ts_sh;
   const float six_ts = 6.0f * ts;
-  for (long long i = static_cast<long long>(blockIdx.x) * Q4T + threadIdx.x; i < nblk;
-       i += static_cast<long long>(gridDim.x) * Q4T) {
-    const int r = static_cast<int>(i / KB), kb = static_cast<int>(i - static_cast<long long>(r) * KB);
-    uint32_t sbyte = 0;
+  const int KS = K / 64;
+  const int items = (R + 127) / 128 * 128 * KS;  // the launcher checks that this fits an int
+  for (int i = blockIdx.x * Q4T + threadIdx.x; i < items; i += gridDim.x * Q4T) {
+    const int a = i >> 7, rr = i & 127;  // scale atom, row inside its 128-row block
+    const int rb = a / KS, ks = a - rb * KS;
+    const int r = rb * 128 + rr;
+    uint32_t bytes = 0;
     if (r < R) {
-      const uint4* p = reinterpret_cast<const uint4*>(src + static_cast<size_t>(r) * K + kb * 16);
-      const uint4 u0 = p[0], u1 = p[1];
-      const uint32_t w[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
-      float v[16];
-      float amax = 0.0f;
+      const uint4* p = reinterpret_cast<const uint4*>(src + static_cast<size_t>(r) * K + ks * 64);
+      uint4 u[8];
 #pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        const float2 f = unpack_bf16x2(w[q]);
-        v[2 * q] = f.x;
-        v[2 * q + 1] = f.y;
-        amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
-      }
-      sbyte = cvt_e4m3x2(amax / six_ts, 0.0f) & 0xFFu;  // block scale code
-      __nv_fp8_e4m3 sb8;
-      sb8.__x = static_cast<__nv_fp8_storage_t>(sbyte);
-      const float den = static_cast<float>(sb8) * ts;  // exact: an E4M3 value times a power of two
-      uint32_t lo = 0, hi = 0;
-      if (den > 0.0f) {
+      for (int t = 0; t < 8; ++t) u[t] = p[t];
+      uint32_t c[8];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          lo |= cvt_e2m1x2(v[2 * q] / den, v[2 * q + 1] / den) << (8 * q);
-          hi |= cvt_e2m1x2(v[8 + 2 * q] / den, v[8 + 2 * q + 1] / den) << (8 * q);
-        }
-      }
-      *reinterpret_cast<uint2*>(codes + static_cast<size_t>(r) * (K / 2) + kb * 8) = make_uint2(lo, hi);
+      for (int j = 0; j < 4; ++j) bytes |= nvfp4_block(u[2 * j], u[2 * j + 1], six_ts, ts, c[2 * j], c[2 * j + 1]) << (8 * j);
+      uint4* o = reinterpret_cast<uint4*>(codes + static_cast<size_t>(r) * (K / 2) + ks * 32);
+      o[0] = make_uint4(c[0], c[1], c[2], c[3]);
+      o[1] = make_uint4(c[4], c[5], c[6], c[7]);
     }
-    const int rb = r / 128, rr = r % 128, ks = kb / 4, j = kb % 4;
-    sf[(static_cast<size_t>(rb) * KS + ks) * 512 + (rr % 32) * 16 + (rr / 32) * 4 + j] = static_cast<uint8_t>(sbyte);
+    *reinterpret_cast<uint32_t*>(sf + static_cast<size_t>(a) * 512 + (rr & 31) * 16 + (rr >> 5) * 4) = bytes;
   }
 }
 
@@ -104,9 +124,10 @@ cudaError_t launch_nvfp4_cast(const void* src, int R, int K, const float* rowama
                               int num_sms, cudaStream_t st) {
   if (R <= 0 || K <= 0) return cudaSuccess;
   if (K % 64) return cudaErrorInvalidValue;
-  const long long nblk = (static_cast<long long>(R) + 127) / 128 * 128 * (K / 16);
-  long long grid = (nblk + Q4T - 1) / Q4T;
-  const long long cap = 8LL * num_sms;
+  const long long items = (static_cast<long long>(R) + 127) / 128 * 128 * (K / 64);
+  if (items > (1LL << 30)) return cudaErrorInvalidValue;
+  long long grid = (items + Q4T - 1) / Q4T;
+  const long long cap = 3LL * num_sms;  // resident CTAs, each paying the amax reduction once
   if (grid > cap) grid = cap;
   nvfp4_cast_kernel<<<static_cast<unsigned>(grid), Q4T, 0, st>>>(reinterpret_cast<const bf16*>(src), R, K, rowamax,
                                                                   ts, reinterpret_cast<uint8_t*>(codes),

@@ -114,7 +114,7 @@ def _e4m3_grid() -> np.ndarray:
 E4M3_GRID = _e4m3_grid()
 
 
-def nvfp4_change_bound(v, delta):
+def nvfp4_change_bound(v, delta, max_exact=2):
     """The oracle's NVFP4 cast of v [R, K] (``oracle.nvfp4``) and a bound on how far the cast
     of any v' with |v' - v| <= delta (elementwise) can land from it.
 
@@ -122,7 +122,14 @@ def nvfp4_change_bound(v, delta):
     its tensor scale is any power of two between the ends' scales; each block's largest
     magnitude lies in its own such interval, so for a given tensor scale its E4M3 block
     scale is any grid value between the ends' casts. For every such pair the element cast
-    is monotone in v', so the ends of [v - delta, v + delta] give the largest distance."""
+    is monotone in v', so the ends of [v - delta, v + delta] give the largest distance.
+
+    A block whose admissible block scales span more than ``max_exact`` + 1 grid values gets
+    a closed-form bound instead of the enumeration (which would cost one pass over the
+    whole tensor per grid value): for a scale product den in [den_lo, den_hi] the cast of s
+    lies within den_hi of s while |s| <= 6 den (half the widest E2M1 spacing, 2, times den),
+    within |s| - 6 den_lo of it beyond, and is 0 where den can be 0; s itself lies within
+    |v - ref| + delta of the oracle's cast."""
     from oracle import nvfp4 as f4
 
     v = np.asarray(v, F64)
@@ -144,13 +151,31 @@ def nvfp4_change_bound(v, delta):
     ends = [(v - delta).reshape(R, nb, 16), (v + delta).reshape(R, nb, 16)]
     ref_b = ref.reshape(R, nb, 16)
     bound = np.zeros((R, nb, 16))
+    wide = np.zeros((R, nb), dtype=bool)
+    den_lo = np.full((R, nb), np.inf)
+    den_hi = np.zeros((R, nb))
     for st in ts_cands:
         i_lo = np.searchsorted(E4M3_GRID, g8.round_to_e4m3(lo_b / (6.0 * st)))
         i_hi = np.searchsorted(E4M3_GRID, g8.round_to_e4m3(hi_b / (6.0 * st)))
-        for k in range(int(np.max(i_hi - i_lo)) + 1):
-            sb = E4M3_GRID[np.minimum(i_lo + k, i_hi)][..., None]
+        wide |= (i_hi - i_lo) > max_exact
+        den_lo = np.minimum(den_lo, E4M3_GRID[i_lo] * st)
+        den_hi = np.maximum(den_hi, E4M3_GRID[i_hi] * st)
+        n_c = i_hi - i_lo
+        for k in range(min(int(np.max(n_c)), max_exact) + 1):
+            sel = None if k == 0 else n_c >= k  # grid value k above the lowest, where admissible
+            sb = E4M3_GRID[i_lo + k if sel is None else i_lo[sel] + k][..., None]
             den = sb * st
             for s in ends:
-                q = np.where(den > 0, f4.round_to_e2m1(s / np.where(den > 0, den, 1.0)), 0.0) * den
-                bound = np.maximum(bound, np.abs(q - ref_b))
+                s_k = s if sel is None else s[sel]
+                q = np.where(den > 0, f4.round_to_e2m1(s_k / np.where(den > 0, den, 1.0)), 0.0) * den
+                if sel is None:
+                    bound = np.maximum(bound, np.abs(q - ref_b))
+                else:
+                    bound[sel] = np.maximum(bound[sel], np.abs(q - ref_b[sel]))
+    if np.any(wide):
+        sabs = ab[wide] + db[wide]  # largest |s| per element of the wide blocks
+        dl, dh = den_lo[wide][:, None], den_hi[wide][:, None]
+        cast_err = np.maximum(dh, sabs - 6.0 * dl)
+        cast_err = np.where(dl > 0, cast_err, np.maximum(cast_err, sabs))
+        bound[wide] = cast_err + np.abs(v.reshape(R, nb, 16)[wide] - ref_b[wide]) + db[wide]
     return ref, bound.reshape(R, K)

@@ -122,3 +122,23 @@ def test_nvfp4_bound_holds_for_every_sampled_perturbation():
     w = v.copy()
     w[3, 5] += 0.7 * np.abs(w[3, 5]) + 0.5
     assert np.any(np.abs(f4.dequantized(w) - ref) > bound)
+
+
+def test_nvfp4_bound_with_wide_scale_ranges():
+    """Budgets comparable to the values give blocks whose block scale can take many grid
+    values; there the closed-form part of the bound takes over from the enumeration. It must
+    still hold for every sampled perturbation and never undercut the full enumeration."""
+    from oracle import nvfp4 as f4
+    rng = np.random.default_rng(5)
+    for scale in (0.3, 1.0, 3.0):
+        v = round_to_bf16(rng.normal(size=(16, 128)) * np.exp(rng.normal(size=(16, 1))))
+        delta = 2 * bf16_ulp(v) + scale * np.abs(rng.normal(size=v.shape)) * np.abs(v).mean()
+        ref, bound = nvfp4_change_bound(v, delta)
+        _, exact = nvfp4_change_bound(v, delta, max_exact=10 ** 6)
+        assert np.all(bound >= exact - 1e-12)
+        assert np.any(bound > exact + 1e-12)  # the closed form did take over somewhere
+        for trial in range(200):
+            t = rng.uniform(-1.0, 1.0, size=v.shape)
+            if trial % 3 == 0:
+                t = np.sign(t)
+            assert np.all(np.abs(f4.dequantized(v + t * delta) - ref) <= bound + 1e-12)
