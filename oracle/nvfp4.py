@@ -40,27 +40,42 @@ E4M3_MAX = 448.0
 BLOCK = 16
 
 
-def round_to_e2m1(v) -> np.ndarray:
-    """Nearest E2M1 value of each float64 input; a tie goes to the neighbour whose
-    mantissa bit is 0 (codes 0, 2, 4, 6: 0, 1, 2, 4); magnitudes above 6 saturate to 6.
-    In [0, 2) the spacing is 0.5, in [2, 4) it is 1, in [4, 6] it is 2."""
-    v = np.asarray(v, F64)
+_CHUNK = 1 << 20  # elements per numpy pass over a large tensor (keeps temporaries in cache)
+
+
+def _round_to_e2m1_flat(v: np.ndarray) -> np.ndarray:
     a = np.minimum(np.abs(v), E2M1_MAX)
     step = np.where(a < 2.0, 0.5, np.where(a < 4.0, 1.0, 2.0))
     lo = np.floor(a / step) * step  # the grid value at or below a
     hi = lo + step
     d_lo, d_hi = a - lo, hi - a
     # a tie keeps the neighbour whose mantissa bit is 0: 0, 1, 2 and 4
-    lo_even = np.isin(lo, (0.0, 1.0, 2.0, 4.0))
+    lo_even = (lo == 0.0) | (lo == 1.0) | (lo == 2.0) | (lo == 4.0)
     pick_hi = (d_hi < d_lo) | ((d_hi == d_lo) & ~lo_even)
     r = np.where(pick_hi, np.minimum(hi, E2M1_MAX), lo)
     return np.copysign(r, v)
 
 
+def round_to_e2m1(v) -> np.ndarray:
+    """Nearest E2M1 value of each float64 input; a tie goes to the neighbour whose
+    mantissa bit is 0 (codes 0, 2, 4, 6: 0, 1, 2, 4); magnitudes above 6 saturate to 6.
+    In [0, 2) the spacing is 0.5, in [2, 4) it is 1, in [4, 6] it is 2. Elementwise (large
+    inputs go through in slices of _CHUNK elements)."""
+    v = np.asarray(v, F64)
+    if v.size <= _CHUNK:
+        return _round_to_e2m1_flat(v)
+    flat = v.reshape(-1)
+    out = np.empty_like(flat)
+    for i in range(0, flat.size, _CHUNK):
+        out[i:i + _CHUNK] = _round_to_e2m1_flat(flat[i:i + _CHUNK])
+    return out.reshape(v.shape)
+
+
 def tensor_scale(x) -> float:
     """s_t = 2^j, j the smallest integer with amax <= 2688 * 2^j; 1 for an all-zero
     tensor. With amax / 2688 = m 2^e (0.5 <= m < 1): j = e - 1 when m = 0.5, else e."""
-    amax = float(np.max(np.abs(np.asarray(x, F64)), initial=0.0))
+    x = np.asarray(x, F64)
+    amax = max(float(np.max(x, initial=0.0)), -float(np.min(x, initial=0.0)))
     if amax <= 0:
         return 1.0
     m, e = np.frexp(amax / (E4M3_MAX * E2M1_MAX))
@@ -76,12 +91,18 @@ def quantize(x, s_t: Optional[float] = None):
     if K % BLOCK:
         raise ValueError("K must be a multiple of 16")
     st = tensor_scale(x) if s_t is None else float(s_t)
-    blocks = x.reshape(R, K // BLOCK, BLOCK)
-    amax_b = np.max(np.abs(blocks), axis=-1)
-    s_b = round_to_e4m3(amax_b / (E2M1_MAX * st))
-    denom = s_b[..., None] * st
-    q = np.where(denom > 0, round_to_e2m1(blocks / np.where(denom > 0, denom, 1.0)), 0.0)
-    return q.reshape(R, K), s_b, st
+    q = np.empty((R, K))
+    s_b = np.empty((R, K // BLOCK))
+    rows = max(1, _CHUNK // max(K, 1))
+    for r0 in range(0, R, rows):  # rows are independent once s_t is fixed
+        blocks = x[r0:r0 + rows].reshape(-1, K // BLOCK, BLOCK)
+        amax_b = np.max(np.abs(blocks), axis=-1)
+        sb = round_to_e4m3(amax_b / (E2M1_MAX * st))
+        denom = sb[..., None] * st
+        q[r0:r0 + rows] = np.where(denom > 0, round_to_e2m1(blocks / np.where(denom > 0, denom, 1.0)),
+                                   0.0).reshape(-1, K)
+        s_b[r0:r0 + rows] = sb
+    return q, s_b, st
 
 
 def dequantized(x) -> np.ndarray:

@@ -136,46 +136,54 @@ def nvfp4_change_bound(v, delta, max_exact=2):
     R, K = v.shape
     delta = np.broadcast_to(np.asarray(delta, F64), v.shape)
     ref = f4.dequantized(v)
-    a = np.abs(v)
-    lo_t = float(np.max(np.maximum(a - delta, 0.0), initial=0.0))
-    hi_t = float(np.max(a + delta, initial=0.0))
+    lo_t = hi_t = 0.0
+    rows = max(1, (1 << 20) // max(K, 1))  # rows per pass (keeps numpy's temporaries in cache)
+    for r0 in range(0, R, rows):
+        a = np.abs(v[r0:r0 + rows])
+        lo_t = max(lo_t, float(np.max(np.maximum(a - delta[r0:r0 + rows], 0.0), initial=0.0)))
+        hi_t = max(hi_t, float(np.max(a + delta[r0:r0 + rows], initial=0.0)))
     st_lo, st_hi = f4.tensor_scale(np.array([[lo_t]])), f4.tensor_scale(np.array([[hi_t]]))
     ts_cands = [st_lo]
     while ts_cands[-1] < st_hi:
         ts_cands.append(ts_cands[-1] * 2.0)
     nb = K // 16
-    ab = a.reshape(R, nb, 16)
-    db = delta.reshape(R, nb, 16)
-    lo_b = np.max(np.maximum(ab - db, 0.0), axis=-1)
-    hi_b = np.max(ab + db, axis=-1)
-    ends = [(v - delta).reshape(R, nb, 16), (v + delta).reshape(R, nb, 16)]
-    ref_b = ref.reshape(R, nb, 16)
-    bound = np.zeros((R, nb, 16))
-    wide = np.zeros((R, nb), dtype=bool)
-    den_lo = np.full((R, nb), np.inf)
-    den_hi = np.zeros((R, nb))
-    for st in ts_cands:
-        i_lo = np.searchsorted(E4M3_GRID, g8.round_to_e4m3(lo_b / (6.0 * st)))
-        i_hi = np.searchsorted(E4M3_GRID, g8.round_to_e4m3(hi_b / (6.0 * st)))
-        wide |= (i_hi - i_lo) > max_exact
-        den_lo = np.minimum(den_lo, E4M3_GRID[i_lo] * st)
-        den_hi = np.maximum(den_hi, E4M3_GRID[i_hi] * st)
-        n_c = i_hi - i_lo
-        for k in range(min(int(np.max(n_c)), max_exact) + 1):
-            sel = None if k == 0 else n_c >= k  # grid value k above the lowest, where admissible
-            sb = E4M3_GRID[i_lo + k if sel is None else i_lo[sel] + k][..., None]
-            den = sb * st
-            for s in ends:
-                s_k = s if sel is None else s[sel]
-                q = np.where(den > 0, f4.round_to_e2m1(s_k / np.where(den > 0, den, 1.0)), 0.0) * den
-                if sel is None:
-                    bound = np.maximum(bound, np.abs(q - ref_b))
-                else:
-                    bound[sel] = np.maximum(bound[sel], np.abs(q - ref_b[sel]))
-    if np.any(wide):
-        sabs = ab[wide] + db[wide]  # largest |s| per element of the wide blocks
-        dl, dh = den_lo[wide][:, None], den_hi[wide][:, None]
-        cast_err = np.maximum(dh, sabs - 6.0 * dl)
-        cast_err = np.where(dl > 0, cast_err, np.maximum(cast_err, sabs))
-        bound[wide] = cast_err + np.abs(v.reshape(R, nb, 16)[wide] - ref_b[wide]) + db[wide]
-    return ref, bound.reshape(R, K)
+    bound = np.zeros((R, K))
+    for r0 in range(0, R, rows):  # rows are independent once the tensor scales are fixed
+        vr, dr = v[r0:r0 + rows], delta[r0:r0 + rows]
+        n = vr.shape[0]
+        ab = np.abs(vr).reshape(n, nb, 16)
+        db = dr.reshape(n, nb, 16)
+        lo_b = np.max(np.maximum(ab - db, 0.0), axis=-1)
+        hi_b = np.max(ab + db, axis=-1)
+        ends = [(vr - dr).reshape(n, nb, 16), (vr + dr).reshape(n, nb, 16)]
+        ref_b = ref[r0:r0 + rows].reshape(n, nb, 16)
+        bd = np.zeros((n, nb, 16))
+        wide = np.zeros((n, nb), dtype=bool)
+        den_lo = np.full((n, nb), np.inf)
+        den_hi = np.zeros((n, nb))
+        for st in ts_cands:
+            i_lo = np.searchsorted(E4M3_GRID, g8.round_to_e4m3(lo_b / (6.0 * st)))
+            i_hi = np.searchsorted(E4M3_GRID, g8.round_to_e4m3(hi_b / (6.0 * st)))
+            wide |= (i_hi - i_lo) > max_exact
+            den_lo = np.minimum(den_lo, E4M3_GRID[i_lo] * st)
+            den_hi = np.maximum(den_hi, E4M3_GRID[i_hi] * st)
+            n_c = i_hi - i_lo
+            for k in range(min(int(np.max(n_c, initial=0)), max_exact) + 1):
+                sel = None if k == 0 else n_c >= k  # grid value k above the lowest, where admissible
+                sb = E4M3_GRID[i_lo + k if sel is None else i_lo[sel] + k][..., None]
+                den = sb * st
+                for s in ends:
+                    s_k = s if sel is None else s[sel]
+                    q = np.where(den > 0, f4.round_to_e2m1(s_k / np.where(den > 0, den, 1.0)), 0.0) * den
+                    if sel is None:
+                        bd = np.maximum(bd, np.abs(q - ref_b))
+                    else:
+                        bd[sel] = np.maximum(bd[sel], np.abs(q - ref_b[sel]))
+        if np.any(wide):
+            sabs = ab[wide] + db[wide]  # largest |s| per element of the wide blocks
+            dl, dh = den_lo[wide][:, None], den_hi[wide][:, None]
+            cast_err = np.maximum(dh, sabs - 6.0 * dl)
+            cast_err = np.where(dl > 0, cast_err, np.maximum(cast_err, sabs))
+            bd[wide] = cast_err + np.abs(vr.reshape(n, nb, 16)[wide] - ref_b[wide]) + db[wide]
+        bound[r0:r0 + rows] = bd.reshape(n, K)
+    return ref, bound
