@@ -35,6 +35,16 @@ __device__ __forceinline__ void store8<float>(float* p, const float (&v)[8]) {
 
 constexpr int NM_WARPS = 16;
 
+// Shared-memory order of the per-column factors: within each 256-column chunk, the lane
+// that owns columns 8l .. 8l+7 finds the first four at 4l and the last four at 128 + 4l,
+// so that a warp's 16-byte reads of either half are 512 contiguous bytes (no bank
+// conflicts; in column order the 32-byte stride between lanes made every read two-way).
+__host__ __device__ __forceinline__ int nm_pos(int col) {
+  const int r = col & 255;
+  return (col & ~255) + ((r & 4) << 5) + ((r >> 3) << 2) + (r & 3);
+}
+__host__ __device__ __forceinline__ int nm_padded(int d) { return (d + 255) / 256 * 256; }
+
 // A row chunk of 8 values kept as loaded (packed bf16 or fp32) between the two passes.
 template <class T>
 struct Raw8;
@@ -71,17 +81,17 @@ __global__ void __launch_bounds__(NM_WARPS * 32, 1) norm_modulate_kernel(
     Fwd f, RowSrc src, const float* __restrict__ gain_w, const float* __restrict__ mod_shared,
     const float* __restrict__ mod_bias, int chunk_shift, int chunk_scale, int rows_per_cta, Tout* __restrict__ out,
     uint8_t* __restrict__ q8, float* __restrict__ dq, float* __restrict__ rowamax) {
-  extern __shared__ float nm_smem[];  // [2 sets][A | S][d]
+  extern __shared__ float nm_smem[];  // [2 sets][A | S][dp], in nm_pos order
   __shared__ int set_b[2];
   __shared__ float red[NM_WARPS];
   __shared__ float tensor_scale;
-  const int d = f.d;
+  const int d = f.d, dp = nm_padded(d);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r0 = blockIdx.x * rows_per_cta;
   const int r1 = min(r0 + rows_per_cta, f.T);
   auto fill = [&](int set, int b) {  // A, S of batch element b into set (all threads)
-    float* A = nm_smem + set * 2 * d;
-    float* S = A + d;
+    float* A = nm_smem + set * 2 * dp;
+    float* S = A + dp;
     const float* sc_s = mod_shared + (static_cast<size_t>(b) * 6 + chunk_scale) * d;
     const float* sh_s = mod_shared + (static_cast<size_t>(b) * 6 + chunk_shift) * d;
     const float* sc_b = mod_bias + static_cast<size_t>(chunk_scale) * d;
@@ -103,8 +113,8 @@ __global__ void __launch_bounds__(NM_WARPS * 32, 1) norm_modulate_kernel(
       for (int k = 0; k < 4; ++k) {
         const int c = c0 + k * blockDim.x;
         if (c < d) {
-          A[c] = (1.0f + g[k]) * (1.0f + (ss_[k] + sb_[k]));
-          S[c] = hs[k] + hb[k];
+          A[nm_pos(c)] = (1.0f + g[k]) * (1.0f + (ss_[k] + sb_[k]));
+          S[nm_pos(c)] = hs[k] + hb[k];
         }
       }
     }
@@ -165,14 +175,15 @@ __global__ void __launch_bounds__(NM_WARPS * 32, 1) norm_modulate_kernel(
     const float ss = warp_sum((ss4[0] + ss4[1]) + (ss4[2] + ss4[3]));
     const float rstd = 1.0f / sqrtf(ss / static_cast<float>(d) + f.eps);
     const bool in_sets = b == set_b[0] || b == set_b[1];  // false only when L < 8 (a group spans 3+ batch elements)
-    const float* A = nm_smem + (b == set_b[0] ? 0 : 2 * d);
-    const float* S = A + d;
+    const float* A = nm_smem + (b == set_b[0] ? 0 : 2 * dp);
+    const float* S = A + dp;
     // the 8 outputs of chunk c (columns col .. col+7) in fp32
     auto chunk_out = [&](int c, int col, float (&o)[8]) {
       float av[8], sv[8];
       if (in_sets) {
-        const float4 a0 = *reinterpret_cast<const float4*>(A + col), a1 = *reinterpret_cast<const float4*>(A + col + 4);
-        const float4 s0 = *reinterpret_cast<const float4*>(S + col), s1 = *reinterpret_cast<const float4*>(S + col + 4);
+        const int p = nm_pos(col);  // columns col .. col+3 at p, col+4 .. col+7 at p + 128
+        const float4 a0 = *reinterpret_cast<const float4*>(A + p), a1 = *reinterpret_cast<const float4*>(A + p + 128);
+        const float4 s0 = *reinterpret_cast<const float4*>(S + p), s1 = *reinterpret_cast<const float4*>(S + p + 128);
         av[0] = a0.x; av[1] = a0.y; av[2] = a0.z; av[3] = a0.w; av[4] = a1.x; av[5] = a1.y; av[6] = a1.z; av[7] = a1.w;
         sv[0] = s0.x; sv[1] = s0.y; sv[2] = s0.z; sv[3] = s0.w; sv[4] = s1.x; sv[5] = s1.y; sv[6] = s1.z; sv[7] = s1.w;
       } else {
@@ -253,7 +264,7 @@ __global__ void __launch_bounds__(NM_WARPS * 32, 1) norm_modulate_kernel(
 template <class Tin, class Tout, int NV, int QM>
 cudaError_t launch_nm(const Fwd& f, RowSrc src, const float* gain_w, const float* mod_shared, const float* mod_bias,
                       int chunk_shift, int chunk_scale, Tout* out, const NormQOut& q, int num_sms, cudaStream_t st) {
-  const size_t smem = static_cast<size_t>(4) * f.d * sizeof(float);  // limit set by norm_init
+  const size_t smem = static_cast<size_t>(4) * nm_padded(f.d) * sizeof(float);  // limit set by norm_init
   const int ctas = num_sms;  // one CTA (16 warps) per SM: the parameter fill is paid once per SM
   int rows = (f.T + ctas - 1) / ctas;
   rows = (rows + NM_WARPS - 1) / NM_WARPS * NM_WARPS;
@@ -267,7 +278,7 @@ cudaError_t launch_nm(const Fwd& f, RowSrc src, const float* gain_w, const float
 template <class Tin, class Tout, int NV, int QM>
 cudaError_t init_nm(int d) {
   return cudaFuncSetAttribute(norm_modulate_kernel<Tin, Tout, NV, QM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              4 * d * static_cast<int>(sizeof(float)));
+                              4 * nm_padded(d) * static_cast<int>(sizeof(float)));
 }
 
 // The e4m3 output modes exist for bf16 outputs and rows of up to NM_Q_MAX_NV * 256 columns.
