@@ -114,7 +114,22 @@ def _e4m3_grid() -> np.ndarray:
 E4M3_GRID = _e4m3_grid()
 
 
-def nvfp4_change_bound(v, delta, max_exact=2):
+def magnitude_range(v, delta):
+    """(max(|v| - delta, 0), max(|v| + delta)) over the whole array: the range of the
+    largest magnitude of any v' with |v' - v| <= delta."""
+    v = np.asarray(v, F64)
+    delta = np.broadcast_to(np.asarray(delta, F64), v.shape)
+    lo_t = hi_t = 0.0
+    flat_v, flat_d = v.reshape(-1), delta.reshape(-1)
+    for i in range(0, flat_v.size, 1 << 20):
+        a = np.abs(flat_v[i:i + (1 << 20)])
+        dd = flat_d[i:i + (1 << 20)]
+        lo_t = max(lo_t, float(np.max(np.maximum(a - dd, 0.0), initial=0.0)))
+        hi_t = max(hi_t, float(np.max(a + dd, initial=0.0)))
+    return lo_t, hi_t
+
+
+def nvfp4_change_bound(v, delta, max_exact=2, tensor_range=None, s_t=None):
     """The oracle's NVFP4 cast of v [R, K] (``oracle.nvfp4``) and a bound on how far the cast
     of any v' with |v' - v| <= delta (elementwise) can land from it.
 
@@ -129,19 +144,23 @@ def nvfp4_change_bound(v, delta, max_exact=2):
     whole tensor per grid value): for a scale product den in [den_lo, den_hi] the cast of s
     lies within den_hi of s while |s| <= 6 den (half the widest E2M1 spacing, 2, times den),
     within |s| - 6 den_lo of it beyond, and is 0 where den can be 0; s itself lies within
-    |v - ref| + delta of the oracle's cast."""
+    |v - ref| + delta of the oracle's cast.
+
+    For rows sampled from a larger tensor, ``s_t`` is the oracle's tensor scale of the
+    whole tensor (the reference cast uses it) and ``tensor_range`` = (lo, hi) the range of
+    the whole tensor's largest magnitude (``magnitude_range`` over all of its rows)."""
     from oracle import nvfp4 as f4
 
     v = np.asarray(v, F64)
     R, K = v.shape
     delta = np.broadcast_to(np.asarray(delta, F64), v.shape)
-    ref = f4.dequantized(v)
-    lo_t = hi_t = 0.0
+    if s_t is None:
+        ref = f4.dequantized(v)
+    else:
+        q_, sb_, _ = f4.quantize(v, s_t=s_t)
+        ref = q_ * np.repeat(sb_, 16, axis=-1) * s_t
     rows = max(1, (1 << 20) // max(K, 1))  # rows per pass (keeps numpy's temporaries in cache)
-    for r0 in range(0, R, rows):
-        a = np.abs(v[r0:r0 + rows])
-        lo_t = max(lo_t, float(np.max(np.maximum(a - delta[r0:r0 + rows], 0.0), initial=0.0)))
-        hi_t = max(hi_t, float(np.max(a + delta[r0:r0 + rows], initial=0.0)))
+    lo_t, hi_t = magnitude_range(v, delta) if tensor_range is None else (float(t) for t in tensor_range)
     st_lo, st_hi = f4.tensor_scale(np.array([[lo_t]])), f4.tensor_scale(np.array([[hi_t]]))
     ts_cands = [st_lo]
     while ts_cands[-1] < st_hi:

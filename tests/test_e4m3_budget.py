@@ -142,3 +142,19 @@ def test_nvfp4_bound_with_wide_scale_ranges():
             if trial % 3 == 0:
                 t = np.sign(t)
             assert np.all(np.abs(f4.dequantized(v + t * delta) - ref) <= bound + 1e-12)
+
+
+def test_nvfp4_bound_on_sampled_rows_matches_the_whole_tensor():
+    """With the whole tensor's scale and magnitude range passed in, the cast and the bound of
+    sampled rows are those rows of the whole tensor's."""
+    from e4m3_budget import magnitude_range
+    from oracle import nvfp4 as f4
+    rng = np.random.default_rng(6)
+    v = round_to_bf16(rng.normal(size=(64, 128)) * np.exp(rng.normal(size=(64, 1))))
+    delta = 2 * bf16_ulp(v) + 0.02 * np.abs(v)
+    ref, bound = nvfp4_change_bound(v, delta)
+    rows = np.array([0, 5, 17, 40, 63])
+    ref_s, bound_s = nvfp4_change_bound(v[rows], delta[rows], tensor_range=magnitude_range(v, delta),
+                                        s_t=f4.tensor_scale(v))
+    np.testing.assert_array_equal(ref_s, ref[rows])
+    np.testing.assert_array_equal(bound_s, bound[rows])
