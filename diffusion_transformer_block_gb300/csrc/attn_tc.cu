@@ -22,7 +22,8 @@
 // projection stored it (so no exponential is left here). The softmax warps read O_t into
 // registers and hand it back (the next unit's first P V may overwrite it); the gate tile
 // arrives by TMA in a ring slot after the unit's last V, each thread overwrites its row
-// of it with the gated output, and every warp TMA-stores its 32 rows.
+// of it with the gated output, and every warp TMA-stores its 32 rows. The slot goes back
+// to the loader once that store has read it, checked after the next unit's first softmax.
 //
 // Persistent: one CTA per SM walks the units u = blockIdx.x, + gridDim.x, ... with one
 // TMEM allocation and one set of barriers, and every barrier phase is counted across
@@ -346,12 +347,25 @@ __global__ void __maxnreg__(168)
     const uint32_t tO = tmem + lane_off + 256 + t * 128;
     int n0 = 0;        // ring index of the current unit's K_0
     int uq = 0;        // units of this tile so far (o_done phases)
+    // Ring slot of this warp's last output store. It is released (the store has read it)
+    // only after the next unit's first P is written, so that the store's completion does
+    // not sit between a unit's epilogue and the next unit's first softmax.
+    int pend = -1;
+    auto release_pend = [&]() {
+      if (pend < 0) return;
+      if (lane == 0) {
+        bulk_wait_read_all();
+        mbar_arrive(&kv_empty[pend]);
+      }
+      pend = -1;
+    };
     uint32_t sp = 0;   // s_full phases consumed
     bool ok = true;
     for (int u = blockIdx.x; ok && u < a.units; u += gridDim.x) {
       const Unit w = unit_of(a, u);
       const int nl = 2 * nkt + w.nt;
       if (t >= w.nt) {
+        release_pend();
         n0 += nl;
         continue;
       }
@@ -422,6 +436,7 @@ __global__ void __maxnreg__(168)
         tmem_st_wait();   // P (and any O rescale) written
         tc_fence_before();
         mbar_arrive(&p_full[t]);
+        release_pend();
       }
       if (!ok) break;
       // ---- epilogue: O_t / l * s -> og (s: the stored gate). O_t is handed back once it is all in
@@ -498,9 +513,8 @@ __global__ void __maxnreg__(168)
             tma_store_3d(&tm_og, buf + kh * HALF_BYTES + quad * 32 * 128, head * HD + kh * 64, r0, w.b);
           bulk_commit();
         }
-        bulk_wait_read_all();         // the store has read this warp's rows of the slot
-        mbar_arrive(&kv_empty[gsl]);  // one of the slot's 4 arrivals
       }
+      pend = gsl;
       // bf16 rounding is monotone, so the largest stored magnitude is the rounded largest
       if (a.lse && valid) a.lse[(static_cast<size_t>(w.b) * a.n_q + head) * a.Lp + ql] = m_run + log2f(l_run);
       if (a.rowamax && valid)
@@ -508,6 +522,7 @@ __global__ void __maxnreg__(168)
       ++uq;
       n0 += nl;
     }
+    release_pend();
     // this warp's output stores have completed before exit
     if (lane == 0) bulk_wait_all();
     __syncwarp();
