@@ -121,6 +121,38 @@ __device__ __forceinline__ float deq_row(const Deq& dq, int row, bool ok) {
 // apply(): called by one epilogue warp for its 32 rows (one per lane) and one 128-column
 // half of the 256-column accumulator. `taddr` = TMEM address of the lane's row at
 // accumulator column 0. TMEM loads are warp-collective; stores are masked by row < M.
+//
+// The QKV+G, residual and SwiGLU epilogues read their warp's 128 accumulator columns
+// through a source, in their own logical order (logical columns [0, 64) at lo, [64, 128)
+// at hi): TmemAcc loads each 32-column chunk from tensor memory when it is needed (chunk
+// loops rolled); RegAcc reads the chunks from registers that the whole share was copied
+// into beforehand (chunk loops unrolled, so every register index is a constant), which
+// lets a kernel hand the accumulator back to its MMAs before the epilogue's work.
+struct TmemAcc {
+  static constexpr int kUnroll = 1;
+  uint32_t lo, hi;
+  __device__ __forceinline__ uint32_t at(int l) const { return l < 64 ? lo + l : hi + (l - 64); }
+  __device__ __forceinline__ void ld32(int l, uint32_t (&r)[32]) const { tmem_ld32(at(l), r); }
+  __device__ __forceinline__ void ld32x2(int l1, int l2, uint32_t (&r)[32], uint32_t (&q)[32]) const {
+    tmem_ld32x2(at(l1), at(l2), r, q);
+  }
+};
+struct RegAcc {
+  static constexpr int kUnroll = 4;
+  const uint32_t (&c0)[32];
+  const uint32_t (&c1)[32];
+  const uint32_t (&c2)[32];
+  const uint32_t (&c3)[32];
+  __device__ __forceinline__ void ld32(int l, uint32_t (&r)[32]) const {
+    const uint32_t(&c)[32] = l < 32 ? c0 : (l < 64 ? c1 : (l < 96 ? c2 : c3));
+#pragma unroll
+    for (int i = 0; i < 32; ++i) r[i] = c[i];
+  }
+  __device__ __forceinline__ void ld32x2(int l1, int l2, uint32_t (&r)[32], uint32_t (&q)[32]) const {
+    ld32(l1, r);
+    ld32(l2, q);
+  }
+};
 
 template <bool S8>
 struct EpiQKVGT {
@@ -129,7 +161,15 @@ struct EpiQKVGT {
   QkvgDst dst;
   int N;  // rows of W_qkvg
   Deq dq;
+  // logical columns = accumulator columns half * 128 .. + 127 (one head)
+  static __device__ __forceinline__ TmemAcc tmem_acc(uint32_t taddr, int half) {
+    return TmemAcc{taddr + half * 128, taddr + half * 128 + 64};
+  }
   __device__ __forceinline__ void apply(int row, int nb, int half, uint32_t taddr, int M) const {
+    apply_acc(row, nb, half, tmem_acc(taddr, half), M);
+  }
+  template <class A>
+  __device__ __forceinline__ void apply_acc(int row, int nb, int half, const A& acc, int M) const {
     constexpr int HD = 128;
     const int n0 = nb * BN + half * HD;
     if (n0 >= N) return;
@@ -142,15 +182,14 @@ struct EpiQKVGT {
     else { kind = 3; head = seg - f.n_q - 2 * f.n_kv; }
     const int b = ok ? row / f.L : 0;
     const int l = ok ? row - b * f.L : 0;
-    const uint32_t t0 = taddr + half * HD;
     const float fa = deq_row<S8>(dq, row, ok);
     uint32_t r[32];
 
     if (kind <= 1) {
       float ss = 0.f;
-#pragma unroll 1
+#pragma unroll(A::kUnroll)
       for (int c = 0; c < 4; ++c) {
-        tmem_ld32(t0 + c * 32, r);
+        acc.ld32(c * 32, r);
         deq32<S8>(r, dq, fa, dq.b, n0 + c * 32);
 #pragma unroll
         for (int i = 0; i < 32; ++i) ss = fmaf(u2f(r[i]), u2f(r[i]), ss);
@@ -167,9 +206,9 @@ struct EpiQKVGT {
       const int nh = kind == 0 ? f.n_q : f.n_kv;
       bf16* out = reinterpret_cast<bf16*>(kind == 0 ? dst.q : dst.k) +
                   ((static_cast<size_t>(b) * nh + head) * f.L + l) * HD;
-#pragma unroll 1
+#pragma unroll(A::kUnroll)
       for (int c = 0; c < 4; ++c) {
-        tmem_ld32(t0 + c * 32, r);
+        acc.ld32(c * 32, r);
         deq32<S8>(r, dq, fa, dq.b, n0 + c * 32);
         if (dst.raw && ok) {  // the projection before the norm, for the backward
           float4* o4 = reinterpret_cast<float4*>(dst.raw + static_cast<size_t>(row) * dst.ldr + n0 + c * 32);
@@ -202,9 +241,9 @@ struct EpiQKVGT {
       // V^T [B, n_kv, hd, Lp]: lanes hold consecutive tokens, so each channel's 32 values
       // from a warp land in one contiguous 64-byte run.
       bf16* vt = reinterpret_cast<bf16*>(dst.vt) + (static_cast<size_t>(b) * f.n_kv + head) * HD * f.Lp + l;
-#pragma unroll 1
+#pragma unroll(A::kUnroll)
       for (int c = 0; c < 4; ++c) {
-        tmem_ld32(t0 + c * 32, r);
+        acc.ld32(c * 32, r);
         deq32<S8>(r, dq, fa, dq.b, n0 + c * 32);
         if (ok) {
 #pragma unroll
@@ -213,9 +252,9 @@ struct EpiQKVGT {
       }
     } else {
       bf16* g = reinterpret_cast<bf16*>(dst.g) + static_cast<size_t>(row) * (f.n_q * HD) + head * HD;
-#pragma unroll 1
+#pragma unroll(A::kUnroll)
       for (int c = 0; c < 4; ++c) {
-        tmem_ld32(t0 + c * 32, r);
+        acc.ld32(c * 32, r);
         deq32<S8>(r, dq, fa, dq.b, n0 + c * 32);
         if (ok) {
           // the gate value sigmoid(xn W_g^T) itself: the attention epilogue and the gate
@@ -266,6 +305,18 @@ struct Res32<float> {
   }
 };
 
+// 8 consecutive residual values of one row (zeros for a row past M)
+__device__ __forceinline__ void res8(const bf16* p, bool ok, float (&o)[8]) {
+  const uint4 u = ok ? __ldg(reinterpret_cast<const uint4*>(p)) : make_uint4(0, 0, 0, 0);
+  const float2 a = unpack_bf16x2(u.x), b = unpack_bf16x2(u.y), c = unpack_bf16x2(u.z), e = unpack_bf16x2(u.w);
+  o[0] = a.x; o[1] = a.y; o[2] = b.x; o[3] = b.y; o[4] = c.x; o[5] = c.y; o[6] = e.x; o[7] = e.y;
+}
+__device__ __forceinline__ void res8(const float* p, bool ok, float (&o)[8]) {
+  const float4 a = ok ? __ldg(reinterpret_cast<const float4*>(p)) : make_float4(0.f, 0.f, 0.f, 0.f);
+  const float4 b = ok ? __ldg(reinterpret_cast<const float4*>(p) + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
+  o[0] = a.x; o[1] = a.y; o[2] = a.z; o[3] = a.w; o[4] = b.x; o[5] = b.y; o[6] = b.z; o[7] = b.w;
+}
+
 // out = res + gate * acc. The attention residual reads the bf16 block input from the
 // caller's split text/image buffers and writes the fp32 residual stream h1; the MLP
 // residual reads h1 and writes the bf16 block output. d is a multiple of 64, so a
@@ -288,8 +339,17 @@ struct EpiResid {
   float* pre = nullptr;  // optional [T, d] fp32: the product before the gate (for the backward)
   // stg: this warp's box (1024-byte aligned); tm_out: the output [T, d] with a box of 128
   // bytes x 32 rows and the 128-byte swizzle
+  // logical columns = accumulator columns half * 128 .. + 127
+  static __device__ __forceinline__ TmemAcc tmem_acc(uint32_t taddr, int half) {
+    return TmemAcc{taddr + half * 128, taddr + half * 128 + 64};
+  }
   __device__ __forceinline__ void apply(int row, int nb, int half, uint32_t taddr, int M, uint8_t* stg, int lane,
                                         const CUtensorMap* tm_out) const {
+    apply_acc(row, nb, half, tmem_acc(taddr, half), M, stg, lane, tm_out);
+  }
+  template <class A>
+  __device__ __forceinline__ void apply_acc(int row, int nb, int half, const A& acc, int M, uint8_t* stg, int lane,
+                                            const CUtensorMap* tm_out) const {
     const int N = f.d;
     const int n0 = nb * BN + half * 128;
     if (n0 >= N) return;
@@ -302,14 +362,21 @@ struct EpiResid {
     const int nc = min(4, (N - n0) >> 5);
     uint8_t* srow = stg + lane * 128;
     const int sw = lane & 7;  // the swizzle of this row: 16-byte unit j sits at j ^ sw
+    // From tensor memory the residual chunk after the current one is loaded ahead; from
+    // registers (which already hold the accumulator, and where the epilogue overlaps the
+    // next tile's products) each chunk is loaded where it is used.
+    constexpr bool kAhead = A::kUnroll == 1;
     Res32<TRes> cur, nxt;
-    if (ok) cur.load(x + n0);
+    if (ok && kAhead) cur.load(x + n0);
     uint32_t r[32];
-#pragma unroll 1
-    for (int c = 0; c < nc; ++c) {
+#pragma unroll(A::kUnroll)
+    for (int c = 0; c < (A::kUnroll == 1 ? nc : 4); ++c) {  // a constant trip count when unrolled
+      if (c < nc) {
       const int col = n0 + c * 32;
-      if (ok && c + 1 < nc) nxt.load(x + col + 32);
-      tmem_ld32(taddr + half * 128 + c * 32, r);
+      if constexpr (kAhead) {
+        if (ok && c + 1 < nc) nxt.load(x + col + 32);
+      }
+      acc.ld32(c * 32, r);
       deq32<S8>(r, dq, fa, dq.b, col);
       if (ok && pre) {
         float4* p4 = reinterpret_cast<float4*>(pre + static_cast<size_t>(row) * N + col);
@@ -325,7 +392,8 @@ struct EpiResid {
 #pragma unroll
       for (int q4 = 0; q4 < 4; ++q4) {
         float xv[8];
-        cur.get8(q4, xv);
+        if constexpr (kAhead) cur.get8(q4, xv);
+        else res8(x + col + 8 * q4, ok, xv);
         const float4 s0 = __ldg(gs4 + 2 * q4), s1 = __ldg(gs4 + 2 * q4 + 1);
         const float4 b0 = __ldg(gb4 + 2 * q4), b1 = __ldg(gb4 + 2 * q4 + 1);
         const float gt[8] = {s0.x + b0.x, s0.y + b0.y, s0.z + b0.z, s0.w + b0.w,
@@ -352,7 +420,8 @@ struct EpiResid {
           bulk_commit();
         }
       }
-      cur = nxt;
+      }
+      if constexpr (kAhead) cur = nxt;
     }
   }
 };
@@ -370,17 +439,25 @@ struct EpiSwiGLUT {
   Deq dq;
   float* pre_a = nullptr;  // optional [T, F] fp32: hn W_gate^T and hn W_up^T (for the backward)
   float* pre_u = nullptr;
-  // accumulator columns [0,128) = hn W_gate^T, [128,256) = hn W_up^T for F-columns nb*128 ..
+  // accumulator columns [0,128) = hn W_gate^T, [128,256) = hn W_up^T for F-columns nb*128 ..;
+  // logical columns: [0, 64) = gate columns half * 64 .., [64, 128) = the same columns of up
+  static __device__ __forceinline__ TmemAcc tmem_acc(uint32_t taddr, int half) {
+    return TmemAcc{taddr + half * 64, taddr + 128 + half * 64};
+  }
   __device__ __forceinline__ void apply(int row, int nb, int half, uint32_t taddr, int M) const {
+    apply_acc(row, nb, half, tmem_acc(taddr, half), M);
+  }
+  template <class A>
+  __device__ __forceinline__ void apply_acc(int row, int nb, int half, const A& acc, int M) const {
     const int f0 = nb * 128 + half * 64;
     if (f0 >= F) return;
     const bool ok = row < M;
     const float fa = deq_row<S8>(dq, row, ok);
     float amax = 0.0f;
     uint32_t rg[32], ru[32];
-#pragma unroll 1
+#pragma unroll(A::kUnroll)
     for (int c = 0; c < 2; ++c) {
-      tmem_ld32x2(taddr + half * 64 + c * 32, taddr + 128 + half * 64 + c * 32, rg, ru);
+      acc.ld32x2(c * 32, 64 + c * 32, rg, ru);
       deq32<S8>(rg, dq, fa, dq.b, f0 + c * 32);
       deq32<S8>(ru, dq, fa, dq.b2, f0 + c * 32);
       if (ok && pre_a) {
@@ -787,7 +864,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 // halves are two TMA boxes of 128 rows stacked in shared memory (so the SwiGLU GEMM's
 // W_gate and W_up rows form one 256-row operand) and their scale atoms two adjacent
 // 4-column groups in tensor memory. The accumulator is single-buffered (the scale copies take
-// tensor-memory columns 256 .. 303), so a tile's epilogue does not overlap the next
+// tensor-memory columns 256 .. 303); each epilogue warp copies its 128 columns into
+// registers and hands the accumulator back at once, so the epilogue's work overlaps the next
 // tile's main loop. Warp roles as in the bf16 kernel: 0 TMA, 1 TMEM + MMA, 2..9 epilogue.
 constexpr int F4_BM = 128, F4_BN = 256;
 constexpr int F4_A_BYTES = F4_BM * 128;
@@ -988,13 +1066,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       tc_fence_after();
       const int row = mb * F4_BM + quad * 32 + lane;
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16);
-      if constexpr (STG > 0)
-        epi.apply(row, nb, half, taddr, M, stg_base + (warp - 2) * STG, lane, &tm_c);
-      else
-        epi.apply(row, nb, half, taddr, M);
+      // this warp's 128 accumulator columns into registers, then the accumulator goes back
+      // to the MMA warp, so that the epilogue's work overlaps the next tile's products
+      uint32_t a0[32], a1[32], a2[32], a3[32];
+      const TmemAcc ta = Epi::tmem_acc(taddr, half);
+      ta.ld32x2(0, 32, a0, a1);
+      ta.ld32x2(64, 96, a2, a3);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(tempty);
+      const RegAcc ra{a0, a1, a2, a3};
+      if constexpr (STG > 0)
+        epi.apply_acc(row, nb, half, ra, M, stg_base + (warp - 2) * STG, lane, &tm_c);
+      else
+        epi.apply_acc(row, nb, half, ra, M);
       acc_phase ^= 1;
     }
     if constexpr (STG > 0) {  // this warp's TMA stores have completed
