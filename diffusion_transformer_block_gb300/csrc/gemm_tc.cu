@@ -857,16 +857,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 // One CTA per 128 x 256 output tile (no CTA pairs), persistent over the tiles. A stage
 // covers 256 elements of K (128 bytes of each operand row): A 128 x 128 B and the two
 // 128-row halves of B by TMA with the 128-byte swizzle, and the stage's scale atoms of A
-// and of both B halves by 1D bulk copies (54 KB). Per stage the MMA thread copies the
-// stage's scale atoms into tensor memory (tcgen05.cp, ordered with its MMAs) and issues
-// one kind::mxf4nvf4 MMA (M = 128, N = 256, K = 64) per 64-element step into the
-// 256-column accumulator, which has the layout the bf16 kernel's epilogues read. The B
-// halves are two TMA boxes of 128 rows stacked in shared memory (so the SwiGLU GEMM's
-// W_gate and W_up rows form one 256-row operand) and their scale atoms two adjacent
-// 4-column groups in tensor memory. The accumulator is single-buffered (the scale copies take
-// tensor-memory columns 256 .. 303); each epilogue warp copies its 128 columns into
-// registers and hands the accumulator back at once, so the epilogue's work overlaps the next
-// tile's main loop. Warp roles as in the bf16 kernel: 0 TMA, 1 TMEM + MMA, 2..9 epilogue.
+// and of both B halves by 1D bulk copies (54 KB). The scale atoms go into tensor memory
+// by tcgen05.cp, split over three threads because a copy occupies its issuing thread far
+// longer than an MMA does: two copy warps take the atoms of the two B halves, the MMA
+// thread those of A, each stage into one of two 48-column slots. The MMA thread waits for
+// the copy warps' copies, then issues one kind::mxf4nvf4 MMA (M = 128, N = 256, K = 64) per
+// 64-element step into the 256-column accumulator, which has the layout the bf16 kernel's
+// epilogues read, and frees the slot with a commit. The B halves are two TMA boxes of 128
+// rows stacked in shared memory (so the SwiGLU GEMM's W_gate and W_up rows form one 256-row
+// operand) and their scale atoms two adjacent 4-column groups in tensor memory. The
+// accumulator is single-buffered (the scale slots take tensor-memory columns 256 .. 351);
+// each epilogue warp copies its 128 columns into registers and hands the accumulator back
+// at once, so the epilogue's work overlaps the next tile's main loop. Warp roles: 0 TMA,
+// 1 TMEM + A scale copies + MMA, 2..9 epilogue, 10 and 11 B scale copies.
 constexpr int F4_BM = 128, F4_BN = 256;
 constexpr int F4_A_BYTES = F4_BM * 128;
 constexpr int F4_BH_BYTES = (F4_BN / 2) * 128;
@@ -878,13 +881,17 @@ template <class Epi>
 __host__ __device__ constexpr int f4_stages() {
   return StgOf<Epi>::value > 0 ? 3 : 4;
 }
+// Two more warps than the bf16 kernel copy the B operand's scale atoms (one warp per
+// 128-row half); 12 warps keep the 168-register cap of 10 (3 warps per SM sub-partition).
+constexpr int F4_THREADS = NUM_THREADS + 64;
+constexpr int F4_SF_SLOT = 48;  // TMEM columns of one stage's scales; two slots
 template <class Epi>
 __host__ __device__ constexpr int f4_smem_bytes() {
   return f4_stages<Epi>() * F4_STAGE + NUM_EPI_WARPS * StgOf<Epi>::value + 1024 + 256;
 }
 
 template <class Epi, bool DUAL>
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+__global__ void __launch_bounds__(F4_THREADS, 1)
     gemm_fp4_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                     const __grid_constant__ CUtensorMap tm_b2, const __grid_constant__ CUtensorMap tm_c, int M,
                     int num_n, int K, int group, int b_blocks, const uint8_t* __restrict__ sf_a,
@@ -899,7 +906,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   uint64_t* tfull = empty + NST;
   uint64_t* tempty = tfull + 1;
   uint64_t* done = tempty + 1;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+  uint64_t* sf_ready = done + 1;     // [2] the B scale copies of a slot have landed (2 arrivals)
+  uint64_t* sf_free = sf_ready + 2;  // [2] the MMAs that read a slot have finished
+  uint64_t* done_cp = sf_free + 2;   // every copy of the two copy warps has finished
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done_cp + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -916,6 +926,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     mbar_init(tfull, 1);
     mbar_init(tempty, NUM_EPI_WARPS);
     mbar_init(done, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&sf_ready[i], 2);
+      mbar_init(&sf_free[i], 1);
+    }
+    mbar_init(done_cp, 2);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -987,19 +1002,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         drain_wait(&full[i % NST], static_cast<uint32_t>((i / NST) & 1), err, SITE_GEMM_TEARDOWN);
     }
   } else if (warp == 1) {
-    // ---------------- scale copies + MMA issue. The whole warp runs the loop (waits,
+    // ---------------- A scale copies + MMA issue. The whole warp runs the loop (waits,
     // addresses and descriptors computed warp-uniformly); lane 0 issues every tcgen05
-    // instruction and commit.
+    // instruction and commit. The B scale atoms of a stage are copied by warps 10 and 11
+    // into the stage's TMEM slot (two slots of 48 columns, alternating by stage): the MMA
+    // thread waits for their copies to land and frees the slot with a commit after the
+    // stage's MMAs.
     constexpr uint32_t idesc = idesc_nvf4_f32(F4_BM, F4_BN);
     int stage = 0;
     uint32_t phase = 0;
+    int slot = 0;
+    uint32_t slot_phase = 0;
     uint32_t acc_phase = 0;
     bool ok = true;
     for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
       if (!__all_sync(0xffffffffu, mbar_wait(tempty, acc_phase ^ 1, wc, SITE_GEMM_MMA))) break;
       tc_fence_after();
       for (int kb = 0; kb < num_kb; ++kb) {
-        if (!__all_sync(0xffffffffu, mbar_wait(&full[stage], phase, wc, SITE_GEMM_MMA))) {
+        if (!__all_sync(0xffffffffu, mbar_wait(&full[stage], phase, wc, SITE_GEMM_MMA)) ||
+            !__all_sync(0xffffffffu, mbar_wait(&sf_ready[slot], slot_phase, wc, SITE_GEMM_MMA))) {
           ok = false;
           break;
         }
@@ -1007,40 +1028,37 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const uint32_t sa = smem_u32(smem + stage * F4_STAGE);
         const uint32_t sb = sa + F4_A_BYTES;
         const uint32_t ssf = sb + 2 * F4_BH_BYTES;
-        const uint32_t t_sf0 = tmem_base + F4_SF_TMEM;
+        const uint32_t t_sf0 = tmem_base + F4_SF_TMEM + slot * F4_SF_SLOT;
         const uint32_t acc = (kb != 0) ? 1u : 0u;
-        // the stage's scale atoms first (TMEM columns: A, then the 256 B rows, per step),
-        // then one M = 128, N = 256 MMA per 64-element step; B row n (0 .. 255) takes its
-        // scales from column t_sf + 4 + n / 32: the two halves' atoms sit side by side
+        // per 64-element step: A's scale atom (TMEM columns +0..3 of the step's group of
+        // 12), then one M = 128, N = 256 MMA; B row n (0 .. 255) takes its scales from
+        // column +4 + n / 32 of the group, where the copy warps put the two halves' atoms
         if (lane == 0) {
           if (4 * kb + 4 <= KS) {
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              tmem_cp_scales(t_sf0 + k * 12, sdesc_rows16(ssf + k * F4_ATOM));
-              tmem_cp_scales(t_sf0 + k * 12 + 4, sdesc_rows16(ssf + (4 + k) * F4_ATOM));
-              tmem_cp_scales(t_sf0 + k * 12 + 8, sdesc_rows16(ssf + (8 + k) * F4_ATOM));
-            }
+            for (int k = 0; k < 4; ++k) tmem_cp_scales(t_sf0 + k * 12, sdesc_rows16(ssf + k * F4_ATOM));
 #pragma unroll
             for (int k = 0; k < 4; ++k)  // 64 elements = 32 bytes of each row per step
               mma_nvf4(tmem_base, sdesc_kmajor_sw128(sa + k * 32), sdesc_kmajor_sw128(sb + k * 32), idesc,
                        t_sf0 + k * 12, t_sf0 + k * 12 + 4, (acc | k) != 0 ? 1u : 0u);
           } else {  // a last stage of fewer than four steps
             const int nks = KS - 4 * kb;
-            for (int k = 0; k < nks; ++k) {
-              tmem_cp_scales(t_sf0 + k * 12, sdesc_rows16(ssf + k * F4_ATOM));
-              tmem_cp_scales(t_sf0 + k * 12 + 4, sdesc_rows16(ssf + (4 + k) * F4_ATOM));
-              tmem_cp_scales(t_sf0 + k * 12 + 8, sdesc_rows16(ssf + (8 + k) * F4_ATOM));
-            }
+            for (int k = 0; k < nks; ++k) tmem_cp_scales(t_sf0 + k * 12, sdesc_rows16(ssf + k * F4_ATOM));
             for (int k = 0; k < nks; ++k)
               mma_nvf4(tmem_base, sdesc_kmajor_sw128(sa + k * 32), sdesc_kmajor_sw128(sb + k * 32), idesc,
                        t_sf0 + k * 12, t_sf0 + k * 12 + 4, (acc | k) != 0 ? 1u : 0u);
           }
-          mma_commit(&empty[stage]);  // frees the stage once these MMAs have read it
+          mma_commit(&empty[stage]);    // frees the stage once these MMAs (and copies) have read it
+          mma_commit(&sf_free[slot]);   // and the scale slot once the MMAs have read it
         }
         __syncwarp();
         if (++stage == NST) {
           stage = 0;
           phase ^= 1;
+        }
+        if (++slot == 2) {
+          slot = 0;
+          slot_phase ^= 1;
         }
       }
       if (!ok) break;
@@ -1051,6 +1069,53 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (lane == 0) {
       mma_commit(done);  // completes when every MMA and copy issued above has finished
       drain_wait(done, 0, err, SITE_GEMM_TEARDOWN);
+    }
+    __syncwarp();
+  } else if (warp >= 2 + NUM_EPI_WARPS) {
+    // ---------------- B scale copies: warp 10 the atoms of B rows 0..127, warp 11 of rows
+    // 128..255, into TMEM columns +4..7 / +8..11 of each step's group in the stage's slot.
+    const int bh = warp - (2 + NUM_EPI_WARPS);
+    int stage = 0;
+    uint32_t phase = 0;
+    int slot = 0;
+    uint32_t slot_phase = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+      for (int kb = 0; kb < num_kb; ++kb) {
+        if (!__all_sync(0xffffffffu, mbar_wait(&full[stage], phase, wc, SITE_GEMM_MMA)) ||
+            !__all_sync(0xffffffffu, mbar_wait(&sf_free[slot], slot_phase ^ 1, wc, SITE_GEMM_MMA))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t ssf = smem_u32(smem + stage * F4_STAGE) + F4_A_BYTES + 2 * F4_BH_BYTES;
+        const uint32_t t_sf0 = tmem_base + F4_SF_TMEM + slot * F4_SF_SLOT + 4 + 4 * bh;
+        if (lane == 0) {
+          if (4 * kb + 4 <= KS) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              tmem_cp_scales(t_sf0 + k * 12, sdesc_rows16(ssf + (4 + 4 * bh + k) * F4_ATOM));
+          } else {
+            const int nks = KS - 4 * kb;
+            for (int k = 0; k < nks; ++k)
+              tmem_cp_scales(t_sf0 + k * 12, sdesc_rows16(ssf + (4 + 4 * bh + k) * F4_ATOM));
+          }
+          mma_commit(&sf_ready[slot]);  // one of the slot's two arrivals, when the copies land
+        }
+        __syncwarp();
+        if (++stage == NST) {
+          stage = 0;
+          phase ^= 1;
+        }
+        if (++slot == 2) {
+          slot = 0;
+          slot_phase ^= 1;
+        }
+      }
+    }
+    if (lane == 0) {
+      mma_commit(done_cp);  // completes when every copy issued above has finished
+      drain_wait(done_cp, 0, err, SITE_GEMM_TEARDOWN);
     }
     __syncwarp();
   } else {
@@ -1119,7 +1184,7 @@ cudaError_t launch_fp4(const CUtensorMap* a, const CUtensorMap* b, const CUtenso
   const int group = (b_all <= a_all && b_all <= (80ll << 20)) ? 1 : 16;
   const int grid = tiles < num_sms ? tiles : num_sms;  // persistent: one CTA per SM
   const int b_blocks = (N + 127) / 128;  // 128-row scale blocks of B (of W_gate / W_up for the SwiGLU GEMM)
-  gemm_fp4_kernel<Epi, DUAL><<<grid, NUM_THREADS, f4_smem_bytes<Epi>(), st>>>(
+  gemm_fp4_kernel<Epi, DUAL><<<grid, F4_THREADS, f4_smem_bytes<Epi>(), st>>>(
       *a, *b, *b2, c ? *c : *a, M, num_n, K, group, b_blocks, sf_a, sf_b, DUAL ? sf_b2 : sf_b, epi, err);
   return cudaGetLastError();
 }
